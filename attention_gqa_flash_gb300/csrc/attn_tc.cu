@@ -1,0 +1,806 @@
+// attn_tc.cu -- masked GQA flash attention on the 5th-generation tensor
+// cores (tcgen05), used for prefill and for the speculative-verify attention.
+//
+// What it computes (mlx-native 0.18.0 src/ops/flash_attn_prefill_tensor.rs,
+// module doc): O = softmax(scale * Q K^T + mask) V with one KV head per
+// n_heads / n_kv_heads query heads and an additive f16 (or bf16) mask; a
+// query row whose mask hides every key yields zeros.
+//
+// Kernel structure (one CTA = one 128-row query tile, 192 threads):
+//   warps 0-3  softmax: each thread owns one query row = one TMEM lane.  It
+//              stages its Q row (f32/bf16 -> f16/bf16) into shared memory,
+//              reads S from TMEM, applies scale and mask, runs the online
+//              softmax in the exp2 domain with lazy rescaling of O (only when
+//              the running max grows by more than 2^8), writes P to shared
+//              memory, and finally normalises O out of TMEM into global memory.
+//   warp 4     TMA producer: streams K and V tiles (128-byte swizzled) through
+//              a ring of 32 KiB stages guarded by full/empty mbarriers.
+//   warp 5     MMA issuer: owns the TMEM allocation; S = Q K^T into one of two
+//              TMEM buffers (so QK^T of the next tile overlaps the softmax of
+//              this one), then O += P V into the TMEM accumulator.
+// Tiles of keys whose mask is entirely -inf are skipped (a classification
+// pre-pass reads the mask once, 64 keys at a time); tiles whose mask is
+// entirely zero do not read the mask at all.
+// head_dim 512 keeps a 128x512 f32 accumulator out of reach of the 512 TMEM
+// columns, so each query tile is processed as two units, one per 256-wide
+// half of the output, both recomputing S.
+// Few tiles (verify) are split along the keys; partial results carry a
+// log2-sum-exp and are merged by a combine kernel.
+// Every mbarrier wait is bounded (2 s); on expiry the CTA raises
+// GQA_FLAG_TIMEOUT, unwinds, frees its TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int BM = 128;
+constexpr int kThreads = 192;
+constexpr int kStageBytes = 32768;
+constexpr float kNegInf = -INFINITY;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+template <int D>
+struct Cfg;
+template <>
+struct Cfg<128> {
+    static constexpr int BN = 128, DS = 128, DO = 128, KSUB = 1, STAGES = 5;
+};
+template <>
+struct Cfg<256> {
+    static constexpr int BN = 64, DS = 256, DO = 256, KSUB = 1, STAGES = 4;
+};
+template <>
+struct Cfg<512> {
+    static constexpr int BN = 64, DS = 256, DO = 256, KSUB = 2, STAGES = 2;
+};
+
+// shared-memory carve-up (offsets from a 1024-byte aligned base)
+template <int D>
+struct Layout {
+    using C = Cfg<D>;
+    static constexpr int kQ = 0;                          // D/64 tiles of [128][64]
+    static constexpr int kP = kQ + BM * D * 2;            // BN/64 tiles of [128][64]
+    static constexpr int kStages = kP + BM * C::BN * 2;   // STAGES x 32 KiB
+    static constexpr int kBars = kStages + C::STAGES * kStageBytes;
+    // barriers: full[S], empty[S], q_full, s_full[2], p_full, o_done, mma_fin
+    static constexpr int kNumBars = 2 * C::STAGES + 6;
+    static constexpr int kTmemSlot = kBars + kNumBars * 8;
+    static constexpr int kAbort = kTmemSlot + 4;
+    static constexpr int kEnd = kAbort + 4;
+    static constexpr int kBytes = kEnd + 1024;  // + alignment slack
+};
+
+struct AttnArgs {
+    const void *q;
+    int q_f32;
+    int64_t q_row, q_head, q_lane;
+    int kv_bf16;
+    const uint16_t *mask;
+    int mask_bf16;
+    int64_t m_row, m_head, m_lane;
+    float *o;
+    int64_t o_row, o_head, o_lane;
+    int lanes, rows, n_heads, n_kv_heads, group, n_keys;
+    int rows_per_head, heads_per_tile, row_tiles, head_tiles;
+    int n_blk;  // key tiles of BN
+    int splits, blk_per_split, d_parts;
+    float scale_log2;
+    const uint8_t *codes;  // [code groups][code_cols] per 64 keys: 0 skip, 1 no mask, 2 mixed
+    int code_cols;
+    int shared_mask;  // mask identical for all heads: code group = (lane, row tile)
+    float *ws_o;      // split partials [unit][BM][DO]
+    float *ws_lse;    // [unit][BM]
+    int32_t *status;
+};
+
+struct Tile {
+    int lane, kh, ht, rt;
+};
+
+__device__ __forceinline__ Tile tile_of(const AttnArgs &a, int tile_id) {
+    Tile t;
+    t.ht = tile_id % a.head_tiles;
+    tile_id /= a.head_tiles;
+    t.kh = tile_id % a.n_kv_heads;
+    tile_id /= a.n_kv_heads;
+    t.lane = tile_id % a.lanes;
+    t.rt = tile_id / a.lanes;
+    return t;
+}
+
+// (head, row) of tile row i; false when the tile row carries no query
+__device__ __forceinline__ bool row_of(const AttnArgs &a, const Tile &t, int i, int &head,
+                                       int &row) {
+    const int hi = i / a.rows_per_head;
+    const int ri = i - hi * a.rows_per_head;
+    const int hg = t.ht * a.heads_per_tile + hi;
+    row = t.rt * a.rows_per_head + ri;
+    head = t.kh * a.group + hg;
+    return hi < a.heads_per_tile && hg < a.group && row < a.rows;
+}
+
+__device__ __forceinline__ int code_group(const AttnArgs &a, const Tile &t) {
+    if (a.shared_mask) return t.lane * a.row_tiles + t.rt;
+    return ((t.lane * a.n_kv_heads + t.kh) * a.head_tiles + t.ht) * a.row_tiles + t.rt;
+}
+
+// code of key tile j (BN keys = BN/64 classification blocks)
+// (a tile that mixes skipped and mask-free blocks still has to apply the mask)
+template <int BN>
+__device__ __forceinline__ int tile_code(const AttnArgs &a, int cg, int j) {
+    int all_skip = 1, all_free = 1;
+#pragma unroll
+    for (int s = 0; s < BN / 64; ++s) {
+        const int c = j * (BN / 64) + s;
+        const int v = c < a.code_cols ? a.codes[(int64_t)cg * a.code_cols + c] : 0;
+        all_skip &= (v == 0);
+        all_free &= (v == 1);
+    }
+    return all_skip ? 0 : (all_free ? 1 : 2);
+}
+
+__device__ __forceinline__ bool is_neg_inf(uint16_t v, int bf16) {
+    return bf16 ? v == 0xff80 : v == 0xfc00;
+}
+__device__ __forceinline__ float mask_to_f32(uint16_t v, int bf16) {
+    return bf16 ? __uint_as_float((uint32_t)v << 16) : __half2float(__ushort_as_half(v));
+}
+
+// ---------------------------------------------------------------------------
+// classification pre-pass: one CTA per (code group, 64 keys), thread = tile row
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(BM) classify_kernel(const AttnArgs a, uint8_t *codes) {
+    const int cg = blockIdx.x, cb = blockIdx.y;
+    Tile t;
+    if (a.shared_mask) {
+        t.lane = cg / a.row_tiles;
+        t.rt = cg - t.lane * a.row_tiles;
+        t.kh = 0;
+        t.ht = 0;
+    } else {
+        t.rt = cg % a.row_tiles;
+        int rest = cg / a.row_tiles;
+        t.ht = rest % a.head_tiles;
+        rest /= a.head_tiles;
+        t.kh = rest % a.n_kv_heads;
+        t.lane = rest / a.n_kv_heads;
+    }
+    int head, row;
+    const bool valid = row_of(a, t, threadIdx.x, head, row);
+    int masked = 1, zero = 1;
+    if (valid) {
+        const uint16_t *m = a.mask + t.lane * a.m_lane + (int64_t)head * a.m_head +
+                            (int64_t)row * a.m_row + (int64_t)cb * 64;
+        const int ncol = min(64, a.n_keys - cb * 64);
+        if (ncol < 64) zero = 0;
+        if ((reinterpret_cast<uintptr_t>(m) & 15) == 0 && ncol == 64) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint4 x = ld_nc_v4(m + v * 8);
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint16_t lo = w[e] & 0xffff, hi = w[e] >> 16;
+                    masked &= is_neg_inf(lo, a.mask_bf16) & is_neg_inf(hi, a.mask_bf16);
+                    zero &= ((lo & 0x7fff) == 0) & ((hi & 0x7fff) == 0);
+                }
+            }
+        } else {
+            for (int c = 0; c < ncol; ++c) {
+                const uint16_t v = m[c];
+                masked &= is_neg_inf(v, a.mask_bf16);
+                zero &= (v & 0x7fff) == 0;
+            }
+        }
+    }
+    const int all_masked = __syncthreads_and(masked);
+    const int all_zero = __syncthreads_and(zero);
+    if (threadIdx.x == 0)
+        codes[(int64_t)cg * a.code_cols + cb] = all_masked ? 0 : (all_zero ? 1 : 2);
+}
+
+// Bounded mbarrier wait shared by all roles of a CTA: gives up after
+// kWaitLimitNs (raising GQA_FLAG_TIMEOUT and the CTA's abort flag) or as soon
+// as another role of the CTA has aborted.
+struct Waiter {
+    volatile int *abort;
+    int32_t *status;
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
+        if (tc::mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = tc::globaltimer_ns();
+        for (uint32_t it = 1;; ++it) {
+            if (tc::mbar_try_wait(bar, parity)) return true;
+            if ((it & 127) == 0) {
+                if (*abort) return false;
+                if (tc::globaltimer_ns() - t0 > kWaitLimitNs) {
+                    *abort = 1;
+                    raise_flag(status, GQA_FLAG_TIMEOUT);
+                    return false;
+                }
+            }
+        }
+    }
+};
+
+// byte offset of the 16-byte chunk `c16` of row `r` in a [128][64] 16-bit tile
+// written with the 128-byte swizzle
+__device__ __forceinline__ uint32_t sw128(int r, int c16) {
+    return (uint32_t)(r * 128 + ((c16 ^ (r & 7)) << 4));
+}
+
+template <int D, class KV>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
+                const __grid_constant__ CUtensorMap tmv) {
+    using C = Cfg<D>;
+    using L = Layout<D>;
+    constexpr int BN = C::BN, DS = C::DS, DO = C::DO, KSUB = C::KSUB, NS = C::STAGES;
+    constexpr bool kBf16 = KV::kind == GQA_DTYPE_BF16;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem =
+        reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+    auto full = [&](int s) { return bar(s); };
+    auto empty = [&](int s) { return bar(NS + s); };
+    const uint32_t q_full = bar(2 * NS), p_full = bar(2 * NS + 3), o_done = bar(2 * NS + 4),
+                   mma_fin = bar(2 * NS + 5);
+    auto s_full = [&](int b) { return bar(2 * NS + 1 + b); };
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlot);
+    const Waiter wt{abort_flag, a.status};
+
+    // ---- which unit: (query tile, output half, key split); heavy row tiles first
+    int idx = blockIdx.x;
+    const int split = idx % a.splits;
+    idx /= a.splits;
+    const int dpart = idx % a.d_parts;
+    idx /= a.d_parts;
+    const int per_rt = a.lanes * a.n_kv_heads * a.head_tiles;
+    const int tile_id = (a.row_tiles - 1 - idx / per_rt) * per_rt + idx % per_rt;
+    const Tile t = tile_of(a, tile_id);
+    const int cg = code_group(a, t);
+    const int jb = split * a.blk_per_split;
+    const int je = min(a.n_blk, jb + a.blk_per_split);
+    const int d_off = dpart * DO;
+    const int head_idx = t.lane * a.n_kv_heads + t.kh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            tc::mbar_init(full(s), 1);
+            tc::mbar_init(empty(s), 1);
+        }
+        tc::mbar_init(q_full, BM);
+        tc::mbar_init(s_full(0), 1);
+        tc::mbar_init(s_full(1), 1);
+        tc::mbar_init(p_full, BM);
+        tc::mbar_init(o_done, 1);
+        tc::mbar_init(mma_fin, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 5) {
+        tc::tmem_alloc<512>(smem_u32(tslot));
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t tm_o = tmem;       // O: DO columns
+    const uint32_t tm_s = tmem + DO;  // S: two buffers of BN columns
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tc::prefetch_tmap(&tmk);
+            tc::prefetch_tmap(&tmv);
+            int stage = 0;
+            uint32_t round = 0;
+            for (int j = jb; j < je && !*abort_flag; ++j) {
+                if (!tile_code<BN>(a, cg, j)) continue;
+                bool ok = true;
+                for (int ks = 0; ks <= KSUB && ok; ++ks) {
+                    if (!(ok = wt.wait(empty(stage), (round & 1) ^ 1))) break;
+                    const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
+                    tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
+                    const bool is_v = ks == KSUB;
+                    const int dc0 = is_v ? d_off / 64 : ks * (DS / 64);
+#pragma unroll
+                    for (int c = 0; c < DS / 64; ++c)
+                        tc::tma_load_3d(dst + c * (BN * 128), is_v ? (const void *)&tmv : (const void *)&tmk,
+                                        full(stage), (dc0 + c) * 64, j * BN, head_idx);
+                    if (++stage == NS) {
+                        stage = 0;
+                        ++round;
+                    }
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_qk = tc::idesc_f16(BM, BN, kBf16, false);
+            const uint32_t id_pv = tc::idesc_f16(BM, DO, kBf16, true);
+            int stage = 0;
+            uint32_t round = 0;
+            int n_s = 0;  // S tiles issued
+            auto next_vis = [&](int j) {
+                while (j < je && !tile_code<BN>(a, cg, j)) ++j;
+                return j;
+            };
+            // S(n_s) = Q K^T into buffer n_s & 1
+            auto issue_s = [&]() -> bool {
+                const uint32_t d_tm = tm_s + (uint32_t)(n_s & 1) * BN;
+                for (int ks = 0; ks < KSUB; ++ks) {
+                    if (!wt.wait(full(stage), round & 1)) return false;
+                    tc::tc_fence_after();
+                    const uint32_t kb = sbase + L::kStages + stage * kStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < DS / 16; ++kk) {
+                        const int dq = ks * DS + kk * 16;
+                        const uint64_t da = tc::smem_desc_sw128(
+                            sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16, 1024);
+                        const uint64_t db = tc::smem_desc_sw128(
+                            kb + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
+                        tc::mma_f16_ss(d_tm, da, db, id_qk, (ks | kk) != 0);
+                    }
+                    tc::mma_commit(empty(stage));
+                    if (++stage == NS) {
+                        stage = 0;
+                        ++round;
+                    }
+                }
+                tc::mma_commit(s_full(n_s & 1));
+                ++n_s;
+                return true;
+            };
+            bool ok = wt.wait(q_full, 0);
+            tc::tc_fence_after();
+            int js = next_vis(jb);
+            if (ok && js < je) {
+                ok = issue_s();
+                js = next_vis(js + 1);
+            }
+            for (int i = 0; ok && i < n_s; ++i) {
+                if (js < je) {
+                    if (!(ok = issue_s())) break;
+                    js = next_vis(js + 1);
+                }
+                if (!(ok = wt.wait(p_full, i & 1))) break;
+                tc::tc_fence_after();
+                if (!(ok = wt.wait(full(stage), round & 1))) break;
+                tc::tc_fence_after();
+                const uint32_t vb = sbase + L::kStages + stage * kStageBytes;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t da = tc::smem_desc_sw128(
+                        sbase + L::kP + (kk / 4) * (BM * 128) + (kk % 4) * 32, 16, 1024);
+                    const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
+                    tc::mma_f16_ss(tm_o, da, db, id_pv, (i | kk) != 0);
+                }
+                tc::mma_commit(empty(stage));
+                if (++stage == NS) {
+                    stage = 0;
+                    ++round;
+                }
+                tc::mma_commit(o_done);
+            }
+            // every MMA of this thread has finished before TMEM can be released
+            tc::mma_commit(mma_fin);
+            wt.wait(mma_fin, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int r = threadIdx.x;  // tile row == TMEM lane
+        int head = 0, row = 0;
+        const bool valid = row_of(a, t, r, head, row);
+        {
+            uint8_t *qs = smem + L::kQ;
+            if (valid && a.q_f32) {
+                const float *src = static_cast<const float *>(a.q) + t.lane * a.q_lane +
+                                   (int64_t)head * a.q_head + (int64_t)row * a.q_row;
+#pragma unroll 4
+                for (int c8 = 0; c8 < D / 8; ++c8) {
+                    const float4 x = ld_nc_f4(src + c8 * 8), y = ld_nc_f4(src + c8 * 8 + 4);
+                    const uint4 v = make_uint4(pack2(KV{}, x.x, x.y), pack2(KV{}, x.z, x.w),
+                                               pack2(KV{}, y.x, y.y), pack2(KV{}, y.z, y.w));
+                    *reinterpret_cast<uint4 *>(qs + (c8 / 8) * (BM * 128) + sw128(r, c8 % 8)) = v;
+                }
+            } else if (valid) {
+                const uint16_t *src = static_cast<const uint16_t *>(a.q) + t.lane * a.q_lane +
+                                      (int64_t)head * a.q_head + (int64_t)row * a.q_row;
+#pragma unroll 4
+                for (int c8 = 0; c8 < D / 8; ++c8)
+                    *reinterpret_cast<uint4 *>(qs + (c8 / 8) * (BM * 128) + sw128(r, c8 % 8)) =
+                        ld_nc_v4(src + c8 * 8);
+            } else {
+                for (int c8 = 0; c8 < D / 8; ++c8)
+                    *reinterpret_cast<uint4 *>(qs + (c8 / 8) * (BM * 128) + sw128(r, c8 % 8)) =
+                        make_uint4(0, 0, 0, 0);
+            }
+            tc::fence_async_smem();
+            tc::mbar_arrive(q_full);
+        }
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint16_t *mrow = valid ? a.mask + t.lane * a.m_lane + (int64_t)head * a.m_head +
+                                           (int64_t)row * a.m_row
+                                     : nullptr;
+        const bool m_vec = valid && (reinterpret_cast<uintptr_t>(mrow) & 15) == 0;
+        float m_ref = kNegInf, l = 0.f;
+        int i = 0;
+        bool ok = true;
+        for (int j = jb; j < je; ++j) {
+            const int code = tile_code<BN>(a, cg, j);
+            if (!code) continue;
+            ok = __all_sync(0xffffffffu, wt.wait(s_full(i & 1), (i >> 1) & 1));
+            if (!ok) break;
+            tc::tc_fence_after();
+            float s[BN];
+#pragma unroll
+            for (int cb = 0; cb < BN / 32; ++cb) {
+                uint32_t rr[32];
+                tc::tmem_ld32(tm_s + (uint32_t)(i & 1) * BN + cb * 32 + lane_base, rr);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[cb * 32 + e] = __uint_as_float(rr[e]);
+            }
+            if (!valid) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) s[c] = kNegInf;
+            } else if (code == 1) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) s[c] *= a.scale_log2;
+            } else {
+                const int c0 = j * BN;
+                if (m_vec && c0 + BN <= a.n_keys) {
+#pragma unroll
+                    for (int v = 0; v < BN / 8; ++v) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(mrow + c0 + v * 8);
+                        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const uint16_t mv = (uint16_t)(w[e / 2] >> ((e & 1) * 16));
+                            s[v * 8 + e] = fmaf(s[v * 8 + e], a.scale_log2,
+                                                mask_to_f32(mv, a.mask_bf16) * kLog2e);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c)
+                        s[c] = (c0 + c < a.n_keys)
+                                   ? fmaf(s[c], a.scale_log2, mask_to_f32(mrow[c0 + c], a.mask_bf16) * kLog2e)
+                                   : kNegInf;
+                }
+            }
+            float mx = kNegInf;
+#pragma unroll
+            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+            float factor = 1.f;
+            bool resc = false;
+            if (m_ref == kNegInf) {
+                m_ref = mx;
+            } else if (mx > m_ref + kRescaleThreshold) {
+                factor = ex2(m_ref - mx);
+                m_ref = mx;
+                resc = true;
+            }
+            const float mu = m_ref == kNegInf ? 0.f : m_ref;
+            uint32_t pk[BN / 2];
+            float rowsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < BN; c += 2) {
+                const float p0 = ex2(s[c] - mu), p1 = ex2(s[c + 1] - mu);
+                rowsum += p0 + p1;
+                pk[c / 2] = pack2(KV{}, p0, p1);
+            }
+            l = l * factor + rowsum;
+            // P.V of the previous tile must be done: P is single-buffered and O may be rescaled
+            if (i > 0) {
+                ok = __all_sync(0xffffffffu, wt.wait(o_done, (i - 1) & 1));
+                if (!ok) break;
+                tc::tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                for (int cb = 0; cb < DO / 32; ++cb) {
+                    uint32_t rr[32];
+                    tc::tmem_ld32(tm_o + cb * 32 + lane_base, rr);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
+                    tc::tmem_st32(tm_o + cb * 32 + lane_base, rr);
+                }
+                tc::tmem_st_wait();
+            }
+            uint8_t *ps = smem + L::kP;
+#pragma unroll
+            for (int c8 = 0; c8 < BN / 8; ++c8)
+                *reinterpret_cast<uint4 *>(ps + (c8 / 8) * (BM * 128) + sw128(r, c8 % 8)) =
+                    make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
+            tc::fence_async_smem();
+            tc::tc_fence_before();
+            tc::mbar_arrive(p_full);
+            ++i;
+        }
+        // ---- epilogue
+        if (ok && i > 0) {
+            ok = __all_sync(0xffffffffu, wt.wait(o_done, (i - 1) & 1));
+            tc::tc_fence_after();
+        }
+        if (ok) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float *dst;
+            if (a.splits == 1) {
+                dst = valid ? a.o + t.lane * a.o_lane + (int64_t)head * a.o_head +
+                                  (int64_t)row * a.o_row + d_off
+                            : nullptr;
+            } else {
+                const int64_t unit = ((int64_t)tile_id * a.d_parts + dpart) * a.splits + split;
+                dst = a.ws_o + (unit * BM + r) * DO;
+                a.ws_lse[unit * BM + r] = l > 0.f ? m_ref + __log2f(l) : kNegInf;
+            }
+#pragma unroll 1
+            for (int cb = 0; cb < DO / 32; ++cb) {
+                uint32_t rr[32];
+                if (i > 0) {
+                    tc::tmem_ld32(tm_o + cb * 32 + lane_base, rr);
+                    tc::tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[e] = 0u;
+                }
+                if (dst) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(dst + cb * 32 + e) =
+                            make_float4(__uint_as_float(rr[e]) * inv, __uint_as_float(rr[e + 1]) * inv,
+                                        __uint_as_float(rr[e + 2]) * inv, __uint_as_float(rr[e + 3]) * inv);
+                }
+            }
+        }
+    }
+
+    // ---- teardown: TMEM is released only after every role is done with it
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc<512>(tmem);
+    }
+}
+
+// One warp per (tile, output half, tile row): merge the key splits.
+template <int DO>
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a, int tiles) {
+    const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= tiles * a.d_parts * BM) return;
+    const int r = wid % BM;
+    const int dpart = (wid / BM) % a.d_parts;
+    const int tile_id = wid / (BM * a.d_parts);
+    const Tile t = tile_of(a, tile_id);
+    int head, row;
+    if (!row_of(a, t, r, head, row)) return;
+    const int64_t u0 = ((int64_t)tile_id * a.d_parts + dpart) * a.splits;
+    float M = kNegInf;
+    for (int s = 0; s < a.splits; ++s) M = fmaxf(M, a.ws_lse[(u0 + s) * BM + r]);
+    float acc[DO / 32];
+#pragma unroll
+    for (int k = 0; k < DO / 32; ++k) acc[k] = 0.f;
+    float L = 0.f;
+    if (M != kNegInf) {
+        for (int s = 0; s < a.splits; ++s) {
+            const float w = ex2(a.ws_lse[(u0 + s) * BM + r] - M);
+            L += w;
+            const float *src = a.ws_o + ((u0 + s) * BM + r) * DO;
+#pragma unroll
+            for (int k = 0; k < DO / 32; ++k) acc[k] += w * src[lane + 32 * k];
+        }
+    }
+    float *out = a.o + t.lane * a.o_lane + (int64_t)head * a.o_head + (int64_t)row * a.o_row +
+                 dpart * DO;
+#pragma unroll
+    for (int k = 0; k < DO / 32; ++k) out[lane + 32 * k] = L > 0.f ? acc[k] / L : 0.f;
+}
+
+}  // namespace
+}  // namespace gqa
+
+// ===========================================================================
+// host side
+// ===========================================================================
+namespace gqa {
+namespace {
+
+struct Plan {
+    int bn, do_, d_parts;
+    int rows_per_head, heads_per_tile, row_tiles, head_tiles, tiles;
+    int n_blk, code_cols, code_groups, splits, bps;
+    bool shared_mask;
+    size_t codes_bytes, part_o_bytes, part_lse_bytes;
+};
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, int n_keys,
+               bool shared_mask) {
+    Plan p{};
+    p.bn = head_dim == 128 ? 128 : 64;
+    p.do_ = head_dim == 512 ? 256 : head_dim;
+    p.d_parts = head_dim / p.do_;
+    const int group = n_heads / n_kv_heads;
+    p.rows_per_head = rows < BM ? rows : BM;
+    p.heads_per_tile = BM / p.rows_per_head;
+    if (p.heads_per_tile > group) p.heads_per_tile = group;
+    p.row_tiles = (rows + p.rows_per_head - 1) / p.rows_per_head;
+    p.head_tiles = (group + p.heads_per_tile - 1) / p.heads_per_tile;
+    p.tiles = lanes * n_kv_heads * p.head_tiles * p.row_tiles;
+    p.n_blk = (n_keys + p.bn - 1) / p.bn;
+    p.code_cols = (n_keys + 63) / 64;
+    p.shared_mask = shared_mask;
+    p.code_groups = shared_mask ? lanes * p.row_tiles : p.tiles;
+    const int units = p.tiles * p.d_parts;
+    int sms = sm_count();
+    if (sms <= 0) sms = 148;
+    p.splits = 1;
+    if (units < sms && p.n_blk > 1) {
+        int s = (sms + units - 1) / units;
+        if (s > p.n_blk) s = p.n_blk;
+        p.splits = s;
+    }
+    p.bps = (p.n_blk + p.splits - 1) / p.splits;
+    p.splits = (p.n_blk + p.bps - 1) / p.bps;
+    p.codes_bytes = align256((size_t)p.code_groups * p.code_cols);
+    if (p.splits > 1) {
+        const size_t nunits = (size_t)p.tiles * p.d_parts * p.splits;
+        p.part_o_bytes = align256(nunits * BM * p.do_ * 4);
+        p.part_lse_bytes = align256(nunits * BM * 4);
+    }
+    return p;
+}
+
+size_t plan_bytes(const Plan &p) { return p.codes_bytes + p.part_o_bytes + p.part_lse_bytes; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// [heads][rows][D] view with element strides (row, head); box = 64 x bn x 1
+bool make_kv_map(CUtensorMap *m, const void *base, bool bf16, int d, int rows, int heads,
+                 int64_t row_stride, int64_t head_stride, int bn) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2,
+                             (cuuint64_t)(heads > 1 ? head_stride * 2 : 16)};
+    cuuint32_t box[3] = {64, (cuuint32_t)bn, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                    const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, class KV>
+cudaError_t run_attn(const AttnArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, int units,
+                     int tiles, cudaStream_t stream) {
+    auto kern = attn_kernel<D, KV>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Layout<D>::kBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    kern<<<units, kThreads, Layout<D>::kBytes, stream>>>(a, mk, mv);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || a.splits == 1) return e;
+    const int warps = tiles * a.d_parts * BM;
+    attn_combine_kernel<Cfg<D>::DO><<<(warps + 3) / 4, 128, 0, stream>>>(a, tiles);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t prefill_workspace_bytes(int rows, int n_heads, int n_kv_heads, int head_dim, int kv_pad) {
+    return plan_bytes(make_plan(1, rows, n_heads, n_kv_heads, head_dim, kv_pad, true));
+}
+
+size_t verify_workspace_bytes(const gqa_ring_params &p) {
+    return plan_bytes(make_plan((int)p.lanes, (int)p.rows, (int)p.q_heads, (int)p.kv_heads,
+                                (int)p.head_dim, (int)p.packed_len, false));
+}
+
+cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t stream) {
+    const bool shared = p.mask_head_stride == 0;
+    const Plan pl = make_plan(p.lanes, p.rows, p.n_heads, p.n_kv_heads, p.head_dim, p.n_keys, shared);
+    AttnArgs a{};
+    a.q = p.q;
+    a.q_f32 = p.q_is_f32 ? 1 : 0;
+    a.q_row = p.q_row_stride;
+    a.q_head = p.q_head_stride;
+    a.q_lane = p.q_lane_stride;
+    a.kv_bf16 = p.kv_dtype == GQA_DTYPE_BF16;
+    a.mask = p.mask;
+    a.mask_bf16 = p.mask_is_bf16 ? 1 : 0;
+    a.m_row = p.mask_row_stride;
+    a.m_head = p.mask_head_stride;
+    a.m_lane = p.mask_lane_stride;
+    a.o = p.o;
+    a.o_row = p.o_row_stride;
+    a.o_head = p.o_head_stride;
+    a.o_lane = p.o_lane_stride;
+    a.lanes = p.lanes;
+    a.rows = p.rows;
+    a.n_heads = p.n_heads;
+    a.n_kv_heads = p.n_kv_heads;
+    a.group = p.n_heads / p.n_kv_heads;
+    a.n_keys = p.n_keys;
+    a.rows_per_head = pl.rows_per_head;
+    a.heads_per_tile = pl.heads_per_tile;
+    a.row_tiles = pl.row_tiles;
+    a.head_tiles = pl.head_tiles;
+    a.n_blk = pl.n_blk;
+    a.splits = pl.splits;
+    a.blk_per_split = pl.bps;
+    a.d_parts = pl.d_parts;
+    a.scale_log2 = p.scale * kLog2e;
+    a.code_cols = pl.code_cols;
+    a.shared_mask = shared ? 1 : 0;
+    char *ws = static_cast<char *>(workspace);
+    a.codes = reinterpret_cast<uint8_t *>(ws);
+    a.ws_o = pl.splits > 1 ? reinterpret_cast<float *>(ws + pl.codes_bytes) : nullptr;
+    a.ws_lse = pl.splits > 1 ? reinterpret_cast<float *>(ws + pl.codes_bytes + pl.part_o_bytes) : nullptr;
+    a.status = p.status;
+
+    CUtensorMap mk, mv;
+    const int heads = p.lanes * p.n_kv_heads;
+    if (!make_kv_map(&mk, p.k, a.kv_bf16, p.head_dim, p.kv_rows, heads, p.k_row_stride,
+                     p.k_head_stride, pl.bn) ||
+        !make_kv_map(&mv, p.v, a.kv_bf16, p.head_dim, p.kv_rows, heads, p.v_row_stride,
+                     p.v_head_stride, pl.bn))
+        return cudaErrorInvalidValue;
+
+    classify_kernel<<<dim3(pl.code_groups, pl.code_cols), BM, 0, stream>>>(a, const_cast<uint8_t *>(a.codes));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int units = pl.tiles * pl.d_parts * pl.splits;
+    const bool bf = a.kv_bf16;
+    switch (p.head_dim) {
+        case 128:
+            return bf ? run_attn<128, BF16>(a, mk, mv, units, pl.tiles, stream)
+                      : run_attn<128, F16>(a, mk, mv, units, pl.tiles, stream);
+        case 256:
+            return bf ? run_attn<256, BF16>(a, mk, mv, units, pl.tiles, stream)
+                      : run_attn<256, F16>(a, mk, mv, units, pl.tiles, stream);
+        case 512:
+            return bf ? run_attn<512, BF16>(a, mk, mv, units, pl.tiles, stream)
+                      : run_attn<512, F16>(a, mk, mv, units, pl.tiles, stream);
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gqa

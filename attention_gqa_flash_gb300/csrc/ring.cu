@@ -1,0 +1,248 @@
+// ring.cu -- DFlash2 ring-KV kernels: pack, mask, commit, draft mask rows.
+//
+// Layouts and semantics follow mlx-native 0.21.1 src/ops/dflash2_attention_pack.rs
+// (dispatch_dflash2_pack_attention_bf16, dispatch_dflash2_attention_mask_bf16,
+// dispatch_dflash2_commit_kv_bf16, dispatch_dflash2_mask_rows_f32 and the worked
+// example in gpu_pack_mask_and_commit_match_ring_semantics).
+//
+// All four are pure data movement: every thread moves 16 bytes of output
+// (8 bf16) with 16-byte loads/stores, so each warp touches whole 128-byte
+// lines.  Grids are sized to a few waves of the SM count and stride over
+// the work.
+#include "common.cuh"
+#include "launch.h"
+
+namespace gqa {
+
+struct RingGeom {
+    int B, H, HK, D, R, W, K, MC;
+};
+
+// Clamp the two ring counters of lane b; report when they were out of range.
+__device__ __forceinline__ void ring_counters(const uint32_t *cache_lengths,
+                                              const uint32_t *write_positions, int b, int W,
+                                              int32_t *status, int &len, int &wp) {
+    uint32_t l = cache_lengths[b];
+    uint32_t p = write_positions ? write_positions[b] : 0u;
+    if (l > (uint32_t)W || p >= (uint32_t)W) raise_flag(status, GQA_FLAG_RING_CLAMPED);
+    len = l > (uint32_t)W ? W : (int)l;
+    wp = (int)(p % (uint32_t)W);
+}
+
+__device__ __forceinline__ uint4 f32x8_to_bf16x8(const float *src) {
+    float4 a = ld_nc_f4(src);
+    float4 b = ld_nc_f4(src + 4);
+    return make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                      pack_bf16x2(b.z, b.w));
+}
+
+// Packed K/V: one thread per 8-element chunk of a packed column, for K and V.
+// Packed Q: one thread per 8-element chunk of a packed query row.
+__global__ void __launch_bounds__(256) pack_attention_kernel(
+    const uint16_t *__restrict__ ring_k, const uint16_t *__restrict__ ring_v,
+    const float *__restrict__ cur_q, const float *__restrict__ cur_k,
+    const float *__restrict__ cur_v, const uint32_t *__restrict__ cache_lengths,
+    const uint32_t *__restrict__ write_positions, uint16_t *__restrict__ packed_q,
+    uint16_t *__restrict__ packed_k, uint16_t *__restrict__ packed_v, RingGeom g,
+    int32_t *status) {
+    const int chunks = g.D / 8;
+    const int64_t kv_work = (int64_t)g.B * g.HK * g.K * chunks;
+    const int64_t q_work = (int64_t)g.B * g.H * g.R * chunks;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < kv_work + q_work;
+         t += stride) {
+        if (t < kv_work) {
+            const int ch = (int)(t % chunks);
+            const int64_t col_id = t / chunks;  // (b, kh, c)
+            const int c = (int)(col_id % g.K);
+            const int64_t bk = col_id / g.K;  // b * HK + kh
+            const int kh = (int)(bk % g.HK);
+            const int b = (int)(bk / g.HK);
+            const int64_t out = col_id * g.D + ch * 8;
+            uint4 vk, vv;
+            if (c < g.R) {
+                const int64_t src = (((int64_t)b * g.R + c) * g.HK + kh) * g.D + ch * 8;
+                vk = f32x8_to_bf16x8(cur_k + src);
+                vv = f32x8_to_bf16x8(cur_v + src);
+            } else {
+                int len, wp;
+                ring_counters(cache_lengths, write_positions, b, g.W, ch == 0 ? status : nullptr,
+                              len, wp);
+                const int j = c - g.R;
+                if (j < len) {
+                    int slot = wp - 1 - j;
+                    slot += (slot < 0) ? g.W : 0;
+                    slot += (slot < 0) ? g.W : 0;
+                    const int64_t src = (bk * g.W + slot) * g.D + ch * 8;
+                    vk = ld_nc_v4(ring_k + src);
+                    vv = ld_nc_v4(ring_v + src);
+                } else {
+                    vk = make_uint4(0, 0, 0, 0);
+                    vv = vk;
+                }
+            }
+            st_v4(packed_k + out, vk);
+            st_v4(packed_v + out, vv);
+        } else {
+            const int64_t u = t - kv_work;
+            const int ch = (int)(u % chunks);
+            const int64_t row_id = u / chunks;  // (b, qh, r)
+            const int r = (int)(row_id % g.R);
+            const int64_t bq = row_id / g.R;
+            const int qh = (int)(bq % g.H);
+            const int b = (int)(bq / g.H);
+            const int64_t src = (((int64_t)b * g.R + r) * g.H + qh) * g.D + ch * 8;
+            st_v4(packed_q + row_id * g.D + ch * 8, f32x8_to_bf16x8(cur_q + src));
+        }
+    }
+}
+
+// Mask: the flat [B][H][R][K] array is cut into 8-element chunks; K is
+// arbitrary, so a chunk may straddle two rows and each element is decided on
+// its own.
+__global__ void __launch_bounds__(256) fill_mask_kernel(const uint32_t *__restrict__ cache_lengths,
+                                                        uint16_t *__restrict__ mask, RingGeom g,
+                                                        int32_t *status) {
+    const int64_t total = (int64_t)g.B * g.H * g.R * g.K;
+    const int64_t nchunks = (total + 7) / 8;
+    const int64_t rows_per_lane = (int64_t)g.H * g.R;
+    if (blockIdx.x == 0 && threadIdx.x < g.B) {
+        if (cache_lengths[threadIdx.x] > (uint32_t)g.W) raise_flag(status, GQA_FLAG_RING_CLAMPED);
+    }
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < nchunks; t += stride) {
+        const int64_t e0 = t * 8;
+        int64_t row = e0 / g.K;
+        int c = (int)(e0 - row * g.K);
+        uint32_t w[4];
+        int cached_b = -1, len = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint16_t val = 0;
+            if (e0 + i < total) {
+                const int b = (int)(row / rows_per_lane);
+                if (b != cached_b) {
+                    uint32_t l = cache_lengths[b];
+                    len = l > (uint32_t)g.W ? g.W : (int)l;
+                    cached_b = b;
+                }
+                const int r = (int)(row % g.R);
+                const int j = c - g.R;
+                const bool visible = c < g.R || (j < len && r + j + 1 < g.W);
+                val = visible ? 0x0000 : 0xff80;
+            }
+            if (i & 1)
+                w[i / 2] |= (uint32_t)val << 16;
+            else
+                w[i / 2] = val;
+            if (++c == g.K) {
+                c = 0;
+                ++row;
+            }
+        }
+        if (e0 + 8 <= total) {
+            st_v4(mask + e0, make_uint4(w[0], w[1], w[2], w[3]));
+        } else {
+            for (int i = 0; e0 + i < total; ++i)
+                mask[e0 + i] = (uint16_t)((w[i / 2] >> ((i & 1) * 16)) & 0xffff);
+        }
+    }
+}
+
+// Commit: one thread per 8-element chunk of an offered (lane, row, kv head).
+__global__ void __launch_bounds__(256) commit_kv_kernel(
+    const float *__restrict__ new_k, const float *__restrict__ new_v,
+    const uint32_t *__restrict__ commit_counts, const uint32_t *__restrict__ write_positions,
+    uint16_t *__restrict__ ring_k, uint16_t *__restrict__ ring_v, RingGeom g, int32_t *status) {
+    const int chunks = g.D / 8;
+    const int64_t work = (int64_t)g.B * g.MC * g.HK * chunks;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < work; t += stride) {
+        const int ch = (int)(t % chunks);
+        const int64_t rest = t / chunks;
+        const int kh = (int)(rest % g.HK);
+        const int64_t bi = rest / g.HK;
+        const int i = (int)(bi % g.MC);
+        const int b = (int)(bi / g.MC);
+        const uint32_t cnt = commit_counts[b];
+        const uint32_t pos = write_positions[b];
+        if (i == 0 && kh == 0 && ch == 0 && (cnt > (uint32_t)g.MC || pos >= (uint32_t)g.W))
+            raise_flag(status, GQA_FLAG_RING_CLAMPED);
+        const int n = cnt > (uint32_t)g.MC ? g.MC : (int)cnt;
+        if (i >= n) continue;
+        const int slot = (int)((pos % (uint32_t)g.W + (uint32_t)i) % (uint32_t)g.W);
+        const int64_t src = rest * g.D + ch * 8;
+        const int64_t dst = (((int64_t)b * g.HK + kh) * g.W + slot) * g.D + ch * 8;
+        st_v4(ring_k + dst, f32x8_to_bf16x8(new_k + src));
+        st_v4(ring_v + dst, f32x8_to_bf16x8(new_v + src));
+    }
+}
+
+// Draft mask rows: rows 1..R-1 of every lane become the widened embedding.
+__global__ void __launch_bounds__(256) set_mask_rows_kernel(const uint16_t *__restrict__ emb,
+                                                            float *__restrict__ hidden, int lanes,
+                                                            int rows, int width) {
+    const int64_t work = (int64_t)lanes * (rows - 1) * width;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < work; t += stride) {
+        const int e = (int)(t % width);
+        const int64_t lr = t / width;
+        const int r = 1 + (int)(lr % (rows - 1));
+        const int l = (int)(lr / (rows - 1));
+        hidden[((int64_t)l * rows + r) * width + e] = __uint_as_float((uint32_t)emb[e] << 16);
+    }
+}
+
+static int grid_for(int64_t work, int sms) {
+    int64_t blocks = (work + 255) / 256;
+    int64_t cap = (int64_t)sms * 8;
+    if (blocks > cap) blocks = cap;
+    return (int)(blocks < 1 ? 1 : blocks);
+}
+
+static RingGeom geom_of(const gqa_ring_params &p) {
+    return RingGeom{(int)p.lanes, (int)p.q_heads,  (int)p.kv_heads,   (int)p.head_dim,
+                    (int)p.rows,  (int)p.window,   (int)p.packed_len, (int)p.max_commit};
+}
+
+cudaError_t launch_pack_attention(const uint16_t *ring_k, const uint16_t *ring_v,
+                                  const float *cur_q, const float *cur_k, const float *cur_v,
+                                  const uint32_t *cache_lengths, const uint32_t *write_positions,
+                                  uint16_t *packed_q, uint16_t *packed_k, uint16_t *packed_v,
+                                  const gqa_ring_params &p, int32_t *status, cudaStream_t stream) {
+    RingGeom g = geom_of(p);
+    int64_t work = (int64_t)g.B * g.HK * g.K * (g.D / 8) + (int64_t)g.B * g.H * g.R * (g.D / 8);
+    pack_attention_kernel<<<grid_for(work, sm_count()), 256, 0, stream>>>(
+        ring_k, ring_v, cur_q, cur_k, cur_v, cache_lengths, write_positions, packed_q, packed_k,
+        packed_v, g, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_mask(const uint32_t *cache_lengths, uint16_t *mask,
+                             const gqa_ring_params &p, int32_t *status, cudaStream_t stream) {
+    RingGeom g = geom_of(p);
+    int64_t work = ((int64_t)g.B * g.H * g.R * g.K + 7) / 8;
+    fill_mask_kernel<<<grid_for(work, sm_count()), 256, 0, stream>>>(cache_lengths, mask, g,
+                                                                      status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_commit_kv(const float *new_k, const float *new_v, const uint32_t *commit_counts,
+                             const uint32_t *write_positions, uint16_t *ring_k, uint16_t *ring_v,
+                             const gqa_ring_params &p, int32_t *status, cudaStream_t stream) {
+    RingGeom g = geom_of(p);
+    int64_t work = (int64_t)g.B * g.MC * g.HK * (g.D / 8);
+    commit_kv_kernel<<<grid_for(work, sm_count()), 256, 0, stream>>>(
+        new_k, new_v, commit_counts, write_positions, ring_k, ring_v, g, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_set_mask_rows(const uint16_t *emb, float *hidden, int lanes, int rows,
+                                 int width, cudaStream_t stream) {
+    int64_t work = (int64_t)lanes * (rows - 1) * width;
+    set_mask_rows_kernel<<<grid_for(work, sm_count()), 256, 0, stream>>>(emb, hidden, lanes, rows,
+                                                                          width);
+    return cudaGetLastError();
+}
+
+}  // namespace gqa

@@ -1,0 +1,226 @@
+/*
+ * gqa_attn.h -- C ABI of the GB300 (sm_103a) grouped-query attention library.
+ *
+ * What is computed.  Grouped-query attention over a KV cache,
+ *     O = softmax(scale * Q K^T + mask) V,
+ * evaluated flash-style with an online softmax; each KV head serves a
+ * contiguous group of n_heads / n_kv_heads query heads (query head h reads
+ * KV head h / (n_heads / n_kv_heads)).  The operations and their layouts
+ * restate three pages:
+ *   mlx-native 0.18.0, src/ops/flash_attn_prefill_tensor.rs      (prefill)
+ *   ferrum-kernels 0.8.3, src/backend/metal/vnext_ops/causal_attention.rs
+ *                                                                (paged decode)
+ *   mlx-native 0.21.1, src/ops/dflash2_attention_pack.rs         (ring KV)
+ *
+ * Conventions shared by every entry point.
+ *   - Return value: a gqa_status.  Validation happens on the host, before
+ *     anything is enqueued; on GQA_INVALID_ARGUMENT nothing was launched and
+ *     gqa_last_error() names the offending field.
+ *   - Device pointers are owned by the caller; the library never allocates,
+ *     frees or retains them.  Every buffer is passed with its size in bytes
+ *     so that layouts can be bounds-checked on the host.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  Kernel faults surface at the caller's
+ *     next synchronisation.
+ *   - Strides are in elements.  Every dimension and stride must fit in int32.
+ *   - Counters that live on the device (context lengths, page ids, ring
+ *     lengths and positions, commit counts) cannot be checked on the host.
+ *     Kernels clamp them into range and OR a GQA_FLAG_* bit into the optional
+ *     device word `status` (may be NULL); they never read or write out of
+ *     bounds because of them.
+ *   - `workspace` is caller-owned device scratch of at least the size the
+ *     matching *_workspace_size() function returns (256-byte aligned).  Two
+ *     calls that run concurrently must not share a workspace.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *gqa_stream_t;
+
+typedef enum {
+    GQA_OK = 0,
+    GQA_INVALID_ARGUMENT = 1, /* bad shape, dtype, stride, size or pointer */
+    GQA_CUDA_ERROR = 2,       /* a CUDA runtime/driver call failed */
+    GQA_DEVICE_TIMEOUT = 3    /* reported through `status` only (GQA_FLAG_TIMEOUT) */
+} gqa_status;
+
+typedef enum { GQA_DTYPE_F16 = 1, GQA_DTYPE_BF16 = 2 } gqa_dtype;
+
+/* Bits OR-ed into the device `status` word. */
+enum {
+    GQA_FLAG_PAGE_CLAMPED = 1,    /* a page id outside [0, num_pages) was clamped */
+    GQA_FLAG_CONTEXT_CLAMPED = 2, /* a context length outside [0, max_pages*page_size] */
+    GQA_FLAG_RING_CLAMPED = 4,    /* cache_length > window, write_position >= window, or
+                                     commit_count outside [0, max_commit] */
+    GQA_FLAG_TIMEOUT = 8          /* a bounded pipeline wait gave up; outputs are invalid */
+};
+
+/* Thread-local description of the last error on this thread ("" if none). */
+const char *gqa_last_error(void);
+/* Library version string. */
+const char *gqa_version(void);
+/* Number of streaming multiprocessors of the current device (0 on error). */
+int gqa_device_sm_count(void);
+
+/* ------------------------------------------------------------------------ */
+/* Prefill (mlx-native 0.18.0 flash_attn_prefill_tensor.rs: module doc,     */
+/* FlashAttnPrefillTensorParams, kv_pad, dispatch_flash_attn_prefill_tensor_f16). */
+/* ------------------------------------------------------------------------ */
+
+/* kv_len rounded up to the 64-row cache step. */
+uint32_t gqa_kv_pad(uint32_t kv_len);
+
+/* Workspace bytes gqa_attn_prefill needs for this shape (per-tile mask
+ * classification and split-KV partial results). */
+size_t gqa_attn_prefill_workspace_size(int rows, int n_heads, int n_kv_heads, int head_dim,
+                                       int kv_pad);
+
+/*
+ * q     f32, element (row i, head h, e) at q[i*q_row_stride + h*q_head_stride + e];
+ *       both strides multiples of 4 (16-byte rows).
+ * k, v  kv_dtype (f16 or bf16), element (key j, kv head g, e) at
+ *       k[j*k_row_stride + g*k_head_stride + e]; strides multiples of 8 and the
+ *       base 16-byte aligned (TMA).  Host contract as on the page: every row
+ *       below kv_pad is finite; padding rows should be zero and masked.
+ * mask  f16 additive mask [rows][kv_pad] (row stride kv_pad), shared by all
+ *       heads; -inf hides a key.  Added after scaling.
+ * o     f32 [rows][n_heads][head_dim], contiguous.
+ * head_dim in {128, 256, 512}; kv_pad a positive multiple of 64;
+ * n_heads a multiple of n_kv_heads.  A query row whose mask hides every key
+ * produces zeros.
+ */
+int gqa_attn_prefill(const float *q, size_t q_bytes, int q_row_stride, int q_head_stride,
+                     const void *k, size_t k_bytes, int k_row_stride, int k_head_stride,
+                     const void *v, size_t v_bytes, int v_row_stride, int v_head_stride,
+                     int kv_dtype, const uint16_t *mask, size_t mask_bytes, float *o,
+                     size_t o_bytes, int rows, int n_heads, int n_kv_heads, int head_dim,
+                     int kv_pad, float scale, void *workspace, size_t workspace_bytes,
+                     int32_t *status, gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Paged decode (ferrum-kernels 0.8.3 causal_attention.rs: paged_state_regions, */
+/* validate_signature, MAXIMUM_HEAD_DIM, the fixed 64 KiB page).             */
+/* ------------------------------------------------------------------------ */
+
+size_t gqa_attn_paged_decode_workspace_size(int num_seqs, int n_heads, int head_dim,
+                                            int max_pages_per_seq, int page_size);
+
+/*
+ * One query token per sequence attends to all context_lens[s] tokens of its
+ * sequence.  Token t of sequence s is slot t % page_size of physical page
+ * page_table[s*max_pages_per_seq + t/page_size]; its K (and, in the second
+ * pool, V) element (kv head g, e) is at
+ *     pool[page*page_stride + slot*token_stride + g*head_stride + e].
+ * q  f32 [num_seqs][n_heads][head_dim] contiguous; o likewise.
+ * k_pages / v_pages  kv_dtype, pool_bytes each (same layout), 16-byte aligned,
+ *     strides multiples of 8.  head_dim in {64, 128, 256}.
+ * page_table  int32 [num_seqs][max_pages_per_seq]; context_lens int32 [num_seqs].
+ * A sequence with context length 0 produces zeros.
+ */
+int gqa_attn_paged_decode(const float *q, size_t q_bytes, const void *k_pages,
+                          const void *v_pages, size_t pool_bytes, int kv_dtype,
+                          int64_t page_stride, int64_t token_stride, int64_t head_stride,
+                          const int32_t *page_table, size_t page_table_bytes,
+                          int max_pages_per_seq, const int32_t *context_lens,
+                          size_t context_lens_bytes, float *o, size_t o_bytes, int num_seqs,
+                          int n_heads, int n_kv_heads, int head_dim, int page_size,
+                          int num_pages, float scale, void *workspace, size_t workspace_bytes,
+                          int32_t *status, gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* DFlash2 ring KV (mlx-native 0.21.1 dflash2_attention_pack.rs).           */
+/* ------------------------------------------------------------------------ */
+
+/* DFlash2AttentionPackParams: lanes 1..4; q_heads a multiple of kv_heads;
+ * head_dim 128 or 256; rows 2..16; window > rows;
+ * packed_len == window - 1 + rows; 1 <= max_commit <= rows. */
+typedef struct {
+    uint32_t lanes, q_heads, kv_heads, head_dim, rows, window, packed_len, max_commit;
+} gqa_ring_params;
+
+/* 1 if the geometry is valid, 0 otherwise (message in gqa_last_error()). */
+int gqa_ring_params_valid(const gqa_ring_params *p);
+
+/*
+ * Pack the verify operands (b lanes, h q_heads, hk kv_heads, d head_dim,
+ * r rows, w window, k packed_len; every buffer contiguous, exact size):
+ *   ring_k, ring_v        bf16 [b][hk][w][d]
+ *   cur_q                 f32  [b][r][h][d]
+ *   cur_k, cur_v          f32  [b][r][hk][d]
+ *   cache_lengths, write_positions  u32 [b] (device)
+ *   packed_q              bf16 [b][h][r][d]  = bf16(cur_q), rounded to nearest even
+ *   packed_k, packed_v    bf16 [b][hk][k][d]: column c < r is bf16(cur row c);
+ *       column r + j is ring slot (write_position - 1 - j) mod w, copied bit for
+ *       bit, when j < cache_length, else zeros.  write_position is the next slot
+ *       commit writes, so the history runs newest first.
+ */
+int gqa_pack_attention(const uint16_t *ring_k, size_t ring_k_bytes, const uint16_t *ring_v,
+                       size_t ring_v_bytes, const float *cur_q, size_t cur_q_bytes,
+                       const float *cur_k, size_t cur_k_bytes, const float *cur_v,
+                       size_t cur_v_bytes, const uint32_t *cache_lengths,
+                       size_t cache_lengths_bytes, const uint32_t *write_positions,
+                       size_t write_positions_bytes, uint16_t *packed_q, size_t packed_q_bytes,
+                       uint16_t *packed_k, size_t packed_k_bytes, uint16_t *packed_v,
+                       size_t packed_v_bytes, const gqa_ring_params *p, int32_t *status,
+                       gqa_stream_t stream);
+
+/*
+ * Additive bf16 mask [b][h][r][k], the same for every head: column c < r is
+ * visible (the draft rows see each other); column r + j is visible to row r'
+ * when j < cache_length and r' + j + 1 < w (the key lies inside the window of
+ * w positions that ends at the query).  Visible 0x0000 (+0), hidden 0xFF80 (-inf).
+ */
+int gqa_fill_mask(const uint32_t *cache_lengths, size_t cache_lengths_bytes, uint16_t *mask,
+                  size_t mask_bytes, const gqa_ring_params *p, int32_t *status,
+                  gqa_stream_t stream);
+
+size_t gqa_attn_verify_workspace_size(const gqa_ring_params *p);
+
+/*
+ * Verify attention over the packed operands: for lane b and query head h,
+ *   O[b][row][h][:] = softmax(scale * packed_q[b][h][row] . packed_k[b][h/g]^T
+ *                             + mask[b][h][row]) packed_v[b][h/g]
+ * o f32 [b][r][h][d] contiguous.  Rows with no visible key produce zeros.
+ */
+int gqa_attn_verify(const uint16_t *packed_q, size_t packed_q_bytes, const uint16_t *packed_k,
+                    size_t packed_k_bytes, const uint16_t *packed_v, size_t packed_v_bytes,
+                    const uint16_t *mask, size_t mask_bytes, float *o, size_t o_bytes,
+                    const gqa_ring_params *p, float scale, void *workspace,
+                    size_t workspace_bytes, int32_t *status, gqa_stream_t stream);
+
+/*
+ * Commit accepted rows: for i < min(commit_counts[b], max_commit),
+ * ring slot (write_positions[b] + i) mod w of lane b receives bf16(new row i)
+ * for every KV head; other slots are untouched.  new_k / new_v f32
+ * [b][max_commit][hk][d].  The counters are read-only: the caller advances
+ * write_positions and cache_lengths.
+ */
+int gqa_commit_kv(const float *new_k, size_t new_k_bytes, const float *new_v,
+                  size_t new_v_bytes, const uint32_t *commit_counts, size_t commit_counts_bytes,
+                  const uint32_t *write_positions, size_t write_positions_bytes,
+                  uint16_t *ring_k, size_t ring_k_bytes, uint16_t *ring_v, size_t ring_v_bytes,
+                  const gqa_ring_params *p, int32_t *status, gqa_stream_t stream);
+
+/*
+ * Draft-input mask rows (dispatch_dflash2_mask_rows_f32): hidden is f32
+ * [lanes*rows][width]; in every lane row 0 (the anchor) is kept and rows
+ * 1..rows-1 are overwritten with the widened bf16 mask_embedding [width].
+ * lanes 1..4, rows 2..16, width > 0.
+ */
+int gqa_set_mask_rows(const uint16_t *mask_embedding, size_t mask_embedding_bytes,
+                      float *hidden, size_t hidden_bytes, uint32_t lanes, uint32_t rows,
+                      uint32_t width, gqa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

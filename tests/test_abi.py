@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads and
+exports every entry point declared in include/gqa_attn.h, the host helpers
+reproduce the pages' constants, and invalid geometry is rejected before any
+launch."""
+import ctypes
+import json
+import pathlib
+import re
+
+import pytest
+
+ROOT = pathlib.Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "gqa_attn.h"
+GOLDEN = pathlib.Path(__file__).parent / "golden"
+
+
+@pytest.fixture(scope="module")
+def g():
+    from attention_gqa_flash_gb300 import build
+    build.build()
+    import attention_gqa_flash_gb300 as pkg
+    pkg.library()
+    return pkg
+
+
+def _declared() -> set[str]:
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(gqa_[a-z0-9_]+)\s*\(", text))
+
+
+def test_every_declared_symbol_is_exported(g):
+    lib = ctypes.CDLL(str(g.LIB_PATH))
+    declared = _declared()
+    assert len(declared) >= 15
+    for name in sorted(declared):
+        assert hasattr(lib, name), f"{name} declared but not exported"
+    assert declared == set(g.exported_symbols())
+
+
+def test_version_and_kv_pad(g):
+    assert "sm_103a" in g.version()
+    ex = json.loads((GOLDEN / "prefill_kv_pad.json").read_text())
+    for kv_len, pad in ex["cases"]:
+        assert g.gqa_kv_pad(kv_len) == pad
+
+
+def test_ring_geometry_validation(g):
+    cases = json.loads((GOLDEN / "dflash2_geometry_cases.json").read_text())["cases"]
+    for c in cases:
+        assert g.gqa_ring_params_valid(c["geometry"]) == c["valid"]
+    assert not g.gqa_ring_params_valid([4, 32, 8, 64, 8, 2048, 2055, 8])
+    assert "invalid DFlash2 attention geometry" in g.library().gqa_last_error().decode()
+    assert g.gqa_ring_params_valid([4, 32, 8, 256, 16, 4096, 4111, 16])
+
+
+def test_prefill_rejects_bad_shapes_before_launch(g):
+    lib = g.library()
+    args = [None, 0, 0, 0, None, 0, 0, 0, None, 0, 0, 0, 1, None, 0, None, 0]
+    rc = lib.gqa_attn_prefill(*args, 64, 5, 2, 128, 64, 1.0, None, 0, None, None)
+    assert rc == 1 and "multiple of n_kv_heads" in lib.gqa_last_error().decode()
+    rc = lib.gqa_attn_prefill(*args, 64, 4, 2, 128, 65, 1.0, None, 0, None, None)
+    assert rc == 1 and "kv_pad" in lib.gqa_last_error().decode()
+    rc = lib.gqa_attn_prefill(*args, 64, 4, 2, 96, 64, 1.0, None, 0, None, None)
+    assert rc == 1 and "head_dim" in lib.gqa_last_error().decode()
+    rc = lib.gqa_attn_prefill(*args, 0, 4, 2, 128, 64, 1.0, None, 0, None, None)
+    assert rc == 1 and "empty shape" in lib.gqa_last_error().decode()
+
+
+def test_decode_rejects_bad_shapes_before_launch(g):
+    lib = g.library()
+    base = [None, 0, None, None, 0, 1, 0, 0, 0, None, 0, 4, None, 0, None, 0]
+    rc = lib.gqa_attn_paged_decode(*base, 2, 6, 4, 128, 16, 8, 1.0, None, 0, None, None)
+    assert rc == 1 and "multiple of n_kv_heads" in lib.gqa_last_error().decode()
+    rc = lib.gqa_attn_paged_decode(*base, 2, 8, 4, 96, 16, 8, 1.0, None, 0, None, None)
+    assert rc == 1 and "head_dim" in lib.gqa_last_error().decode()
+
+
+def test_ring_ops_reject_wrong_sizes_before_launch(g):
+    lib = g.library()
+    p = g.GqaRingParams(1, 1, 1, 128, 2, 4, 5, 2)
+    fake = ctypes.c_void_p(256)   # never dereferenced: sizes are checked first
+    rc = lib.gqa_fill_mask(fake, 4, fake, 2 * 5 * 2 - 2, ctypes.byref(p), None, None)
+    assert rc == 1 and "mask must be 20 bytes" in lib.gqa_last_error().decode()
+    bad = g.GqaRingParams(1, 1, 1, 128, 2, 4, 4, 2)
+    rc = lib.gqa_fill_mask(fake, 4, fake, 16, ctypes.byref(bad), None, None)
+    assert rc == 1
+
+
+def test_page_math_matches_the_fixed_page_capability():
+    """ferrum-kernels causal_attention.rs page math, restated for the library's
+    page layout: 4096 B/token (kv_heads 4, head_dim 256, f16, K and V),
+    64 KiB pages of 16 tokens, 17 tokens -> 2 pages, 262144 tokens -> 16384 pages."""
+    ex = json.loads((GOLDEN / "paged_page_math.json").read_text())
+    per_token = ex["kv_heads"] * ex["head_dim"] * ex["element_bytes"] * 2
+    assert per_token == ex["state_bytes_per_token"]
+    page_bytes = ex["derived_page_bytes"]
+    assert page_bytes // per_token == ex["derived_tokens_per_page"]
+    pages = lambda tokens: -(-tokens * per_token // page_bytes)
+    assert pages(17) == ex["tokens_17_physical_pages"]
+    assert pages(ex["maximum_context_tokens"]) == ex["maximum_pages"]
