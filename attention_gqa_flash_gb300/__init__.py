@@ -61,6 +61,8 @@ def library() -> ctypes.CDLL:
             "gqa_last_error": (ctypes.c_char_p, []),
             "gqa_version": (ctypes.c_char_p, []),
             "gqa_device_sm_count": (i32, []),
+            "gqa_timing_enable": (i32, [i32]),
+            "gqa_timing_last_ms": (f32, []),
             "gqa_kv_pad": (ctypes.c_uint32, [ctypes.c_uint32]),
             "gqa_attn_prefill_workspace_size": (sz, [i32] * 5),
             "gqa_attn_prefill": (i32, [vp, sz, i32, i32, vp, sz, i32, i32, vp, sz, i32, i32, i32,
@@ -89,7 +91,8 @@ def library() -> ctypes.CDLL:
 
 def exported_symbols() -> list[str]:
     """Names of the C entry points this binding wraps."""
-    return ["gqa_last_error", "gqa_version", "gqa_device_sm_count", "gqa_kv_pad",
+    return ["gqa_last_error", "gqa_version", "gqa_device_sm_count", "gqa_timing_enable",
+            "gqa_timing_last_ms", "gqa_kv_pad",
             "gqa_attn_prefill_workspace_size", "gqa_attn_prefill",
             "gqa_attn_paged_decode_workspace_size", "gqa_attn_paged_decode",
             "gqa_ring_params_valid", "gqa_pack_attention", "gqa_fill_mask",
@@ -135,6 +138,16 @@ def _ring(p) -> GqaRingParams:
     if isinstance(p, GqaRingParams):
         return p
     return GqaRingParams(*[int(x) for x in p])
+
+
+def gqa_timing_enable(enable: bool) -> None:
+    """Record CUDA events around each call's dominant kernel (measurement only)."""
+    _check(library().gqa_timing_enable(1 if enable else 0))
+
+
+def gqa_timing_last_ms() -> float:
+    """Elapsed ms of the dominant kernel of the most recent call (-1 if none)."""
+    return float(library().gqa_timing_last_ms())
 
 
 def version() -> str:

@@ -100,6 +100,18 @@ int sm_count() {
     return cache[dev];
 }
 
+namespace {
+bool g_timing = false;
+bool g_timing_recorded = false;
+cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+}  // namespace
+
+void timing_mark(bool before, cudaStream_t stream) {
+    if (!g_timing) return;
+    cudaEventRecord(before ? g_ev_start : g_ev_stop, stream);
+    if (!before) g_timing_recorded = true;
+}
+
 }  // namespace gqa
 
 extern "C" {
@@ -109,6 +121,25 @@ const char *gqa_last_error(void) { return g_last_error.c_str(); }
 const char *gqa_version(void) { return "gqa-attn-gb300 0.1.0 (sm_103a)"; }
 
 int gqa_device_sm_count(void) { return gqa::sm_count(); }
+
+int gqa_timing_enable(int enable) {
+    if (enable && !gqa::g_ev_start) {
+        cudaError_t e = cudaEventCreate(&gqa::g_ev_start);
+        if (e == cudaSuccess) e = cudaEventCreate(&gqa::g_ev_stop);
+        if (e != cudaSuccess) return cuda_fail("timing events", e);
+    }
+    gqa::g_timing = enable != 0;
+    gqa::g_timing_recorded = false;
+    return ok();
+}
+
+float gqa_timing_last_ms(void) {
+    if (!gqa::g_timing_recorded) return -1.f;
+    float ms = -1.f;
+    if (cudaEventSynchronize(gqa::g_ev_stop) != cudaSuccess) return -1.f;
+    if (cudaEventElapsedTime(&ms, gqa::g_ev_start, gqa::g_ev_stop) != cudaSuccess) return -1.f;
+    return ms;
+}
 
 uint32_t gqa_kv_pad(uint32_t kv_len) { return (uint32_t)(((uint64_t)kv_len + 63) / 64 * 64); }
 

@@ -82,6 +82,7 @@ struct AttnArgs {
     int q_f32;
     int64_t q_row, q_head, q_lane;
     int kv_bf16;
+    int k_rows_dim1, v_rows_dim1;  // tensor map is {d, rows, heads} (1) or {d, heads, rows} (0)
     const uint16_t *mask;
     int mask_bf16;
     int64_t m_row, m_head, m_lane;
@@ -306,25 +307,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::prefetch_tmap(&tmv);
             int stage = 0;
             uint32_t round = 0;
-            for (int j = jb; j < je && !*abort_flag; ++j) {
-                if (!tile_code<BN>(a, cg, j)) continue;
-                bool ok = true;
-                for (int ks = 0; ks <= KSUB && ok; ++ks) {
-                    if (!(ok = wt.wait(empty(stage), (round & 1) ^ 1))) break;
-                    const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
-                    tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
-                    const bool is_v = ks == KSUB;
-                    const int dc0 = is_v ? d_off / 64 : ks * (DS / 64);
+            // one stage: DS/64 boxes of [BN rows][64 columns] from K (sub-stage ks) or V
+            auto load = [&](int j, bool is_v, int ks) -> bool {
+                if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
+                const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
+                tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
+                const int dc0 = is_v ? d_off / 64 : ks * (DS / 64);
+                const int rows_dim1 = is_v ? a.v_rows_dim1 : a.k_rows_dim1;
+                const int c1 = rows_dim1 ? j * BN : head_idx;
+                const int c2 = rows_dim1 ? head_idx : j * BN;
 #pragma unroll
-                    for (int c = 0; c < DS / 64; ++c)
-                        tc::tma_load_3d(dst + c * (BN * 128), is_v ? (const void *)&tmv : (const void *)&tmk,
-                                        full(stage), (dc0 + c) * 64, j * BN, head_idx);
-                    if (++stage == NS) {
-                        stage = 0;
-                        ++round;
-                    }
+                for (int c = 0; c < DS / 64; ++c)
+                    tc::tma_load_3d(dst + c * (BN * 128), is_v ? (const void *)&tmv : (const void *)&tmk,
+                                    full(stage), (dc0 + c) * 64, c1, c2);
+                if (++stage == NS) {
+                    stage = 0;
+                    ++round;
                 }
-                if (!ok) break;
+                return true;
+            };
+            auto next_vis = [&](int j) {
+                while (j < je && !tile_code<BN>(a, cg, j)) ++j;
+                return j;
+            };
+            // the MMA issuer consumes K of tile i+1 before V of tile i: K0, K1, V0, K2, V1, ...
+            bool ok = true;
+            int jc = next_vis(jb);
+            for (int ks = 0; ks < KSUB && ok && jc < je; ++ks) ok = load(jc, false, ks);
+            while (ok && jc < je) {
+                const int jn = next_vis(jc + 1);
+                for (int ks = 0; ks < KSUB && ok && jn < je; ++ks) ok = load(jn, false, ks);
+                if (ok) ok = load(jc, true, 0);
+                jc = jn;
             }
         }
     } else if (warp == 5) {
@@ -686,15 +700,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [heads][rows][D] view with element strides (row, head); box = 64 x bn x 1
+// rows x heads x D view with element strides (row, head).  The two outer
+// dimensions are ordered by increasing stride; with a box of one head the
+// shared-memory image is the same [bn rows][64 columns] either way.
+bool rows_first(int heads, int64_t row_stride, int64_t head_stride) {
+    return heads == 1 || row_stride <= head_stride;
+}
+
 bool make_kv_map(CUtensorMap *m, const void *base, bool bf16, int d, int rows, int heads,
                  int64_t row_stride, int64_t head_stride, int bn) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
-    cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2,
-                             (cuuint64_t)(heads > 1 ? head_stride * 2 : 16)};
-    cuuint32_t box[3] = {64, (cuuint32_t)bn, 1};
+    const bool rf = rows_first(heads, row_stride, head_stride);
+    const int64_t hs = heads > 1 ? head_stride : row_stride * rows;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)(rf ? rows : heads),
+                          (cuuint64_t)(rf ? heads : rows)};
+    cuuint64_t strides[2] = {(cuuint64_t)(rf ? row_stride : hs) * 2,
+                             (cuuint64_t)(rf ? hs : row_stride) * 2};
+    cuuint32_t box[3] = {64, rf ? (cuuint32_t)bn : 1u, rf ? 1u : (cuuint32_t)bn};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                     const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -714,7 +737,9 @@ cudaError_t run_attn(const AttnArgs &a, const CUtensorMap &mk, const CUtensorMap
         if (e != cudaSuccess) return e;
         configured = true;
     }
+    timing_mark(true, stream);
     kern<<<units, kThreads, Layout<D>::kBytes, stream>>>(a, mk, mv);
+    timing_mark(false, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.splits == 1) return e;
     const int warps = tiles * a.d_parts * BM;
@@ -777,6 +802,8 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
 
     CUtensorMap mk, mv;
     const int heads = p.lanes * p.n_kv_heads;
+    a.k_rows_dim1 = rows_first(heads, p.k_row_stride, p.k_head_stride) ? 1 : 0;
+    a.v_rows_dim1 = rows_first(heads, p.v_row_stride, p.v_head_stride) ? 1 : 0;
     if (!make_kv_map(&mk, p.k, a.kv_bf16, p.head_dim, p.kv_rows, heads, p.k_row_stride,
                      p.k_head_stride, pl.bn) ||
         !make_kv_map(&mv, p.v, a.kv_bf16, p.head_dim, p.kv_rows, heads, p.v_row_stride,

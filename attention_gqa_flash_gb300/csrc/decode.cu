@@ -334,7 +334,9 @@ cudaError_t run(const DecodeArgs &a, cudaStream_t stream) {
     int64_t grid = (int64_t)sm_count() * occ;
     if (grid > units) grid = units;
     if (grid < 1) grid = 1;
+    timing_mark(true, stream);
     kern<<<(int)grid, kWarps * 32, smem, stream>>>(a);
+    timing_mark(false, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int warps = a.num_seqs * a.n_heads;

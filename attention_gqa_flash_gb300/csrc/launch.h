@@ -12,6 +12,10 @@ namespace gqa {
 // SM count of the current device (cached per device).
 int sm_count();
 
+// Timing hook: record the start (before=true) or stop event around a
+// dominant kernel launch when gqa_timing_enable(1) is in effect.
+void timing_mark(bool before, cudaStream_t stream);
+
 // ring.cu
 cudaError_t launch_pack_attention(const uint16_t *ring_k, const uint16_t *ring_v,
                                   const float *cur_q, const float *cur_k, const float *cur_v,

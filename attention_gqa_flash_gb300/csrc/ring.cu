@@ -212,9 +212,11 @@ cudaError_t launch_pack_attention(const uint16_t *ring_k, const uint16_t *ring_v
                                   const gqa_ring_params &p, int32_t *status, cudaStream_t stream) {
     RingGeom g = geom_of(p);
     int64_t work = (int64_t)g.B * g.HK * g.K * (g.D / 8) + (int64_t)g.B * g.H * g.R * (g.D / 8);
+    timing_mark(true, stream);
     pack_attention_kernel<<<grid_for(work, sm_count()), 256, 0, stream>>>(
         ring_k, ring_v, cur_q, cur_k, cur_v, cache_lengths, write_positions, packed_q, packed_k,
         packed_v, g, status);
+    timing_mark(false, stream);
     return cudaGetLastError();
 }
 
@@ -222,8 +224,10 @@ cudaError_t launch_fill_mask(const uint32_t *cache_lengths, uint16_t *mask,
                              const gqa_ring_params &p, int32_t *status, cudaStream_t stream) {
     RingGeom g = geom_of(p);
     int64_t work = ((int64_t)g.B * g.H * g.R * g.K + 7) / 8;
+    timing_mark(true, stream);
     fill_mask_kernel<<<grid_for(work, sm_count()), 256, 0, stream>>>(cache_lengths, mask, g,
                                                                       status);
+    timing_mark(false, stream);
     return cudaGetLastError();
 }
 
@@ -232,16 +236,20 @@ cudaError_t launch_commit_kv(const float *new_k, const float *new_v, const uint3
                              const gqa_ring_params &p, int32_t *status, cudaStream_t stream) {
     RingGeom g = geom_of(p);
     int64_t work = (int64_t)g.B * g.MC * g.HK * (g.D / 8);
+    timing_mark(true, stream);
     commit_kv_kernel<<<grid_for(work, sm_count()), 256, 0, stream>>>(
         new_k, new_v, commit_counts, write_positions, ring_k, ring_v, g, status);
+    timing_mark(false, stream);
     return cudaGetLastError();
 }
 
 cudaError_t launch_set_mask_rows(const uint16_t *emb, float *hidden, int lanes, int rows,
                                  int width, cudaStream_t stream) {
     int64_t work = (int64_t)lanes * (rows - 1) * width;
+    timing_mark(true, stream);
     set_mask_rows_kernel<<<grid_for(work, sm_count()), 256, 0, stream>>>(emb, hidden, lanes, rows,
                                                                           width);
+    timing_mark(false, stream);
     return cudaGetLastError();
 }
 

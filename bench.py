@@ -1,0 +1,493 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 GQA attention library.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--paths all|main]
+
+Prints ONE JSON line on rank 0.  The headline is the causal prefill at
+head_dim 256 (2048 queries over 2048 keys, 16 query / 8 KV heads, f16 K/V,
+scale 1): `value` is algorithmic TFLOP/s (4*d FLOPs per visible
+(query, key) pair and head) over the device time of one call through the C
+ABI with inputs resident in HBM.  `paths` adds, measured in the same run,
+the head_dim-512 prefix prefill (TFLOP/s), the paged decode (KV GB/s) and
+the speculative-verify chain pack -> mask -> attention -> commit (GB/s of
+algorithmic bytes).  Every input is seeded and synthetic (workloads module).
+
+Timing: W untimed warm-up steps, then K steps, each preceded by an L2 flush
+(a 512 MiB device write, outside the step's CUDA-event pair) and timed with
+CUDA events on the launching stream, bracketed by a barrier and a device
+synchronisation.  `roofline` times the dominant kernel alone with events the
+library records around its launch (gqa_timing_enable).  SM clocks are sampled
+with nvidia-smi during the timed region.  Under torchrun (N>1) every rank runs
+an independent replica (the path shards into independent problems; no
+collective is on the data path) and the slowest rank's time is used.
+
+--impl reference times the float64 CPU oracle on a bounded sample of the
+same workload on the host cores (the only implementation the pages allow to
+run here).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import pathlib
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = pathlib.Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "prefill attn TFLOP/s & decode/verify KV GB/s (1×GB300, % of roofline)"
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+def peaks() -> tuple[dict, str]:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return d, "measured"
+        except Exception:
+            pass
+    return FALLBACK, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict | None:
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "samples": len(rows),
+                "reasons": reasons}
+
+
+def traffic_for(kernel: str, workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's source has changed since the counters were taken."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    try:
+        table = json.loads(p.read_text())
+    except Exception:
+        return None
+    e = table.get(f"{kernel}@{workload}")
+    if not e:
+        return None
+    src = ROOT / e["source"]
+    if not src.exists() or hashlib.sha256(src.read_bytes()).hexdigest() != e["source_sha256"]:
+        return None
+    return float(e["bytes_per_launch"])
+
+
+# ---------------------------------------------------------------------------
+# timing helpers
+# ---------------------------------------------------------------------------
+class Timer:
+    def __init__(self, torch, dist):
+        self.torch = torch
+        self.dist = dist
+        self.flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+
+    def flush(self):
+        self.flush_buf.zero_()
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+        self.torch.cuda.synchronize()
+
+    def steps(self, fn, steps: int, warmup: int) -> list[float]:
+        """Per-step device ms of fn (L2 flushed before each step)."""
+        torch = self.torch
+        for _ in range(warmup):
+            self.flush()
+            fn()
+        self.barrier()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for e0, e1 in evs:
+            self.flush()
+            e0.record()
+            fn()
+            e1.record()
+        self.barrier()
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+    def kernel_ms(self, g, fn, reps: int) -> float:
+        """Mean device ms of the dominant kernel of fn's last library call."""
+        g.gqa_timing_enable(True)
+        out = []
+        try:
+            for _ in range(reps):
+                self.flush()
+                fn()
+                out.append(g.gqa_timing_last_ms())
+        finally:
+            g.gqa_timing_enable(False)
+        return sum(out) / len(out)
+
+    def max_over_ranks(self, x: float) -> float:
+        if self.dist is None:
+            return x
+        t = self.torch.tensor([x], dtype=self.torch.float64, device="cuda")
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# workloads: each returns (step_fn, info) with algorithmic work per step
+# ---------------------------------------------------------------------------
+def _dev(torch, a, kind=None):
+    a = np.ascontiguousarray(a)
+    if kind == "bf16":
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+    if kind == "u32":
+        return torch.from_numpy(a.view(np.int32)).cuda()
+    return torch.from_numpy(a).cuda()
+
+
+def setup_prefill(torch, g, case):
+    kind = "bf16" if case.kv_dtype == "bf16" else None
+    q, k, v, m = (_dev(torch, case.q), _dev(torch, case.k, kind), _dev(torch, case.v, kind),
+                  _dev(torch, case.mask))
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(1, g.gqa_attn_prefill_workspace_size(case.rows, case.n_heads,
+                                                              case.n_kv_heads, case.head_dim,
+                                                              case.kv_pad)),
+                     dtype=torch.uint8, device="cuda")
+
+    def step():
+        g.gqa_attn_prefill(q, k, v, m, case.scale, out=out, workspace=ws)
+
+    # host copies of the same inputs for the end-to-end measurement
+    pin = lambda t: t.cpu().pin_memory()
+    hq, hk, hv, hm = pin(q), pin(k), pin(v), pin(m)
+    hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        m.copy_(hm, non_blocking=True)
+        g.gqa_attn_prefill(q, k, v, m, case.scale, out=out, workspace=ws)
+        hout.copy_(out, non_blocking=True)
+
+    nb = lambda t: t.numel() * t.element_size()
+    # classification pre-pass + attention kernel (these workloads need no key split)
+    info = {"flops": case.flops(), "h2d": nb(q) + nb(k) + nb(v) + nb(m), "d2h": nb(out),
+            "launches": 2}
+    return step, e2e_step, info
+
+
+def setup_decode(torch, g, c):
+    q, kp, vp = _dev(torch, c.q), _dev(torch, c.k_pool), _dev(torch, c.v_pool)
+    pt, cl = _dev(torch, c.page_table), _dev(torch, c.context_lens)
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    ws = torch.empty(g.gqa_attn_paged_decode_workspace_size(c.num_seqs, c.n_heads, c.head_dim,
+                                                            c.max_pages_per_seq, c.page_size),
+                     dtype=torch.uint8, device="cuda")
+
+    def step():
+        g.gqa_attn_paged_decode(q, kp, vp, pt, cl, c.scale, out=out, workspace=ws)
+
+    pages_used = int(sum(-(-int(x) // c.page_size) for x in c.context_lens))
+    kv = c.kv_bytes()
+    qo = q.numel() * 4
+    info = {"bytes": kv + 2 * qo + pages_used * 4 + c.num_seqs * 4,
+            "kernel_bytes": kv + qo + pages_used * 4 + c.num_seqs * 4, "kv_bytes": kv,
+            "launches": 2}
+    return step, info
+
+
+def setup_verify(torch, g, c):
+    B, H, HK, D, R, W, K, MC = c.geom
+    rk, rv = _dev(torch, c.ring_k, "bf16"), _dev(torch, c.ring_v, "bf16")
+    cq, ck, cv = _dev(torch, c.cur_q), _dev(torch, c.cur_k), _dev(torch, c.cur_v)
+    nk, nv = _dev(torch, c.new_k), _dev(torch, c.new_v)
+    lens, pos = _dev(torch, c.cache_lengths, "u32"), _dev(torch, c.write_positions, "u32")
+    cnt = _dev(torch, c.commit_counts, "u32")
+    pq = torch.empty((B, H, R, D), dtype=torch.bfloat16, device="cuda")
+    pk = torch.empty((B, HK, K, D), dtype=torch.bfloat16, device="cuda")
+    pv = torch.empty_like(pk)
+    mask = torch.empty((B, H, R, K), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((B, R, H, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(1, g.gqa_attn_verify_workspace_size(c.geom)), dtype=torch.uint8,
+                     device="cuda")
+    ops = {
+        "pack": lambda: g.gqa_pack_attention(rk, rv, cq, ck, cv, lens, pos, pq, pk, pv, c.geom),
+        "mask": lambda: g.gqa_fill_mask(lens, mask, c.geom),
+        "attn": lambda: g.gqa_attn_verify(pq, pk, pv, mask, c.geom, c.scale, out=out,
+                                          workspace=ws),
+        "commit": lambda: g.gqa_commit_kv(nk, nv, cnt, pos, rk, rv, c.geom),
+    }
+
+    def step():
+        for f in ops.values():
+            f()
+
+    hist = int(sum(min(int(x), W - 1) for x in c.cache_lengths))
+    n_commit = int(sum(min(int(x), MC) for x in c.commit_counts))
+    nb = lambda t: t.numel() * t.element_size()
+    by = {
+        "pack": hist * HK * D * 2 * 2 + nb(cq) + nb(ck) + nb(cv) + nb(pq) + nb(pk) + nb(pv),
+        "mask": nb(mask),
+        "attn": nb(pq) + nb(pk) + nb(pv) + nb(mask) + nb(out),
+        "commit": n_commit * HK * D * (4 + 2) * 2,
+    }
+    return step, ops, {"bytes": by, "launches": 1 + 1 + 2 + 1}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_prefill_sample(case, n_pairs: int, seed: int = 0):
+    """Time the float64 oracle on n_pairs sampled (row, head) outputs; returns
+    (seconds, algorithmic flops of the sample)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    pairs = np.stack([rng.integers(0, case.rows, n_pairs), rng.integers(0, case.n_heads, n_pairs)],
+                     axis=1).astype(np.int32)
+    vis = (case.mask == 0).sum(axis=1)
+    flops = float(4.0 * case.head_dim * vis[pairs[:, 0]].sum())
+    t0 = time.perf_counter()
+    oracle.attention(case.q, case.k, case.v, kv_dtype=case.kv_dtype, scale=case.scale,
+                     mask=case.mask, pairs=pairs)
+    return time.perf_counter() - t0, flops
+
+
+def cpu_baseline(case, target_s: float = 12.0) -> dict:
+    import oracle
+    t, f = oracle_prefill_sample(case, 64)
+    per_pair = max(t / 64, 1e-6)
+    n = int(min(case.rows * case.n_heads, max(64, target_s / per_pair)))
+    t, f = oracle_prefill_sample(case, n, seed=1)
+    return {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} random (query row, head) outputs of {case.name} "
+                      f"({f / 1e9:.1f} GFLOP, {t:.1f} s), float64 C with OpenMP"}
+
+
+def run_reference(args, case) -> None:
+    """--impl reference: the oracle, as it stands, on bounded samples of the workload."""
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    n = 512
+    for _ in range(args.warmup):
+        oracle_prefill_sample(case, 32)
+    times, flops = [], []
+    for s in range(args.steps):
+        t, f = oracle_prefill_sample(case, n, seed=100 + s)
+        times.append(t)
+        flops.append(f)
+    value = sum(flops) / sum(times) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": case.name, "sample_per_step": f"{n} (row, head) outputs"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"{n} random (query row, head) outputs per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--paths", choices=("all", "main"), default="all")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import workloads
+    head = workloads.prefill_d256(seed=0)
+    if args.impl == "reference":
+        run_reference(args, head)
+        return
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    import attention_gqa_flash_gb300 as g
+    g.library()
+    pk, peak_src = peaks()
+    tensor_peak = float(pk.get("bf16_tflops", FALLBACK["bf16_tflops"]))
+    tensor_peak_sustained = float(pk.get("bf16_tflops_sustained", tensor_peak))
+    hbm_peak = float(pk.get("hbm_gbs", FALLBACK["hbm_gbs"]))
+    tm = Timer(torch, dist)
+
+    # ---- headline: prefill d256
+    step, e2e_step, info = setup_prefill(torch, g, head)
+    with Clocks(local) as clk:
+        ms = tm.steps(step, args.steps, args.warmup)
+    ms_step = tm.max_over_ranks(sum(ms) / len(ms))
+    value = world * info["flops"] / (ms_step * 1e-3) / 1e12
+    kern = tm.kernel_ms(g, step, max(10, args.steps))
+    achieved = info["flops"] / (kern * 1e-3) / 1e12
+    e2e_ms = tm.max_over_ranks(sum(tm.steps(e2e_step, args.steps, args.warmup)) / args.steps)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded NumPy: Q ~ N(0, 1/16) f32, K/V ~ N(0,1) f16, causal mask)",
+        "config": {"workload": head.name, "rows": head.rows, "kv_len": head.kv_len,
+                   "n_heads": head.n_heads, "n_kv_heads": head.n_kv_heads,
+                   "head_dim": head.head_dim, "scale": head.scale,
+                   "flops_per_step": info["flops"],
+                   "l2": "flushed before every timed step (512 MiB device write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "attn_kernel<256,f16>", "achieved": achieved,
+                     "peak": tensor_peak, "unit": "TFLOP/s", "frac": achieved / tensor_peak,
+                     "kernel_ms": kern,
+                     "peak_source": f"{peak_src} bf16_tflops (burst); f16 dense rate equals bf16",
+                     "traffic": traffic_for("attn_kernel<256,f16>", head.name)},
+        "e2e": {"value": world * info["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": info["h2d"],
+                "d2h_bytes_per_step": info["d2h"]},
+        "gpu_launches": info["launches"] * args.steps,
+        "clocks": clk.summary(),
+    }
+    del step, e2e_step
+    torch.cuda.empty_cache()
+
+    if args.paths == "all":
+        paths = {}
+        # prefill d512 with a 7168-token prefix
+        c512 = workloads.prefill_d512_prefix(seed=0)
+        s512, _, i512 = setup_prefill(torch, g, c512)
+        ms = tm.steps(s512, max(5, args.steps // 2), args.warmup)
+        t = tm.max_over_ranks(sum(ms) / len(ms))
+        k = tm.kernel_ms(g, s512, 5)
+        paths["prefill_d512_prefix"] = {
+            "workload": c512.name, "value": world * i512["flops"] / (t * 1e-3) / 1e12,
+            "unit": "TFLOP/s", "ms_per_step": t,
+            "roofline": {"bound": "tensor", "kernel": "attn_kernel<512,f16>",
+                         "achieved": i512["flops"] / (k * 1e-3) / 1e12, "peak": tensor_peak,
+                         "unit": "TFLOP/s", "frac": i512["flops"] / (k * 1e-3) / 1e12 / tensor_peak,
+                         "kernel_ms": k, "traffic": traffic_for("attn_kernel<512,f16>", c512.name),
+                         "note": "two output halves recompute Q.K^T: executed FLOPs are 1.5x"}}
+        del s512
+        torch.cuda.empty_cache()
+        # paged decode
+        dc = workloads.paged_decode(seed=0)
+        sd, idc = setup_decode(torch, g, dc)
+        ms = tm.steps(sd, max(5, args.steps // 2), args.warmup)
+        t = tm.max_over_ranks(sum(ms) / len(ms))
+        k = tm.kernel_ms(g, sd, 5)
+        paths["paged_decode"] = {
+            "workload": dc.name, "value": world * idc["bytes"] / (t * 1e-3) / 1e9, "unit": "GB/s",
+            "kv_bytes_per_step": idc["kv_bytes"], "ms_per_step": t,
+            "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel<f16,128>",
+                         "achieved": idc["kernel_bytes"] / (k * 1e-3) / 1e9, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": idc["kernel_bytes"] / (k * 1e-3) / 1e9 / hbm_peak,
+                         "kernel_ms": k, "traffic": traffic_for("paged_decode_kernel<f16,128>", dc.name)}}
+        del sd, dc
+        torch.cuda.empty_cache()
+        # speculative verify chain
+        vc = workloads.verify_full(seed=0)
+        sv, ops, iv = setup_verify(torch, g, vc)
+        ms = tm.steps(sv, max(5, args.steps // 2), args.warmup)
+        t = tm.max_over_ranks(sum(ms) / len(ms))
+        total = sum(iv["bytes"].values())
+        kernels = {}
+        for name, f in ops.items():
+            k = tm.kernel_ms(g, f, 5)
+            kernels[name] = {"bytes": iv["bytes"][name], "kernel_ms": k,
+                             "achieved_gbs": iv["bytes"][name] / (k * 1e-3) / 1e9,
+                             "frac": iv["bytes"][name] / (k * 1e-3) / 1e9 / hbm_peak}
+        paths["verify_chain"] = {"workload": vc.name, "value": world * total / (t * 1e-3) / 1e9,
+                                 "unit": "GB/s", "ms_per_step": t, "bytes_per_step": total,
+                                 "peak": hbm_peak, "frac": total / (t * 1e-3) / 1e9 / hbm_peak,
+                                 "kernels": kernels}
+        line["paths"] = paths
+        line["gpu_launches"] += (2 + 2 + iv["launches"]) * max(5, args.steps // 2)
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(head)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -70,6 +70,19 @@ const char *gqa_version(void);
 /* Number of streaming multiprocessors of the current device (0 on error). */
 int gqa_device_sm_count(void);
 
+/*
+ * Kernel timing for measurement tools (process-wide, not thread-safe).  While
+ * enabled, every entry point records a pair of CUDA events on its stream
+ * immediately before and after the launch of its dominant kernel (the
+ * attention kernel of prefill/verify, the split-KV kernel of paged decode,
+ * the single kernel of each ring op).  gqa_timing_last_ms() waits for the
+ * most recent pair and returns its elapsed milliseconds, or -1 when nothing
+ * was recorded since the last enable.  Returns GQA_CUDA_ERROR if the events
+ * cannot be created.
+ */
+int gqa_timing_enable(int enable);
+float gqa_timing_last_ms(void);
+
 /* ------------------------------------------------------------------------ */
 /* Prefill (mlx-native 0.18.0 flash_attn_prefill_tensor.rs: module doc,     */
 /* FlashAttnPrefillTensorParams, kv_pad, dispatch_flash_attn_prefill_tensor_f16). */
