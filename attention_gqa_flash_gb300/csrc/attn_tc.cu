@@ -46,28 +46,51 @@ constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Q and P are the A operand of the two MMAs.  With GQA_TMEM_A they live in
+// tensor memory (written by the softmax threads with tcgen05.st), so the MMAs
+// read only K or V from shared memory and shared memory holds only the K/V
+// ring.  head_dim 512 keeps Q in shared memory: its 256 TMEM columns do not
+// fit next to O and S.
+#ifndef GQA_TMEM_A
+#define GQA_TMEM_A 0
+#endif
+constexpr int kSmemBudget = 232448 - 1024 - 512;
+
 template <int D>
-struct Cfg;
+struct Tiles;
 template <>
-struct Cfg<128> {
-    static constexpr int BN = 128, DS = 128, DO = 128, KSUB = 1, STAGES = 5;
+struct Tiles<128> {
+    static constexpr int BN = 128, DS = 128, DO = 128, KSUB = 1;
 };
 template <>
-struct Cfg<256> {
-    static constexpr int BN = 64, DS = 256, DO = 256, KSUB = 1, STAGES = 4;
+struct Tiles<256> {
+    static constexpr int BN = 64, DS = 256, DO = 256, KSUB = 1;
 };
 template <>
-struct Cfg<512> {
-    static constexpr int BN = 64, DS = 256, DO = 256, KSUB = 2, STAGES = 2;
+struct Tiles<512> {
+    static constexpr int BN = 64, DS = 256, DO = 256, KSUB = 2;
+};
+template <int D>
+struct Cfg : Tiles<D> {
+    using T = Tiles<D>;
+    static constexpr bool QTM = GQA_TMEM_A && D <= 256;  // Q in TMEM
+    static constexpr bool PTM = GQA_TMEM_A;              // P in TMEM (over its S buffer)
+    static constexpr int QBYTES = QTM ? 0 : BM * D * 2;
+    static constexpr int PBYTES = PTM ? 0 : BM * T::BN * 2;
+    static constexpr int STAGES = (kSmemBudget - QBYTES - PBYTES) / kStageBytes;
+    // TMEM columns: O [0, DO), S0/S1 [DO, DO + 2 BN), Q [DO + 2 BN, + D/2)
+    static constexpr int kColS = T::DO, kColQ = T::DO + 2 * T::BN;
+    static_assert(kColQ + (QTM ? D / 2 : 0) <= 512, "TMEM overflow");
+    static_assert(STAGES >= 2, "ring too small");
 };
 
 // shared-memory carve-up (offsets from a 1024-byte aligned base)
 template <int D>
 struct Layout {
     using C = Cfg<D>;
-    static constexpr int kQ = 0;                          // D/64 tiles of [128][64]
-    static constexpr int kP = kQ + BM * D * 2;            // BN/64 tiles of [128][64]
-    static constexpr int kStages = kP + BM * C::BN * 2;   // STAGES x 32 KiB
+    static constexpr int kQ = 0;                          // D/64 tiles of [128][64] (if in smem)
+    static constexpr int kP = kQ + C::QBYTES;             // BN/64 tiles of [128][64] (if in smem)
+    static constexpr int kStages = kP + C::PBYTES;        // STAGES x 32 KiB
     static constexpr int kBars = kStages + C::STAGES * kStageBytes;
     // barriers: full[S], empty[S], q_full, s_full[2], p_full, o_done, mma_fin
     static constexpr int kNumBars = 2 * C::STAGES + 6;
@@ -297,8 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tm_o = tmem;       // O: DO columns
-    const uint32_t tm_s = tmem + DO;  // S: two buffers of BN columns
+    const uint32_t tm_o = tmem;              // O: DO columns
+    const uint32_t tm_s = tmem + C::kColS;   // S: two buffers of BN columns (P over S)
+    const uint32_t tm_q = tmem + C::kColQ;   // Q: D/2 columns (when in TMEM)
 
     if (warp == 4) {
         // ------------------------------------------------------------ producer
@@ -363,11 +387,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < DS / 16; ++kk) {
                         const int dq = ks * DS + kk * 16;
-                        const uint64_t da = tc::smem_desc_sw128(
-                            sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16, 1024);
                         const uint64_t db = tc::smem_desc_sw128(
                             kb + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
-                        tc::mma_f16_ss(d_tm, da, db, id_qk, (ks | kk) != 0);
+                        if constexpr (C::QTM) {
+                            tc::mma_f16_ts(d_tm, tm_q + dq / 2, db, id_qk, (ks | kk) != 0);
+                        } else {
+                            const uint64_t da = tc::smem_desc_sw128(
+                                sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16,
+                                1024);
+                            tc::mma_f16_ss(d_tm, da, db, id_qk, (ks | kk) != 0);
+                        }
                     }
                     tc::mma_commit(empty(stage));
                     if (++stage == NS) {
@@ -398,10 +427,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t vb = sbase + L::kStages + stage * kStageBytes;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t da = tc::smem_desc_sw128(
-                        sbase + L::kP + (kk / 4) * (BM * 128) + (kk % 4) * 32, 16, 1024);
                     const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
-                    tc::mma_f16_ss(tm_o, da, db, id_pv, (i | kk) != 0);
+                    if constexpr (C::PTM) {
+                        tc::mma_f16_ts(tm_o, tm_s + (uint32_t)(i & 1) * BN + kk * 8, db, id_pv,
+                                       (i | kk) != 0);
+                    } else {
+                        const uint64_t da = tc::smem_desc_sw128(
+                            sbase + L::kP + (kk / 4) * (BM * 128) + (kk % 4) * 32, 16, 1024);
+                        tc::mma_f16_ss(tm_o, da, db, id_pv, (i | kk) != 0);
+                    }
                 }
                 tc::mma_commit(empty(stage));
                 if (++stage == NS) {
@@ -420,7 +454,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = threadIdx.x;  // tile row == TMEM lane
         int head = 0, row = 0;
         const bool valid = row_of(a, t, r, head, row);
-        {
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        if constexpr (C::QTM) {
+            // Q row -> TMEM lane r, 64 elements (32 columns) per tcgen05.st
+#pragma unroll 1
+            for (int cb = 0; cb < D / 64; ++cb) {
+                uint32_t w[32];
+                if (valid && a.q_f32) {
+                    const float *src = static_cast<const float *>(a.q) + t.lane * a.q_lane +
+                                       (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64;
+#pragma unroll
+                    for (int v = 0; v < 16; ++v) {
+                        const float4 x = ld_nc_f4(src + v * 4);
+                        w[2 * v] = pack2(KV{}, x.x, x.y);
+                        w[2 * v + 1] = pack2(KV{}, x.z, x.w);
+                    }
+                } else if (valid) {
+                    const uint16_t *src = static_cast<const uint16_t *>(a.q) + t.lane * a.q_lane +
+                                          (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const uint4 x = ld_nc_v4(src + v * 8);
+                        w[4 * v] = x.x;
+                        w[4 * v + 1] = x.y;
+                        w[4 * v + 2] = x.z;
+                        w[4 * v + 3] = x.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int v = 0; v < 32; ++v) w[v] = 0u;
+                }
+                tc::tmem_st32(tm_q + cb * 32 + lane_base, w);
+            }
+            tc::tmem_st_wait();
+            tc::tc_fence_before();
+            tc::mbar_arrive(q_full);
+        } else {
             uint8_t *qs = smem + L::kQ;
             if (valid && a.q_f32) {
                 const float *src = static_cast<const float *>(a.q) + t.lane * a.q_lane +
@@ -447,7 +516,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_async_smem();
             tc::mbar_arrive(q_full);
         }
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const uint16_t *mrow = valid ? a.mask + t.lane * a.m_lane + (int64_t)head * a.m_head +
                                            (int64_t)row * a.m_row
                                      : nullptr;
@@ -538,12 +606,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc::tmem_st_wait();
             }
-            uint8_t *ps = smem + L::kP;
+            if constexpr (C::PTM) {
+                // P over the first BN/2 columns of the S buffer it came from
 #pragma unroll
-            for (int c8 = 0; c8 < BN / 8; ++c8)
-                *reinterpret_cast<uint4 *>(ps + (c8 / 8) * (BM * 128) + sw128(r, c8 % 8)) =
-                    make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
-            tc::fence_async_smem();
+                for (int cb = 0; cb < BN / 64; ++cb) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) w[e] = pk[cb * 32 + e];
+                    tc::tmem_st32(tm_s + (uint32_t)(i & 1) * BN + cb * 32 + lane_base, w);
+                }
+                tc::tmem_st_wait();
+            } else {
+                uint8_t *ps = smem + L::kP;
+#pragma unroll
+                for (int c8 = 0; c8 < BN / 8; ++c8)
+                    *reinterpret_cast<uint4 *>(ps + (c8 / 8) * (BM * 128) + sw128(r, c8 % 8)) =
+                        make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
+                tc::fence_async_smem();
+            }
             tc::tc_fence_before();
             tc::mbar_arrive(p_full);
             ++i;
