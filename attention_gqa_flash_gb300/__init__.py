@@ -63,6 +63,7 @@ def library() -> ctypes.CDLL:
             "gqa_device_sm_count": (i32, []),
             "gqa_timing_enable": (i32, [i32]),
             "gqa_timing_last_ms": (f32, []),
+            "gqa_selftest_bounded_wait": (i32, [vp, i32, vp]),
             "gqa_kv_pad": (ctypes.c_uint32, [ctypes.c_uint32]),
             "gqa_attn_prefill_workspace_size": (sz, [i32] * 5),
             "gqa_attn_prefill": (i32, [vp, sz, i32, i32, vp, sz, i32, i32, vp, sz, i32, i32, i32,
@@ -92,7 +93,7 @@ def library() -> ctypes.CDLL:
 def exported_symbols() -> list[str]:
     """Names of the C entry points this binding wraps."""
     return ["gqa_last_error", "gqa_version", "gqa_device_sm_count", "gqa_timing_enable",
-            "gqa_timing_last_ms", "gqa_kv_pad",
+            "gqa_timing_last_ms", "gqa_selftest_bounded_wait", "gqa_kv_pad",
             "gqa_attn_prefill_workspace_size", "gqa_attn_prefill",
             "gqa_attn_paged_decode_workspace_size", "gqa_attn_paged_decode",
             "gqa_ring_params_valid", "gqa_pack_attention", "gqa_fill_mask",
@@ -148,6 +149,12 @@ def gqa_timing_enable(enable: bool) -> None:
 def gqa_timing_last_ms() -> float:
     """Elapsed ms of the dominant kernel of the most recent call (-1 if none)."""
     return float(library().gqa_timing_last_ms())
+
+
+def gqa_selftest_bounded_wait(status: torch.Tensor, timeout_ms: int, stream=None) -> None:
+    """Run the bounded-wait self-test; GQA_FLAG_TIMEOUT lands in `status`."""
+    _cuda("status", status, (torch.int32,))
+    _check(library().gqa_selftest_bounded_wait(_ptr(status), int(timeout_ms), _stream(stream)))
 
 
 def version() -> str:

@@ -133,6 +133,14 @@ int gqa_timing_enable(int enable) {
     return ok();
 }
 
+int gqa_selftest_bounded_wait(int32_t *status, int timeout_ms, gqa_stream_t stream) {
+    if (!status) return fail("selftest: status must not be NULL");
+    if (timeout_ms < 1 || timeout_ms > 10000) return fail("selftest: timeout_ms must be 1..10000");
+    cudaError_t e = gqa::launch_bounded_wait_selftest(status, timeout_ms, cs(stream));
+    if (e != cudaSuccess) return cuda_fail("selftest launch", e);
+    return ok();
+}
+
 float gqa_timing_last_ms(void) {
     if (!gqa::g_timing_recorded) return -1.f;
     float ms = -1.f;

@@ -236,6 +236,7 @@ __global__ void __launch_bounds__(BM) classify_kernel(const AttnArgs a, uint8_t 
 struct Waiter {
     volatile int *abort;
     int32_t *status;
+    uint64_t limit_ns;
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
         if (tc::mbar_try_wait(bar, parity)) return true;
         const uint64_t t0 = tc::globaltimer_ns();
@@ -243,7 +244,7 @@ struct Waiter {
             if (tc::mbar_try_wait(bar, parity)) return true;
             if ((it & 127) == 0) {
                 if (*abort) return false;
-                if (tc::globaltimer_ns() - t0 > kWaitLimitNs) {
+                if (tc::globaltimer_ns() - t0 > limit_ns) {
                     *abort = 1;
                     raise_flag(status, GQA_FLAG_TIMEOUT);
                     return false;
@@ -252,6 +253,19 @@ struct Waiter {
         }
     }
 };
+
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// arrives on; the wait must give up after limit_ns and raise GQA_FLAG_TIMEOUT.
+__global__ void bounded_wait_selftest_kernel(int32_t *status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    const uint32_t b = smem_u32(&bar);
+    tc::mbar_init(b, 1);
+    tc::fence_mbar_init();
+    abort_flag = 0;
+    const Waiter wt{&abort_flag, status, limit_ns};
+    wt.wait(b, 0);
+}
 
 // byte offset of the 16-byte chunk `c16` of row `r` in a [128][64] 16-bit tile
 // written with the 128-byte swizzle
@@ -280,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto s_full = [&](int b) { return bar(2 * NS + 1 + b); };
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlot);
-    const Waiter wt{abort_flag, a.status};
+    const Waiter wt{abort_flag, a.status, kWaitLimitNs};
 
     // ---- which unit: (query tile, output half, key split); heavy row tiles first
     int idx = blockIdx.x;
@@ -828,6 +842,11 @@ cudaError_t run_attn(const AttnArgs &a, const CUtensorMap &mk, const CUtensorMap
 }
 
 }  // namespace
+
+cudaError_t launch_bounded_wait_selftest(int32_t *status, int timeout_ms, cudaStream_t stream) {
+    bounded_wait_selftest_kernel<<<1, 1, 0, stream>>>(status, (uint64_t)timeout_ms * 1000000ull);
+    return cudaGetLastError();
+}
 
 size_t prefill_workspace_bytes(int rows, int n_heads, int n_kv_heads, int head_dim, int kv_pad) {
     return plan_bytes(make_plan(1, rows, n_heads, n_kv_heads, head_dim, kv_pad, true));

@@ -83,6 +83,15 @@ int gqa_device_sm_count(void);
 int gqa_timing_enable(int enable);
 float gqa_timing_last_ms(void);
 
+/*
+ * Diagnostic: launch one thread that waits, with the same bounded mbarrier
+ * wait the attention kernel uses, on a barrier nothing ever arrives on.  The
+ * wait gives up after timeout_ms (1..10000) and ORs GQA_FLAG_TIMEOUT into the
+ * device word `status`; the context stays usable.  Lets callers check the
+ * failure path of the bounded waits without faulting or hanging a GPU.
+ */
+int gqa_selftest_bounded_wait(int32_t *status, int timeout_ms, gqa_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Prefill (mlx-native 0.18.0 flash_attn_prefill_tensor.rs: module doc,     */
 /* FlashAttnPrefillTensorParams, kv_pad, dispatch_flash_attn_prefill_tensor_f16). */
