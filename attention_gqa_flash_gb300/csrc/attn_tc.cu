@@ -52,7 +52,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // ring.  head_dim 512 keeps Q in shared memory: its 256 TMEM columns do not
 // fit next to O and S.
 #ifndef GQA_TMEM_A
-#define GQA_TMEM_A 0
+#define GQA_TMEM_A 1
 #endif
 constexpr int kSmemBudget = 232448 - 1024 - 512;
 

@@ -41,11 +41,10 @@ def _run(g, c, table=None, kpool=None, vpool=None, ctx=None):
     (128, 40, 2, "bf16")])
 def test_small_ragged_contexts(lib, head_dim, n_heads, n_kv, dtype):
     from gpu_helpers import assert_attention_close
+    # ragged edges: 1 token, exactly one page, one past a page, one chunk, one past, ...
     c = workloads.paged_decode(num_seqs=9, ctx_lo=1, ctx_hi=700, num_pages=600, n_heads=n_heads,
                                n_kv_heads=n_kv, head_dim=head_dim, kv_dtype=dtype,
-                               seed=head_dim + n_heads)
-    # pin the ragged edges: 1 token, exactly one page, one past a page, one chunk, one past
-    c.context_lens[:6] = [1, 16, 17, 256, 257, 511]
+                               seed=head_dim + n_heads, fixed_lens=[1, 16, 17, 256, 257, 511])
     got, st = _run(lib, c)
     assert st == 0
     ref = oracle.paged_decode(c.q, c.k_pool, c.v_pool, kv_dtype=dtype, page_table=c.page_table,
@@ -54,8 +53,8 @@ def test_small_ragged_contexts(lib, head_dim, n_heads, n_kv, dtype):
 
 
 def test_zero_context_gives_zeros(lib):
-    c = workloads.paged_decode(num_seqs=3, ctx_lo=5, ctx_hi=40, num_pages=16, seed=2)
-    c.context_lens[1] = 0
+    c = workloads.paged_decode(num_seqs=3, ctx_lo=5, ctx_hi=40, num_pages=16, seed=2,
+                               fixed_lens=[7, 0])
     got, st = _run(lib, c)
     assert st == 0
     assert np.all(got[1] == 0)

@@ -188,13 +188,17 @@ class DecodeCase:
 def paged_decode(*, num_seqs: int = 64, ctx_lo: int = 512, ctx_hi: int = 16384,
                  num_pages: int = 65536, page_size: int = 16, n_heads: int = 32,
                  n_kv_heads: int = 8, head_dim: int = 128, kv_dtype: str = "f16",
-                 scale: float | None = None, seed: int = 0,
-                 name: str | None = None) -> DecodeCase:
+                 scale: float | None = None, seed: int = 0, name: str | None = None,
+                 fixed_lens=None) -> DecodeCase:
     """context_lens ~ U{ctx_lo..ctx_hi}; pages are taken in order from a random
     permutation of the pool; unused pages and the unused tail of each
-    sequence's last page are NaN, so a stray read poisons the result."""
+    sequence's last page are NaN, so a stray read poisons the result.
+    fixed_lens (optional) replaces the first len(fixed_lens) drawn lengths
+    before pages are assigned."""
     rng = np.random.default_rng(seed)
     ctx = rng.integers(ctx_lo, ctx_hi, size=num_seqs, endpoint=True).astype(np.int32)
+    if fixed_lens is not None:
+        ctx[:len(fixed_lens)] = fixed_lens
     perm = rng.permutation(num_pages).astype(np.int32)
     max_pages = -(-ctx_hi // page_size)
     need = -(-ctx.astype(np.int64) // page_size)
