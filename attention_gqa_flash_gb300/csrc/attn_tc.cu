@@ -602,13 +602,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[c / 2] = pack2(KV{}, p0, p1);
             }
             l = l * factor + rowsum;
-            // P.V of the previous tile must be done: P is single-buffered and O may be rescaled
-            if (i > 0) {
+            // P.V of the previous tile must be done before O is rescaled, and, when P
+            // lives in shared memory (one buffer), before P is overwritten.  A P kept in
+            // TMEM goes over this tile's own S buffer, which the previous P.V does not
+            // read, so without a rescale the softmax runs ahead of the tensor pipe.
+            // (P.V of this tile cannot complete before P is written, so the parity
+            // of o_done is never ambiguous.)
+            const bool any_resc = __any_sync(0xffffffffu, resc);
+            if (i > 0 && (!C::PTM || any_resc)) {
                 ok = __all_sync(0xffffffffu, wt.wait(o_done, (i - 1) & 1));
                 if (!ok) break;
                 tc::tc_fence_after();
             }
-            if (__any_sync(0xffffffffu, resc)) {
+            if (any_resc) {
 #pragma unroll 1
                 for (int cb = 0; cb < DO / 32; ++cb) {
                     uint32_t rr[32];
