@@ -31,6 +31,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "launch.h"
@@ -54,7 +55,9 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 #ifndef GQA_TMEM_A
 #define GQA_TMEM_A 1
 #endif
-constexpr int kSmemBudget = 232448 - 1024 - 512;
+// key tiles one CTA may visit (the list of visible tiles lives in shared memory)
+constexpr int kMaxListTiles = 768;
+constexpr int kSmemBudget = 232448 - 1024 - 256 - 2 * kMaxListTiles;
 
 template <int D>
 struct Tiles;
@@ -92,12 +95,15 @@ struct Layout {
     static constexpr int kP = kQ + C::QBYTES;             // BN/64 tiles of [128][64] (if in smem)
     static constexpr int kStages = kP + C::PBYTES;        // STAGES x 32 KiB
     static constexpr int kBars = kStages + C::STAGES * kStageBytes;
-    // barriers: full[S], empty[S], q_full, s_full[2], p_full, o_done, mma_fin
-    static constexpr int kNumBars = 2 * C::STAGES + 6;
+    // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], o_done[2], mma_fin
+    static constexpr int kNumBars = 2 * C::STAGES + 8;
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 4;
-    static constexpr int kEnd = kAbort + 4;
+    static constexpr int kNumVis = kAbort + 4;
+    static constexpr int kList = kNumVis + 4;  // visible key tiles: uint16 each
+    static constexpr int kEnd = kList + 2 * kMaxListTiles;
     static constexpr int kBytes = kEnd + 1024;  // + alignment slack
+    static_assert(kBytes <= 232448, "shared memory overflow");
 };
 
 struct AttnArgs {
@@ -106,6 +112,8 @@ struct AttnArgs {
     int64_t q_row, q_head, q_lane;
     int kv_bf16;
     int k_rows_dim1, v_rows_dim1;  // tensor map is {d, rows, heads} (1) or {d, heads, rows} (0)
+    // prefill tiles of one head and 128 rows move Q (f32) in and O out by TMA
+    int q_tma, o_tma, q_rows_dim1, o_rows_dim1;
     const uint16_t *mask;
     int mask_bf16;
     int64_t m_row, m_head, m_lane;
@@ -276,11 +284,13 @@ __device__ __forceinline__ uint32_t sw128(int r, int c16) {
 template <int D, class KV>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
-                const __grid_constant__ CUtensorMap tmv) {
+                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq,
+                const __grid_constant__ CUtensorMap tmo) {
     using C = Cfg<D>;
     using L = Layout<D>;
     constexpr int BN = C::BN, DS = C::DS, DO = C::DO, KSUB = C::KSUB, NS = C::STAGES;
     constexpr bool kBf16 = KV::kind == GQA_DTYPE_BF16;
+    constexpr int kQStages = D / 64;  // an f32 Q tile crosses the ring 64 columns per stage
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem =
@@ -289,11 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
     auto full = [&](int s) { return bar(s); };
     auto empty = [&](int s) { return bar(NS + s); };
-    const uint32_t q_full = bar(2 * NS), p_full = bar(2 * NS + 3), o_done = bar(2 * NS + 4),
-                   mma_fin = bar(2 * NS + 5);
+    const uint32_t q_full = bar(2 * NS);
     auto s_full = [&](int b) { return bar(2 * NS + 1 + b); };
+    auto p_full = [&](int b) { return bar(2 * NS + 3 + b); };
+    auto o_done = [&](int b) { return bar(2 * NS + 5 + b); };
+    const uint32_t mma_fin = bar(2 * NS + 7);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlot);
+    int *n_vis_smem = reinterpret_cast<int *>(smem + L::kNumVis);
+    uint16_t *list = reinterpret_cast<uint16_t *>(smem + L::kList);
     const Waiter wt{abort_flag, a.status, kWaitLimitNs};
 
     // ---- which unit: (query tile, output half, key split); heavy row tiles first
@@ -310,6 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int je = min(a.n_blk, jb + a.blk_per_split);
     const int d_off = dpart * DO;
     const int head_idx = t.lane * a.n_kv_heads + t.kh;
+    const int q_head0 = t.kh * a.group + t.ht * a.heads_per_tile;  // TMA paths: one head
+    const int q_row0 = t.rt * a.rows_per_head;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -318,13 +334,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(empty(s), 1);
         }
         tc::mbar_init(q_full, BM);
-        tc::mbar_init(s_full(0), 1);
-        tc::mbar_init(s_full(1), 1);
-        tc::mbar_init(p_full, BM);
-        tc::mbar_init(o_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(s_full(b), 1);
+            tc::mbar_init(p_full(b), BM);
+            tc::mbar_init(o_done(b), 1);
+        }
         tc::mbar_init(mma_fin, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
+    }
+    if (warp == 4) {
+        // visible key tiles of this unit in order: (j - jb) | 0x8000 when the mask applies
+        int n = 0;
+        for (int base = jb; base < je; base += 32) {
+            const int j = base + lane;
+            const int code = j < je ? tile_code<BN>(a, cg, j) : 0;
+            const unsigned vis = __ballot_sync(0xffffffffu, code != 0);
+            if (code)
+                list[n + __popc(vis & ((1u << lane) - 1u))] =
+                    (uint16_t)((j - jb) | (code == 2 ? 0x8000 : 0));
+            n += __popc(vis);
+        }
+        if (lane == 0) *n_vis_smem = n;
     }
     if (warp == 5) {
         tc::tmem_alloc<512>(smem_u32(tslot));
@@ -334,9 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tm_o = tmem;              // O: DO columns
-    const uint32_t tm_s = tmem + C::kColS;   // S: two buffers of BN columns (P over S)
-    const uint32_t tm_q = tmem + C::kColQ;   // Q: D/2 columns (when in TMEM)
+    const uint32_t tm_o = tmem;             // O: DO columns
+    const uint32_t tm_s = tmem + C::kColS;  // S: two buffers of BN columns (P over S)
+    const uint32_t tm_q = tmem + C::kColQ;  // Q: D/2 columns (when in TMEM)
+    const int n_vis = *n_vis_smem;
+    auto tile_at = [&](int v) { return jb + (list[v] & 0x7fff); };
 
     if (warp == 4) {
         // ------------------------------------------------------------ producer
@@ -345,7 +378,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::prefetch_tmap(&tmv);
             int stage = 0;
             uint32_t round = 0;
-            // one stage: DS/64 boxes of [BN rows][64 columns] from K (sub-stage ks) or V
+            auto next = [&]() {
+                if (++stage == NS) {
+                    stage = 0;
+                    ++round;
+                }
+            };
+            bool ok = true;
+            // f32 Q tile first (consumed by the softmax warps): [128 rows][32 cols] boxes
+            if (a.q_tma) {
+                tc::prefetch_tmap(&tmq);
+                for (int qs = 0; qs < kQStages && ok; ++qs) {
+                    if (!(ok = wt.wait(empty(stage), (round & 1) ^ 1))) break;
+                    const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
+                    tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
+#pragma unroll
+                    for (int b = 0; b < 2; ++b)
+                        tc::tma_load_3d(dst + b * 16384, &tmq, full(stage), qs * 64 + b * 32,
+                                        a.q_rows_dim1 ? q_row0 : q_head0,
+                                        a.q_rows_dim1 ? q_head0 : q_row0);
+                    next();
+                }
+            }
+            // one stage: DS/64 boxes of [BN rows][64 columns] of K (sub-stage ks) or V
             auto load = [&](int j, bool is_v, int ks) -> bool {
                 if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
                 const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
@@ -358,25 +413,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < DS / 64; ++c)
                     tc::tma_load_3d(dst + c * (BN * 128), is_v ? (const void *)&tmv : (const void *)&tmk,
                                     full(stage), (dc0 + c) * 64, c1, c2);
-                if (++stage == NS) {
-                    stage = 0;
-                    ++round;
-                }
+                next();
                 return true;
             };
-            auto next_vis = [&](int j) {
-                while (j < je && !tile_code<BN>(a, cg, j)) ++j;
-                return j;
-            };
-            // the MMA issuer consumes K of tile i+1 before V of tile i: K0, K1, V0, K2, V1, ...
-            bool ok = true;
-            int jc = next_vis(jb);
-            for (int ks = 0; ks < KSUB && ok && jc < je; ++ks) ok = load(jc, false, ks);
-            while (ok && jc < je) {
-                const int jn = next_vis(jc + 1);
-                for (int ks = 0; ks < KSUB && ok && jn < je; ++ks) ok = load(jn, false, ks);
-                if (ok) ok = load(jc, true, 0);
-                jc = jn;
+            // the MMA issuer consumes K of tile v+1 before V of tile v: K0, K1, V0, K2, V1, ...
+            for (int ks = 0; ks < KSUB && ok && n_vis > 0; ++ks) ok = load(tile_at(0), false, ks);
+            for (int v = 0; ok && v < n_vis; ++v) {
+                for (int ks = 0; ks < KSUB && ok && v + 1 < n_vis; ++ks) ok = load(tile_at(v + 1), false, ks);
+                if (ok) ok = load(tile_at(v), true, 0);
             }
         }
     } else if (warp == 5) {
@@ -384,16 +428,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t id_qk = tc::idesc_f16(BM, BN, kBf16, false);
             const uint32_t id_pv = tc::idesc_f16(BM, DO, kBf16, true);
-            int stage = 0;
-            uint32_t round = 0;
-            int n_s = 0;  // S tiles issued
-            auto next_vis = [&](int j) {
-                while (j < je && !tile_code<BN>(a, cg, j)) ++j;
-                return j;
+            int stage = a.q_tma ? kQStages % NS : 0;
+            uint32_t round = a.q_tma ? kQStages / NS : 0;
+            auto next = [&]() {
+                if (++stage == NS) {
+                    stage = 0;
+                    ++round;
+                }
             };
-            // S(n_s) = Q K^T into buffer n_s & 1
-            auto issue_s = [&]() -> bool {
-                const uint32_t d_tm = tm_s + (uint32_t)(n_s & 1) * BN;
+            // S(v) = Q K^T into buffer v & 1
+            auto issue_s = [&](int v) -> bool {
+                const uint32_t d_tm = tm_s + (uint32_t)(v & 1) * BN;
                 for (int ks = 0; ks < KSUB; ++ks) {
                     if (!wt.wait(full(stage), round & 1)) return false;
                     tc::tc_fence_after();
@@ -401,8 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < DS / 16; ++kk) {
                         const int dq = ks * DS + kk * 16;
-                        const uint64_t db = tc::smem_desc_sw128(
-                            kb + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
+                        const uint64_t db =
+                            tc::smem_desc_sw128(kb + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
                         if constexpr (C::QTM) {
                             tc::mma_f16_ts(d_tm, tm_q + dq / 2, db, id_qk, (ks | kk) != 0);
                         } else {
@@ -413,28 +458,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     tc::mma_commit(empty(stage));
-                    if (++stage == NS) {
-                        stage = 0;
-                        ++round;
-                    }
+                    next();
                 }
-                tc::mma_commit(s_full(n_s & 1));
-                ++n_s;
+                tc::mma_commit(s_full(v & 1));
                 return true;
             };
             bool ok = wt.wait(q_full, 0);
             tc::tc_fence_after();
-            int js = next_vis(jb);
-            if (ok && js < je) {
-                ok = issue_s();
-                js = next_vis(js + 1);
-            }
-            for (int i = 0; ok && i < n_s; ++i) {
-                if (js < je) {
-                    if (!(ok = issue_s())) break;
-                    js = next_vis(js + 1);
-                }
-                if (!(ok = wt.wait(p_full, i & 1))) break;
+            if (ok && n_vis > 0) ok = issue_s(0);
+            for (int i = 0; ok && i < n_vis; ++i) {
+                if (i + 1 < n_vis && !(ok = issue_s(i + 1))) break;
+                if (!(ok = wt.wait(p_full(i & 1), (i >> 1) & 1))) break;
                 tc::tc_fence_after();
                 if (!(ok = wt.wait(full(stage), round & 1))) break;
                 tc::tc_fence_after();
@@ -452,11 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tc::mma_commit(empty(stage));
-                if (++stage == NS) {
-                    stage = 0;
-                    ++round;
-                }
-                tc::mma_commit(o_done);
+                next();
+                tc::mma_commit(o_done(i & 1));
             }
             // every MMA of this thread has finished before TMEM can be released
             tc::mma_commit(mma_fin);
@@ -466,11 +497,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ softmax
         const int r = threadIdx.x;  // tile row == TMEM lane
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         int head = 0, row = 0;
         const bool valid = row_of(a, t, r, head, row);
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        if constexpr (C::QTM) {
-            // Q row -> TMEM lane r, 64 elements (32 columns) per tcgen05.st
+        bool ok = true;
+
+        // ---- Q row -> TMEM (or the shared-memory Q tile), rounded to K/V's type
+        auto put_q = [&](int cb, const uint32_t(&w)[32]) {  // 64 elements at column block cb
+            if constexpr (C::QTM) {
+                tc::tmem_st32(tm_q + cb * 32 + lane_base, w);
+            } else {
+                uint8_t *qs = smem + L::kQ + cb * (BM * 128);
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8)
+                    *reinterpret_cast<uint4 *>(qs + sw128(r, c8)) =
+                        make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
+            }
+        };
+        if (a.q_tma) {
+            // f32 Q arrives by TMA through the first kQStages ring stages
+            int stage = 0;
+            uint32_t round = 0;
+            for (int qs = 0; qs < kQStages; ++qs) {
+                if (ok) ok = wt.wait(full(stage), round & 1);
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) {
+                    const uint8_t *src = smem + L::kStages + stage * kStageBytes;
+                    uint32_t w[32];
+#pragma unroll
+                    for (int b = 0; b < 2; ++b)
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4) {
+                            const float4 x = *reinterpret_cast<const float4 *>(
+                                src + b * 16384 + r * 128 + ((c4 ^ (r & 7)) << 4));
+                            w[b * 16 + c4 * 2] = pack2(KV{}, x.x, x.y);
+                            w[b * 16 + c4 * 2 + 1] = pack2(KV{}, x.z, x.w);
+                        }
+                    put_q(qs, w);
+                }
+                tc::named_bar(1, BM);  // all softmax threads are done with this stage
+                if (r == 0) tc::mbar_arrive(empty(stage));
+                if (++stage == NS) {
+                    stage = 0;
+                    ++round;
+                }
+            }
+        } else {
+            // each thread reads its own row
 #pragma unroll 1
             for (int cb = 0; cb < D / 64; ++cb) {
                 uint32_t w[32];
@@ -498,59 +571,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int v = 0; v < 32; ++v) w[v] = 0u;
                 }
-                tc::tmem_st32(tm_q + cb * 32 + lane_base, w);
+                put_q(cb, w);
             }
-            tc::tmem_st_wait();
-            tc::tc_fence_before();
-            tc::mbar_arrive(q_full);
-        } else {
-            uint8_t *qs = smem + L::kQ;
-            if (valid && a.q_f32) {
-                const float *src = static_cast<const float *>(a.q) + t.lane * a.q_lane +
-                                   (int64_t)head * a.q_head + (int64_t)row * a.q_row;
-#pragma unroll 4
-                for (int c8 = 0; c8 < D / 8; ++c8) {
-                    const float4 x = ld_nc_f4(src + c8 * 8), y = ld_nc_f4(src + c8 * 8 + 4);
-                    const uint4 v = make_uint4(pack2(KV{}, x.x, x.y), pack2(KV{}, x.z, x.w),
-                                               pack2(KV{}, y.x, y.y), pack2(KV{}, y.z, y.w));
-                    *reinterpret_cast<uint4 *>(qs + (c8 / 8) * (BM * 128) + sw128(r, c8 % 8)) = v;
-                }
-            } else if (valid) {
-                const uint16_t *src = static_cast<const uint16_t *>(a.q) + t.lane * a.q_lane +
-                                      (int64_t)head * a.q_head + (int64_t)row * a.q_row;
-#pragma unroll 4
-                for (int c8 = 0; c8 < D / 8; ++c8)
-                    *reinterpret_cast<uint4 *>(qs + (c8 / 8) * (BM * 128) + sw128(r, c8 % 8)) =
-                        ld_nc_v4(src + c8 * 8);
-            } else {
-                for (int c8 = 0; c8 < D / 8; ++c8)
-                    *reinterpret_cast<uint4 *>(qs + (c8 / 8) * (BM * 128) + sw128(r, c8 % 8)) =
-                        make_uint4(0, 0, 0, 0);
-            }
-            tc::fence_async_smem();
-            tc::mbar_arrive(q_full);
         }
+        if constexpr (C::QTM)
+            tc::tmem_st_wait();
+        else
+            tc::fence_async_smem();
+        tc::tc_fence_before();
+        tc::mbar_arrive(q_full);
+
+        // ---- key tiles
         const uint16_t *mrow = valid ? a.mask + t.lane * a.m_lane + (int64_t)head * a.m_head +
                                            (int64_t)row * a.m_row
                                      : nullptr;
         const bool m_vec = valid && (reinterpret_cast<uintptr_t>(mrow) & 15) == 0;
         float m_ref = kNegInf, l = 0.f;
         int i = 0;
-        bool ok = true;
-        for (int j = jb; j < je; ++j) {
-            const int code = tile_code<BN>(a, cg, j);
-            if (!code) continue;
+        for (; ok && i < n_vis; ++i) {
+            const int j = tile_at(i);
+            const int code = (list[i] & 0x8000) ? 2 : 1;
             ok = __all_sync(0xffffffffu, wt.wait(s_full(i & 1), (i >> 1) & 1));
             if (!ok) break;
             tc::tc_fence_after();
             float s[BN];
+            {
+                uint32_t rr[BN];
 #pragma unroll
-            for (int cb = 0; cb < BN / 32; ++cb) {
-                uint32_t rr[32];
-                tc::tmem_ld32(tm_s + (uint32_t)(i & 1) * BN + cb * 32 + lane_base, rr);
+                for (int cb = 0; cb < BN / 32; ++cb)
+                    tc::tmem_ld32(tm_s + (uint32_t)(i & 1) * BN + cb * 32 + lane_base,
+                                  *reinterpret_cast<uint32_t(*)[32]>(rr + cb * 32));
                 tc::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[cb * 32 + e] = __uint_as_float(rr[e]);
+                for (int c = 0; c < BN; ++c) {
+                    asm volatile("" : "+r"(rr[c]));  // keep every use after the wait
+                    s[c] = __uint_as_float(rr[c]);
+                }
             }
             if (!valid) {
 #pragma unroll
@@ -580,9 +636,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    : kNegInf;
                 }
             }
-            float mx = kNegInf;
+            // row max with four independent chains
+            float mq[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-            for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+            for (int c = 4; c < BN; c += 4) {
+                mq[0] = fmaxf(mq[0], s[c]);
+                mq[1] = fmaxf(mq[1], s[c + 1]);
+                mq[2] = fmaxf(mq[2], s[c + 2]);
+                mq[3] = fmaxf(mq[3], s[c + 3]);
+            }
+            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             float factor = 1.f;
             bool resc = false;
             if (m_ref == kNegInf) {
@@ -594,23 +657,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float mu = m_ref == kNegInf ? 0.f : m_ref;
             uint32_t pk[BN / 2];
-            float rowsum = 0.f;
+            float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < BN; c += 2) {
+            for (int c = 0; c < BN; c += 4) {
                 const float p0 = ex2(s[c] - mu), p1 = ex2(s[c + 1] - mu);
-                rowsum += p0 + p1;
+                const float p2 = ex2(s[c + 2] - mu), p3 = ex2(s[c + 3] - mu);
+                rs[0] += p0;
+                rs[1] += p1;
+                rs[2] += p2;
+                rs[3] += p3;
                 pk[c / 2] = pack2(KV{}, p0, p1);
+                pk[c / 2 + 1] = pack2(KV{}, p2, p3);
             }
-            l = l * factor + rowsum;
+            l = l * factor + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
             // P.V of the previous tile must be done before O is rescaled, and, when P
             // lives in shared memory (one buffer), before P is overwritten.  A P kept in
             // TMEM goes over this tile's own S buffer, which the previous P.V does not
             // read, so without a rescale the softmax runs ahead of the tensor pipe.
-            // (P.V of this tile cannot complete before P is written, so the parity
-            // of o_done is never ambiguous.)
+            // Parity waits are unambiguous: S(i) complete implies every MMA issued
+            // before it (P.V up to tile i-2) completed, and P.V(i) cannot complete
+            // before P(i) is written.
             const bool any_resc = __any_sync(0xffffffffu, resc);
             if (i > 0 && (!C::PTM || any_resc)) {
-                ok = __all_sync(0xffffffffu, wt.wait(o_done, (i - 1) & 1));
+                ok = __all_sync(0xffffffffu, wt.wait(o_done((i - 1) & 1), ((i - 1) >> 1) & 1));
                 if (!ok) break;
                 tc::tc_fence_after();
             }
@@ -621,7 +690,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::tmem_ld32(tm_o + cb * 32 + lane_base, rr);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
+                    for (int e = 0; e < 32; ++e) {
+                        asm volatile("" : "+r"(rr[e]));
+                        rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
+                    }
                     tc::tmem_st32(tm_o + cb * 32 + lane_base, rr);
                 }
                 tc::tmem_st_wait();
@@ -629,12 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (C::PTM) {
                 // P over the first BN/2 columns of the S buffer it came from
 #pragma unroll
-                for (int cb = 0; cb < BN / 64; ++cb) {
-                    uint32_t w[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) w[e] = pk[cb * 32 + e];
-                    tc::tmem_st32(tm_s + (uint32_t)(i & 1) * BN + cb * 32 + lane_base, w);
-                }
+                for (int cb = 0; cb < BN / 64; ++cb)
+                    tc::tmem_st32(tm_s + (uint32_t)(i & 1) * BN + cb * 32 + lane_base,
+                                  *reinterpret_cast<const uint32_t(*)[32]>(pk + cb * 32));
                 tc::tmem_st_wait();
             } else {
                 uint8_t *ps = smem + L::kP;
@@ -645,16 +714,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_async_smem();
             }
             tc::tc_fence_before();
-            tc::mbar_arrive(p_full);
-            ++i;
+            tc::mbar_arrive(p_full(i & 1));
         }
-        // ---- epilogue
-        if (ok && i > 0) {
-            ok = __all_sync(0xffffffffu, wt.wait(o_done, (i - 1) & 1));
+
+        // ---- epilogue: both outstanding P.V (tiles n-2 and n-1) must be complete
+        const int n_done = i;
+        if (ok && n_done > 0) {
+            ok = __all_sync(0xffffffffu, wt.wait(o_done((n_done - 1) & 1), ((n_done - 1) >> 1) & 1));
+            if (ok && n_done >= 2)
+                ok = __all_sync(0xffffffffu,
+                                wt.wait(o_done((n_done - 2) & 1), ((n_done - 2) >> 1) & 1));
             tc::tc_fence_after();
         }
-        if (ok) {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+        const bool have_o = ok && n_done > 0;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (a.o_tma) {
+            // O -> shared memory ([128 rows][32 f32] boxes, 128-byte swizzle) -> TMA store.
+            // The ring (or, at head_dim 512, the Q tile) is idle once the last P.V is done.
+            uint8_t *stg = smem + (D == 512 ? L::kQ : L::kStages);
+#pragma unroll 1
+            for (int cb = 0; cb < DO / 32; ++cb) {
+                uint32_t rr[32];
+                if (have_o) {
+                    tc::tmem_ld32(tm_o + cb * 32 + lane_base, rr);
+                    tc::tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[e] = 0u;
+                }
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    asm volatile("" : "+r"(rr[4 * c4]), "+r"(rr[4 * c4 + 1]), "+r"(rr[4 * c4 + 2]),
+                                 "+r"(rr[4 * c4 + 3]));
+                    *reinterpret_cast<float4 *>(stg + cb * 16384 + r * 128 + ((c4 ^ (r & 7)) << 4)) =
+                        make_float4(__uint_as_float(rr[4 * c4]) * inv, __uint_as_float(rr[4 * c4 + 1]) * inv,
+                                    __uint_as_float(rr[4 * c4 + 2]) * inv,
+                                    __uint_as_float(rr[4 * c4 + 3]) * inv);
+                }
+            }
+            tc::fence_async_smem();
+            tc::named_bar(1, BM);
+            if (r == 0 && !*abort_flag) {
+#pragma unroll 1
+                for (int cb = 0; cb < DO / 32; ++cb)
+                    tc::tma_store_3d(&tmo, smem_u32(stg + cb * 16384), d_off + cb * 32,
+                                     a.o_rows_dim1 ? q_row0 : q_head0, a.o_rows_dim1 ? q_head0 : q_row0);
+                tc::bulk_commit();
+                tc::bulk_wait0();
+            }
+        } else if (ok) {
             float *dst;
             if (a.splits == 1) {
                 dst = valid ? a.o + t.lane * a.o_lane + (int64_t)head * a.o_head +
@@ -668,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int cb = 0; cb < DO / 32; ++cb) {
                 uint32_t rr[32];
-                if (i > 0) {
+                if (have_o) {
                     tc::tmem_ld32(tm_o + cb * 32 + lane_base, rr);
                     tc::tmem_ld_wait();
                 } else {
@@ -677,10 +785,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (dst) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
+                    for (int e = 0; e < 32; e += 4) {
+                        asm volatile("" : "+r"(rr[e]), "+r"(rr[e + 1]), "+r"(rr[e + 2]), "+r"(rr[e + 3]));
                         *reinterpret_cast<float4 *>(dst + cb * 32 + e) =
                             make_float4(__uint_as_float(rr[e]) * inv, __uint_as_float(rr[e + 1]) * inv,
                                         __uint_as_float(rr[e + 2]) * inv, __uint_as_float(rr[e + 3]) * inv);
+                    }
                 }
             }
         }
@@ -775,6 +885,7 @@ Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, i
         p.splits = s;
     }
     p.bps = (p.n_blk + p.splits - 1) / p.splits;
+    if (p.bps > kMaxListTiles) p.bps = kMaxListTiles;  // a unit's tile list fits in shared memory
     p.splits = (p.n_blk + p.bps - 1) / p.bps;
     p.codes_bytes = align256((size_t)p.code_groups * p.code_cols);
     if (p.splits > 1) {
@@ -807,28 +918,30 @@ bool rows_first(int heads, int64_t row_stride, int64_t head_stride) {
     return heads == 1 || row_stride <= head_stride;
 }
 
-bool make_kv_map(CUtensorMap *m, const void *base, bool bf16, int d, int rows, int heads,
-                 int64_t row_stride, int64_t head_stride, int bn) {
+// A 3-D tiled map over a [rows][heads][d] view with element strides (row,
+// head): box = box_inner columns x box_rows rows x one head, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, int d, int rows,
+              int heads, int64_t row_stride, int64_t head_stride, int box_inner, int box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     const bool rf = rows_first(heads, row_stride, head_stride);
     const int64_t hs = heads > 1 ? head_stride : row_stride * rows;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)(rf ? rows : heads),
                           (cuuint64_t)(rf ? heads : rows)};
-    cuuint64_t strides[2] = {(cuuint64_t)(rf ? row_stride : hs) * 2,
-                             (cuuint64_t)(rf ? hs : row_stride) * 2};
-    cuuint32_t box[3] = {64, rf ? (cuuint32_t)bn : 1u, rf ? 1u : (cuuint32_t)bn};
+    cuuint64_t strides[2] = {(cuuint64_t)(rf ? row_stride : hs) * esize,
+                             (cuuint64_t)(rf ? hs : row_stride) * esize};
+    cuuint32_t box[3] = {(cuuint32_t)box_inner, rf ? (cuuint32_t)box_rows : 1u,
+                         rf ? 1u : (cuuint32_t)box_rows};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                    const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 template <int D, class KV>
-cudaError_t run_attn(const AttnArgs &a, const CUtensorMap &mk, const CUtensorMap &mv, int units,
-                     int tiles, cudaStream_t stream) {
+cudaError_t run_attn(const AttnArgs &a, const CUtensorMap *maps, int units, int tiles,
+                     cudaStream_t stream) {
     auto kern = attn_kernel<D, KV>;
     static bool configured = false;
     if (!configured) {
@@ -838,7 +951,7 @@ cudaError_t run_attn(const AttnArgs &a, const CUtensorMap &mk, const CUtensorMap
         configured = true;
     }
     timing_mark(true, stream);
-    kern<<<units, kThreads, Layout<D>::kBytes, stream>>>(a, mk, mv);
+    kern<<<units, kThreads, Layout<D>::kBytes, stream>>>(a, maps[0], maps[1], maps[2], maps[3]);
     timing_mark(false, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.splits == 1) return e;
@@ -905,15 +1018,32 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     a.ws_lse = pl.splits > 1 ? reinterpret_cast<float *>(ws + pl.codes_bytes + pl.part_o_bytes) : nullptr;
     a.status = p.status;
 
-    CUtensorMap mk, mv;
+    // K, V (and, for single-head 128-row prefill tiles, f32 Q and O) tensor maps
+    CUtensorMap maps[4];
+    memset(maps, 0, sizeof maps);
     const int heads = p.lanes * p.n_kv_heads;
+    const CUtensorMapDataType kvt =
+        a.kv_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     a.k_rows_dim1 = rows_first(heads, p.k_row_stride, p.k_head_stride) ? 1 : 0;
     a.v_rows_dim1 = rows_first(heads, p.v_row_stride, p.v_head_stride) ? 1 : 0;
-    if (!make_kv_map(&mk, p.k, a.kv_bf16, p.head_dim, p.kv_rows, heads, p.k_row_stride,
-                     p.k_head_stride, pl.bn) ||
-        !make_kv_map(&mv, p.v, a.kv_bf16, p.head_dim, p.kv_rows, heads, p.v_row_stride,
-                     p.v_head_stride, pl.bn))
+    if (!make_map(&maps[0], p.k, kvt, 2, p.head_dim, p.kv_rows, heads, p.k_row_stride,
+                  p.k_head_stride, 64, pl.bn) ||
+        !make_map(&maps[1], p.v, kvt, 2, p.head_dim, p.kv_rows, heads, p.v_row_stride,
+                  p.v_head_stride, 64, pl.bn))
         return cudaErrorInvalidValue;
+    const bool single_head_tiles = p.lanes == 1 && pl.heads_per_tile == 1 && pl.rows_per_head == BM;
+    if (single_head_tiles && p.q_is_f32 &&
+        make_map(&maps[2], p.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.head_dim, p.rows, p.n_heads,
+                 p.q_row_stride, p.q_head_stride, 32, BM)) {
+        a.q_tma = 1;
+        a.q_rows_dim1 = rows_first(p.n_heads, p.q_row_stride, p.q_head_stride) ? 1 : 0;
+    }
+    if (single_head_tiles && pl.splits == 1 &&
+        make_map(&maps[3], p.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.head_dim, p.rows, p.n_heads,
+                 p.o_row_stride, p.o_head_stride, 32, BM)) {
+        a.o_tma = 1;
+        a.o_rows_dim1 = rows_first(p.n_heads, p.o_row_stride, p.o_head_stride) ? 1 : 0;
+    }
 
     classify_kernel<<<dim3(pl.code_groups, pl.code_cols), BM, 0, stream>>>(a, const_cast<uint8_t *>(a.codes));
     cudaError_t e = cudaGetLastError();
@@ -922,14 +1052,14 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     const bool bf = a.kv_bf16;
     switch (p.head_dim) {
         case 128:
-            return bf ? run_attn<128, BF16>(a, mk, mv, units, pl.tiles, stream)
-                      : run_attn<128, F16>(a, mk, mv, units, pl.tiles, stream);
+            return bf ? run_attn<128, BF16>(a, maps, units, pl.tiles, stream)
+                      : run_attn<128, F16>(a, maps, units, pl.tiles, stream);
         case 256:
-            return bf ? run_attn<256, BF16>(a, mk, mv, units, pl.tiles, stream)
-                      : run_attn<256, F16>(a, mk, mv, units, pl.tiles, stream);
+            return bf ? run_attn<256, BF16>(a, maps, units, pl.tiles, stream)
+                      : run_attn<256, F16>(a, maps, units, pl.tiles, stream);
         case 512:
-            return bf ? run_attn<512, BF16>(a, mk, mv, units, pl.tiles, stream)
-                      : run_attn<512, F16>(a, mk, mv, units, pl.tiles, stream);
+            return bf ? run_attn<512, BF16>(a, maps, units, pl.tiles, stream)
+                      : run_attn<512, F16>(a, maps, units, pl.tiles, stream);
         default:
             return cudaErrorInvalidValue;
     }

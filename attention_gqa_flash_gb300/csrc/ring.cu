@@ -36,8 +36,11 @@ __device__ __forceinline__ uint4 f32x8_to_bf16x8(const float *src) {
                       pack_bf16x2(b.z, b.w));
 }
 
-// Packed K/V: one thread per 8-element chunk of a packed column, for K and V.
-// Packed Q: one thread per 8-element chunk of a packed query row.
+// Grid row y < B*HK packs the K/V columns of (lane, KV head) y; grid row
+// B*HK + (b*H + qh) packs the query rows of head qh of lane b.  Within a grid
+// row every thread moves one 8-element chunk (16 bytes of output) per step, so
+// the index arithmetic is 32-bit with a compile-time chunk count.
+template <int D>
 __global__ void __launch_bounds__(256) pack_attention_kernel(
     const uint16_t *__restrict__ ring_k, const uint16_t *__restrict__ ring_v,
     const float *__restrict__ cur_q, const float *__restrict__ cur_k,
@@ -45,54 +48,46 @@ __global__ void __launch_bounds__(256) pack_attention_kernel(
     const uint32_t *__restrict__ write_positions, uint16_t *__restrict__ packed_q,
     uint16_t *__restrict__ packed_k, uint16_t *__restrict__ packed_v, RingGeom g,
     int32_t *status) {
-    const int chunks = g.D / 8;
-    const int64_t kv_work = (int64_t)g.B * g.HK * g.K * chunks;
-    const int64_t q_work = (int64_t)g.B * g.H * g.R * chunks;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < kv_work + q_work;
-         t += stride) {
-        if (t < kv_work) {
-            const int ch = (int)(t % chunks);
-            const int64_t col_id = t / chunks;  // (b, kh, c)
-            const int c = (int)(col_id % g.K);
-            const int64_t bk = col_id / g.K;  // b * HK + kh
-            const int kh = (int)(bk % g.HK);
-            const int b = (int)(bk / g.HK);
-            const int64_t out = col_id * g.D + ch * 8;
+    constexpr int chunks = D / 8;
+    const int y = blockIdx.y;
+    const int step = gridDim.x * blockDim.x;
+    if (y < g.B * g.HK) {
+        const int b = y / g.HK, kh = y - (y / g.HK) * g.HK;
+        int len, wp;
+        ring_counters(cache_lengths, write_positions, b, g.W,
+                      blockIdx.x == 0 && threadIdx.x == 0 ? status : nullptr, len, wp);
+        const uint16_t *rk = ring_k + (int64_t)y * g.W * D;
+        const uint16_t *rv = ring_v + (int64_t)y * g.W * D;
+        uint16_t *pk = packed_k + (int64_t)y * g.K * D;
+        uint16_t *pv = packed_v + (int64_t)y * g.K * D;
+        const int work = g.K * chunks;
+        for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < work; u += step) {
+            const int c = u / chunks, ch = u % chunks;
             uint4 vk, vv;
             if (c < g.R) {
-                const int64_t src = (((int64_t)b * g.R + c) * g.HK + kh) * g.D + ch * 8;
+                const int64_t src = (((int64_t)b * g.R + c) * g.HK + kh) * D + ch * 8;
                 vk = f32x8_to_bf16x8(cur_k + src);
                 vv = f32x8_to_bf16x8(cur_v + src);
+            } else if (c - g.R < len) {
+                int slot = wp - 1 - (c - g.R);
+                slot += (slot < 0) ? g.W : 0;
+                vk = ld_nc_v4(rk + (int64_t)slot * D + ch * 8);
+                vv = ld_nc_v4(rv + (int64_t)slot * D + ch * 8);
             } else {
-                int len, wp;
-                ring_counters(cache_lengths, write_positions, b, g.W, ch == 0 ? status : nullptr,
-                              len, wp);
-                const int j = c - g.R;
-                if (j < len) {
-                    int slot = wp - 1 - j;
-                    slot += (slot < 0) ? g.W : 0;
-                    slot += (slot < 0) ? g.W : 0;
-                    const int64_t src = (bk * g.W + slot) * g.D + ch * 8;
-                    vk = ld_nc_v4(ring_k + src);
-                    vv = ld_nc_v4(ring_v + src);
-                } else {
-                    vk = make_uint4(0, 0, 0, 0);
-                    vv = vk;
-                }
+                vk = make_uint4(0, 0, 0, 0);
+                vv = vk;
             }
-            st_v4(packed_k + out, vk);
-            st_v4(packed_v + out, vv);
-        } else {
-            const int64_t u = t - kv_work;
-            const int ch = (int)(u % chunks);
-            const int64_t row_id = u / chunks;  // (b, qh, r)
-            const int r = (int)(row_id % g.R);
-            const int64_t bq = row_id / g.R;
-            const int qh = (int)(bq % g.H);
-            const int b = (int)(bq / g.H);
-            const int64_t src = (((int64_t)b * g.R + r) * g.H + qh) * g.D + ch * 8;
-            st_v4(packed_q + row_id * g.D + ch * 8, f32x8_to_bf16x8(cur_q + src));
+            st_v4(pk + (int64_t)u * 8, vk);
+            st_v4(pv + (int64_t)u * 8, vv);
+        }
+    } else {
+        const int bq = y - g.B * g.HK;  // b * H + qh
+        const int b = bq / g.H, qh = bq - (bq / g.H) * g.H;
+        const int work = g.R * chunks;
+        for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < work; u += step) {
+            const int r = u / chunks, ch = u % chunks;
+            const int64_t src = (((int64_t)b * g.R + r) * g.H + qh) * D + ch * 8;
+            st_v4(packed_q + ((int64_t)bq * g.R + r) * D + ch * 8, f32x8_to_bf16x8(cur_q + src));
         }
     }
 }
@@ -105,39 +100,43 @@ __global__ void __launch_bounds__(256) fill_mask_kernel(const uint32_t *__restri
                                                         int32_t *status) {
     const int64_t total = (int64_t)g.B * g.H * g.R * g.K;
     const int64_t nchunks = (total + 7) / 8;
-    const int64_t rows_per_lane = (int64_t)g.H * g.R;
     if (blockIdx.x == 0 && threadIdx.x < g.B) {
         if (cache_lengths[threadIdx.x] > (uint32_t)g.W) raise_flag(status, GQA_FLAG_RING_CLAMPED);
     }
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < nchunks; t += stride) {
+        // decompose the chunk's first element once, then step through the 8 elements
         const int64_t e0 = t * 8;
-        int64_t row = e0 / g.K;
+        const int64_t row = e0 / g.K;
         int c = (int)(e0 - row * g.K);
+        int r = (int)(row % g.R);
+        const int64_t bh = row / g.R;
+        int b = (int)(bh / g.H);
+        int hh = (int)(bh - (int64_t)b * g.H);
+        auto len_of = [&](int lane) {
+            const uint32_t l = cache_lengths[lane];
+            return l > (uint32_t)g.W ? g.W : (int)l;
+        };
+        int len = b < g.B ? len_of(b) : 0;
         uint32_t w[4];
-        int cached_b = -1, len = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            uint16_t val = 0;
-            if (e0 + i < total) {
-                const int b = (int)(row / rows_per_lane);
-                if (b != cached_b) {
-                    uint32_t l = cache_lengths[b];
-                    len = l > (uint32_t)g.W ? g.W : (int)l;
-                    cached_b = b;
-                }
-                const int r = (int)(row % g.R);
-                const int j = c - g.R;
-                const bool visible = c < g.R || (j < len && r + j + 1 < g.W);
-                val = visible ? 0x0000 : 0xff80;
-            }
+            const int j = c - g.R;
+            const bool visible = c < g.R || (j < len && r + j + 1 < g.W);
+            const uint32_t val = visible ? 0x0000u : 0xff80u;
             if (i & 1)
-                w[i / 2] |= (uint32_t)val << 16;
+                w[i / 2] |= val << 16;
             else
                 w[i / 2] = val;
             if (++c == g.K) {
                 c = 0;
-                ++row;
+                if (++r == g.R) {
+                    r = 0;
+                    if (++hh == g.H) {
+                        hh = 0;
+                        if (++b < g.B) len = len_of(b);
+                    }
+                }
             }
         }
         if (e0 + 8 <= total) {
@@ -211,11 +210,23 @@ cudaError_t launch_pack_attention(const uint16_t *ring_k, const uint16_t *ring_v
                                   uint16_t *packed_q, uint16_t *packed_k, uint16_t *packed_v,
                                   const gqa_ring_params &p, int32_t *status, cudaStream_t stream) {
     RingGeom g = geom_of(p);
-    int64_t work = (int64_t)g.B * g.HK * g.K * (g.D / 8) + (int64_t)g.B * g.H * g.R * (g.D / 8);
+    // x blocks per slab: enough for about 8 resident CTAs per SM overall, and no
+    // more than one chunk per thread of the largest slab
+    const int slabs = g.B * g.HK + g.B * g.H;
+    const int per_slab = (int)(((int64_t)g.K * (g.D / 8) + 255) / 256);
+    int bx = (sm_count() * 8 + slabs - 1) / slabs;
+    if (bx > per_slab) bx = per_slab;
+    if (bx < 1) bx = 1;
+    const dim3 grid(bx, slabs);
     timing_mark(true, stream);
-    pack_attention_kernel<<<grid_for(work, sm_count()), 256, 0, stream>>>(
-        ring_k, ring_v, cur_q, cur_k, cur_v, cache_lengths, write_positions, packed_q, packed_k,
-        packed_v, g, status);
+    if (g.D == 128)
+        pack_attention_kernel<128><<<grid, 256, 0, stream>>>(ring_k, ring_v, cur_q, cur_k, cur_v,
+                                                             cache_lengths, write_positions, packed_q,
+                                                             packed_k, packed_v, g, status);
+    else
+        pack_attention_kernel<256><<<grid, 256, 0, stream>>>(ring_k, ring_v, cur_q, cur_k, cur_v,
+                                                             cache_lengths, write_positions, packed_q,
+                                                             packed_k, packed_v, g, status);
     timing_mark(false, stream);
     return cudaGetLastError();
 }
