@@ -6,21 +6,25 @@
 // n_heads / n_kv_heads query heads and an additive f16 (or bf16) mask; a
 // query row whose mask hides every key yields zeros.
 //
-// Kernel structure (one CTA = one 128-row query tile, 192 threads):
-//   warps 0-3  softmax: each thread owns one query row = one TMEM lane.  It
-//              stages its Q row (f32/bf16 -> f16/bf16) into shared memory,
-//              reads S from TMEM, applies scale and mask, runs the online
-//              softmax in the exp2 domain with lazy rescaling of O (only when
-//              the running max grows by more than 2^8), writes P to shared
-//              memory, and finally normalises O out of TMEM into global memory.
-//   warp 4     TMA producer: streams K and V tiles (128-byte swizzled) through
-//              a ring of 32 KiB stages guarded by full/empty mbarriers.
-//   warp 5     MMA issuer: owns the TMEM allocation; S = Q K^T into one of two
-//              TMEM buffers (so QK^T of the next tile overlaps the softmax of
-//              this one), then O += P V into the TMEM accumulator.
-// Tiles of keys whose mask is entirely -inf are skipped (a classification
-// pre-pass reads the mask once, 64 keys at a time); tiles whose mask is
-// entirely zero do not read the mask at all.
+// Kernel structure (one CTA = one 128-row query tile, 320 threads):
+//   warps 0-7  softmax: two threads per query row (warp w and w+4 share the
+//              TMEM lanes of rows 32(w%4)..+31, each takes half of the 128
+//              columns of a key tile).  They stage Q (f32/bf16 -> f16/bf16),
+//              read S from TMEM, apply scale and mask, run the online softmax
+//              in the exp2 domain with lazy rescaling of O (only when the row
+//              maximum grows by more than 2^8; the two halves agree on the
+//              maximum through shared memory), write P over S in TMEM, and
+//              finally normalise O into global memory.
+//   warp 8     TMA producer: streams Q (f32 prefill), K and V tiles (128-byte
+//              swizzle) through a ring of 32 KiB stages guarded by full/empty
+//              mbarriers.
+//   warp 9     MMA issuer: owns the TMEM allocation; S = Q K^T into one of two
+//              TMEM buffers (the next tile's Q K^T overlaps this tile's
+//              softmax), then O += P V with P read from TMEM.
+// Key tiles are 128 wide so every MMA has N = 128 (narrower tcgen05 shapes
+// run far below the tensor-core rate).  Tiles whose mask is entirely -inf are
+// skipped (a classification pre-pass reads the mask once, 64 keys at a time);
+// tiles whose mask is entirely zero do not read the mask at all.
 // head_dim 512 keeps a 128x512 f32 accumulator out of reach of the 512 TMEM
 // columns, so each query tile is processed as two units, one per 256-wide
 // half of the output, both recomputing S.
@@ -40,69 +44,54 @@
 namespace gqa {
 namespace {
 
-constexpr int BM = 128;
-constexpr int kThreads = 192;
-constexpr int kStageBytes = 32768;
+constexpr int BM = 128;                  // query rows per tile (TMEM lanes)
+constexpr int BN = 128;                  // keys per tile
+constexpr int kSoftmaxWarps = 8;
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kStageBytes = 32768;       // 128 rows x 128 columns of 16-bit, or 128 x 64 f32
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-
-// Q and P are the A operand of the two MMAs.  With GQA_TMEM_A they live in
-// tensor memory (written by the softmax threads with tcgen05.st), so the MMAs
-// read only K or V from shared memory and shared memory holds only the K/V
-// ring.  head_dim 512 keeps Q in shared memory: its 256 TMEM columns do not
-// fit next to O and S.
-#ifndef GQA_TMEM_A
-#define GQA_TMEM_A 1
-#endif
 // key tiles one CTA may visit (the list of visible tiles lives in shared memory)
-constexpr int kMaxListTiles = 768;
-constexpr int kSmemBudget = 232448 - 1024 - 256 - 2 * kMaxListTiles;
+constexpr int kMaxListTiles = 256;
+// shared memory left for the Q tile and the ring after barriers, the row-max
+// exchange and the tile list (the dynamic shared memory base is 1024-aligned)
+constexpr int kSmemBudget = 232448 - 256 - 2048 - 2 * kMaxListTiles;
 
+// Per head_dim: KSUB stages per K tile, VSUB per V tile (DO output columns),
+// Q in TMEM only at head_dim 128 (at 256 and 512, O and two S buffers fill
+// the 512 TMEM columns).
 template <int D>
-struct Tiles;
-template <>
-struct Tiles<128> {
-    static constexpr int BN = 128, DS = 128, DO = 128, KSUB = 1;
-};
-template <>
-struct Tiles<256> {
-    static constexpr int BN = 64, DS = 256, DO = 256, KSUB = 1;
-};
-template <>
-struct Tiles<512> {
-    static constexpr int BN = 64, DS = 256, DO = 256, KSUB = 2;
-};
-template <int D>
-struct Cfg : Tiles<D> {
-    using T = Tiles<D>;
-    static constexpr bool QTM = GQA_TMEM_A && D <= 256;  // Q in TMEM
-    static constexpr bool PTM = GQA_TMEM_A;              // P in TMEM (over its S buffer)
+struct Cfg {
+    static constexpr int DO = D == 512 ? 256 : D;
+    static constexpr int KSUB = D / 128, VSUB = DO / 128;
+    static constexpr bool QTM = D == 128;
     static constexpr int QBYTES = QTM ? 0 : BM * D * 2;
-    static constexpr int PBYTES = PTM ? 0 : BM * T::BN * 2;
-    static constexpr int STAGES = (kSmemBudget - QBYTES - PBYTES) / kStageBytes;
-    // TMEM columns: O [0, DO), S0/S1 [DO, DO + 2 BN), Q [DO + 2 BN, + D/2)
-    static constexpr int kColS = T::DO, kColQ = T::DO + 2 * T::BN;
+    static constexpr int STAGES = (kSmemBudget - QBYTES) / kStageBytes;
+    // TMEM columns: O [0, DO), S0/S1 [DO, DO + 256), Q [DO + 256, + D/2)
+    static constexpr int kColS = DO, kColQ = DO + 2 * BN;
     static_assert(kColQ + (QTM ? D / 2 : 0) <= 512, "TMEM overflow");
-    static_assert(STAGES >= 2, "ring too small");
+    static_assert(STAGES >= 3, "ring too small");
 };
 
 // shared-memory carve-up (offsets from a 1024-byte aligned base)
 template <int D>
 struct Layout {
     using C = Cfg<D>;
-    static constexpr int kQ = 0;                          // D/64 tiles of [128][64] (if in smem)
-    static constexpr int kP = kQ + C::QBYTES;             // BN/64 tiles of [128][64] (if in smem)
-    static constexpr int kStages = kP + C::PBYTES;        // STAGES x 32 KiB
+    static constexpr int kQ = 0;                     // D/64 tiles of [128][64] (head_dim >= 256)
+    static constexpr int kStages = kQ + C::QBYTES;   // STAGES x 32 KiB
     static constexpr int kBars = kStages + C::STAGES * kStageBytes;
     // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], o_done[2], mma_fin
     static constexpr int kNumBars = 2 * C::STAGES + 8;
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kNumVis = kAbort + 4;
-    static constexpr int kList = kNumVis + 4;  // visible key tiles: uint16 each
+    static constexpr int kXchg = kNumVis + 8;      // row-max exchange: [2 tiles][2 halves][128] f32
+    static constexpr int kList = kXchg + 2 * 2 * BM * 4;  // visible key tiles: uint16 each
     static constexpr int kEnd = kList + 2 * kMaxListTiles;
-    static constexpr int kBytes = kEnd + 1024;  // + alignment slack
+    static constexpr int kBytes = kEnd;
     static_assert(kBytes <= 232448, "shared memory overflow");
 };
 
@@ -163,9 +152,8 @@ __device__ __forceinline__ int code_group(const AttnArgs &a, const Tile &t) {
     return ((t.lane * a.n_kv_heads + t.kh) * a.head_tiles + t.ht) * a.row_tiles + t.rt;
 }
 
-// code of key tile j (BN keys = BN/64 classification blocks)
-// (a tile that mixes skipped and mask-free blocks still has to apply the mask)
-template <int BN>
+// code of key tile j (BN keys = two classification blocks of 64); a tile that
+// mixes skipped and mask-free blocks still has to apply the mask
 __device__ __forceinline__ int tile_code(const AttnArgs &a, int cg, int j) {
     int all_skip = 1, all_free = 1;
 #pragma unroll
@@ -281,6 +269,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int c16) {
     return (uint32_t)(r * 128 + ((c16 ^ (r & 7)) << 4));
 }
 
+
 template <int D, class KV>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
@@ -288,13 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tmo) {
     using C = Cfg<D>;
     using L = Layout<D>;
-    constexpr int BN = C::BN, DS = C::DS, DO = C::DO, KSUB = C::KSUB, NS = C::STAGES;
+    constexpr int DO = C::DO, KSUB = C::KSUB, VSUB = C::VSUB, NS = C::STAGES;
     constexpr bool kBf16 = KV::kind == GQA_DTYPE_BF16;
     constexpr int kQStages = D / 64;  // an f32 Q tile crosses the ring 64 columns per stage
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem =
-        reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
     auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
     auto full = [&](int s) { return bar(s); };
@@ -307,8 +294,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlot);
     int *n_vis_smem = reinterpret_cast<int *>(smem + L::kNumVis);
+    float *xchg = reinterpret_cast<float *>(smem + L::kXchg);
     uint16_t *list = reinterpret_cast<uint16_t *>(smem + L::kList);
     const Waiter wt{abort_flag, a.status, kWaitLimitNs};
+    // the swizzled layouts below assume a 1024-byte aligned shared-memory base
+    if (sbase & 1023u) {
+        if (threadIdx.x == 0) raise_flag(a.status, GQA_FLAG_TIMEOUT);
+        return;
+    }
 
     // ---- which unit: (query tile, output half, key split); heavy row tiles first
     int idx = blockIdx.x;
@@ -333,22 +326,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(full(s), 1);
             tc::mbar_init(empty(s), 1);
         }
-        tc::mbar_init(q_full, BM);
+        tc::mbar_init(q_full, kSoftmaxThreads);
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(s_full(b), 1);
-            tc::mbar_init(p_full(b), BM);
+            tc::mbar_init(p_full(b), kSoftmaxThreads);
             tc::mbar_init(o_done(b), 1);
         }
         tc::mbar_init(mma_fin, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // visible key tiles of this unit in order: (j - jb) | 0x8000 when the mask applies
         int n = 0;
         for (int base = jb; base < je; base += 32) {
             const int j = base + lane;
-            const int code = j < je ? tile_code<BN>(a, cg, j) : 0;
+            const int code = j < je ? tile_code(a, cg, j) : 0;
             const unsigned vis = __ballot_sync(0xffffffffu, code != 0);
             if (code)
                 list[n + __popc(vis & ((1u << lane) - 1u))] =
@@ -357,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) *n_vis_smem = n;
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc::tmem_alloc<512>(smem_u32(tslot));
         tc::tmem_relinquish();
     }
@@ -367,11 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tslot;
     const uint32_t tm_o = tmem;             // O: DO columns
     const uint32_t tm_s = tmem + C::kColS;  // S: two buffers of BN columns (P over S)
-    const uint32_t tm_q = tmem + C::kColQ;  // Q: D/2 columns (when in TMEM)
+    const uint32_t tm_q = tmem + C::kColQ;  // Q: D/2 columns (head_dim 128)
     const int n_vis = *n_vis_smem;
     auto tile_at = [&](int v) { return jb + (list[v] & 0x7fff); };
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tc::prefetch_tmap(&tmk);
@@ -385,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             bool ok = true;
-            // f32 Q tile first (consumed by the softmax warps): [128 rows][32 cols] boxes
+            // f32 Q tile first (consumed by the softmax warps): [128 rows][32 f32] boxes
             if (a.q_tma) {
                 tc::prefetch_tmap(&tmq);
                 for (int qs = 0; qs < kQStages && ok; ++qs) {
@@ -400,34 +393,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     next();
                 }
             }
-            // one stage: DS/64 boxes of [BN rows][64 columns] of K (sub-stage ks) or V
-            auto load = [&](int j, bool is_v, int ks) -> bool {
+            // one stage: two boxes of [BN rows][64 columns] of K or V starting at column d0
+            auto load = [&](int j, bool is_v, int d0) -> bool {
                 if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
                 const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
                 tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
-                const int dc0 = is_v ? d_off / 64 : ks * (DS / 64);
                 const int rows_dim1 = is_v ? a.v_rows_dim1 : a.k_rows_dim1;
                 const int c1 = rows_dim1 ? j * BN : head_idx;
                 const int c2 = rows_dim1 ? head_idx : j * BN;
 #pragma unroll
-                for (int c = 0; c < DS / 64; ++c)
+                for (int c = 0; c < 2; ++c)
                     tc::tma_load_3d(dst + c * (BN * 128), is_v ? (const void *)&tmv : (const void *)&tmk,
-                                    full(stage), (dc0 + c) * 64, c1, c2);
+                                    full(stage), d0 + c * 64, c1, c2);
                 next();
                 return true;
             };
             // the MMA issuer consumes K of tile v+1 before V of tile v: K0, K1, V0, K2, V1, ...
-            for (int ks = 0; ks < KSUB && ok && n_vis > 0; ++ks) ok = load(tile_at(0), false, ks);
+            for (int ks = 0; ks < KSUB && ok && n_vis > 0; ++ks) ok = load(tile_at(0), false, ks * 128);
             for (int v = 0; ok && v < n_vis; ++v) {
-                for (int ks = 0; ks < KSUB && ok && v + 1 < n_vis; ++ks) ok = load(tile_at(v + 1), false, ks);
-                if (ok) ok = load(tile_at(v), true, 0);
+                for (int ks = 0; ks < KSUB && ok && v + 1 < n_vis; ++ks)
+                    ok = load(tile_at(v + 1), false, ks * 128);
+                for (int vs = 0; vs < VSUB && ok; ++vs) ok = load(tile_at(v), true, d_off + vs * 128);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t id_qk = tc::idesc_f16(BM, BN, kBf16, false);
-            const uint32_t id_pv = tc::idesc_f16(BM, DO, kBf16, true);
+            const uint32_t idesc_qk = tc::idesc_f16(BM, BN, kBf16, false);
+            const uint32_t idesc_pv = tc::idesc_f16(BM, 128, kBf16, true);
             int stage = a.q_tma ? kQStages % NS : 0;
             uint32_t round = a.q_tma ? kQStages / NS : 0;
             auto next = [&]() {
@@ -444,17 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::tc_fence_after();
                     const uint32_t kb = sbase + L::kStages + stage * kStageBytes;
 #pragma unroll
-                    for (int kk = 0; kk < DS / 16; ++kk) {
-                        const int dq = ks * DS + kk * 16;
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const int dq = ks * 128 + kk * 16;
                         const uint64_t db =
                             tc::smem_desc_sw128(kb + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
                         if constexpr (C::QTM) {
-                            tc::mma_f16_ts(d_tm, tm_q + dq / 2, db, id_qk, (ks | kk) != 0);
+                            tc::mma_f16_ts(d_tm, tm_q + dq / 2, db, idesc_qk, (ks | kk) != 0);
                         } else {
                             const uint64_t da = tc::smem_desc_sw128(
                                 sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16,
                                 1024);
-                            tc::mma_f16_ss(d_tm, da, db, id_qk, (ks | kk) != 0);
+                            tc::mma_f16_ss(d_tm, da, db, idesc_qk, (ks | kk) != 0);
                         }
                     }
                     tc::mma_commit(empty(stage));
@@ -470,23 +463,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (i + 1 < n_vis && !(ok = issue_s(i + 1))) break;
                 if (!(ok = wt.wait(p_full(i & 1), (i >> 1) & 1))) break;
                 tc::tc_fence_after();
-                if (!(ok = wt.wait(full(stage), round & 1))) break;
-                tc::tc_fence_after();
-                const uint32_t vb = sbase + L::kStages + stage * kStageBytes;
+                // the VSUB stages of V(i) follow each other in the ring
+                int st[VSUB];
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
-                    if constexpr (C::PTM) {
-                        tc::mma_f16_ts(tm_o, tm_s + (uint32_t)(i & 1) * BN + kk * 8, db, id_pv,
-                                       (i | kk) != 0);
-                    } else {
-                        const uint64_t da = tc::smem_desc_sw128(
-                            sbase + L::kP + (kk / 4) * (BM * 128) + (kk % 4) * 32, 16, 1024);
-                        tc::mma_f16_ss(tm_o, da, db, id_pv, (i | kk) != 0);
-                    }
+                for (int vs = 0; vs < VSUB; ++vs) {
+                    if (ok) ok = wt.wait(full(stage), round & 1);
+                    st[vs] = stage;
+                    next();
                 }
-                tc::mma_commit(empty(stage));
-                next();
+                if (!ok) break;
+                tc::tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+#pragma unroll
+                    for (int vs = 0; vs < VSUB; ++vs) {
+                        const uint32_t vb = sbase + L::kStages + st[vs] * kStageBytes;
+                        const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
+                        tc::mma_f16_ts(tm_o + vs * 128, tm_s + (uint32_t)(i & 1) * BN + kk * 8, db,
+                                       idesc_pv, (i | kk) != 0);
+                    }
+#pragma unroll
+                for (int vs = 0; vs < VSUB; ++vs) tc::mma_commit(empty(st[vs]));
                 tc::mma_commit(o_done(i & 1));
             }
             // every MMA of this thread has finished before TMEM can be released
@@ -496,71 +493,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
-        const int r = threadIdx.x;  // tile row == TMEM lane
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        // warp w: rows 32 (w % 4) .. + 31 (TMEM lanes), column half h = w / 4
+        const int r = (warp & 3) * 32 + lane;
+        const int h = warp >> 2;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int pair_bar = 2 + (warp & 3);  // named barrier of warps w and w + 4
         int head = 0, row = 0;
         const bool valid = row_of(a, t, r, head, row);
         bool ok = true;
 
-        // ---- Q row -> TMEM (or the shared-memory Q tile), rounded to K/V's type
-        auto put_q = [&](int cb, const uint32_t(&w)[32]) {  // 64 elements at column block cb
+        // ---- Q: this thread's 32 columns of each 64-column block, as f16/bf16
+        auto put_q = [&](int cb, const uint32_t(&w)[16]) {
             if constexpr (C::QTM) {
-                tc::tmem_st32(tm_q + cb * 32 + lane_base, w);
+                tc::tmem_st16(tm_q + cb * 32 + h * 16 + lane_base, w);
             } else {
                 uint8_t *qs = smem + L::kQ + cb * (BM * 128);
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8)
-                    *reinterpret_cast<uint4 *>(qs + sw128(r, c8)) =
-                        make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(qs + sw128(r, h * 4 + c)) =
+                        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
             }
         };
         if (a.q_tma) {
-            // f32 Q arrives by TMA through the first kQStages ring stages
+            // f32 Q arrives by TMA through the first kQStages ring stages; half h
+            // converts box h (32 columns)
             int stage = 0;
             uint32_t round = 0;
             for (int qs = 0; qs < kQStages; ++qs) {
                 if (ok) ok = wt.wait(full(stage), round & 1);
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok) {
-                    const uint8_t *src = smem + L::kStages + stage * kStageBytes;
-                    uint32_t w[32];
+                    const uint8_t *src = smem + L::kStages + stage * kStageBytes + h * 16384;
+                    uint32_t w[16];
 #pragma unroll
-                    for (int b = 0; b < 2; ++b)
-#pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4) {
-                            const float4 x = *reinterpret_cast<const float4 *>(
-                                src + b * 16384 + r * 128 + ((c4 ^ (r & 7)) << 4));
-                            w[b * 16 + c4 * 2] = pack2(KV{}, x.x, x.y);
-                            w[b * 16 + c4 * 2 + 1] = pack2(KV{}, x.z, x.w);
-                        }
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 x =
+                            *reinterpret_cast<const float4 *>(src + r * 128 + ((c4 ^ (r & 7)) << 4));
+                        w[c4 * 2] = pack2(KV{}, x.x, x.y);
+                        w[c4 * 2 + 1] = pack2(KV{}, x.z, x.w);
+                    }
                     put_q(qs, w);
                 }
-                tc::named_bar(1, BM);  // all softmax threads are done with this stage
-                if (r == 0) tc::mbar_arrive(empty(stage));
+                tc::named_bar(1, kSoftmaxThreads);  // every softmax thread is done with this stage
+                if (threadIdx.x == 0) tc::mbar_arrive(empty(stage));
                 if (++stage == NS) {
                     stage = 0;
                     ++round;
                 }
             }
         } else {
-            // each thread reads its own row
+            // each thread reads its half of its own row
 #pragma unroll 1
             for (int cb = 0; cb < D / 64; ++cb) {
-                uint32_t w[32];
+                uint32_t w[16];
                 if (valid && a.q_f32) {
                     const float *src = static_cast<const float *>(a.q) + t.lane * a.q_lane +
-                                       (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64;
+                                       (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64 + h * 32;
 #pragma unroll
-                    for (int v = 0; v < 16; ++v) {
+                    for (int v = 0; v < 8; ++v) {
                         const float4 x = ld_nc_f4(src + v * 4);
                         w[2 * v] = pack2(KV{}, x.x, x.y);
                         w[2 * v + 1] = pack2(KV{}, x.z, x.w);
                     }
                 } else if (valid) {
                     const uint16_t *src = static_cast<const uint16_t *>(a.q) + t.lane * a.q_lane +
-                                          (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64;
+                                          (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64 + h * 32;
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
+                    for (int v = 0; v < 4; ++v) {
                         const uint4 x = ld_nc_v4(src + v * 8);
                         w[4 * v] = x.x;
                         w[4 * v + 1] = x.y;
@@ -569,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
 #pragma unroll
-                    for (int v = 0; v < 32; ++v) w[v] = 0u;
+                    for (int v = 0; v < 16; ++v) w[v] = 0u;
                 }
                 put_q(cb, w);
             }
@@ -581,71 +580,83 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tc_fence_before();
         tc::mbar_arrive(q_full);
 
-        // ---- key tiles
+        // ---- key tiles: this thread owns columns [h*64, h*64 + 64) of every tile
         const uint16_t *mrow = valid ? a.mask + t.lane * a.m_lane + (int64_t)head * a.m_head +
-                                           (int64_t)row * a.m_row
+                                           (int64_t)row * a.m_row + h * 64
                                      : nullptr;
         const bool m_vec = valid && (reinterpret_cast<uintptr_t>(mrow) & 15) == 0;
         float m_ref = kNegInf, l = 0.f;
-        int i = 0;
-        for (; ok && i < n_vis; ++i) {
+        int n_done = 0;  // tiles whose P this thread has handed to the MMA issuer
+        // Both warps of a row pair run every iteration and every pair barrier, even
+        // after a failed wait (they then skip the work), so neither can be left at
+        // a barrier its partner never reaches.
+        for (int i = 0; i < n_vis; ++i) {
             const int j = tile_at(i);
             const int code = (list[i] & 0x8000) ? 2 : 1;
-            ok = __all_sync(0xffffffffu, wt.wait(s_full(i & 1), (i >> 1) & 1));
-            if (!ok) break;
-            tc::tc_fence_after();
-            float s[BN];
-            {
-                uint32_t rr[BN];
+            if (ok) ok = __all_sync(0xffffffffu, wt.wait(s_full(i & 1), (i >> 1) & 1));
+            float s[64];
+            float mx = kNegInf;
+            if (ok) {
+                tc::tc_fence_after();
+                {
+                    uint32_t rr[64];
+                    tc::tmem_ld32(tm_s + (uint32_t)(i & 1) * BN + h * 64 + lane_base,
+                                  *reinterpret_cast<uint32_t(*)[32]>(rr));
+                    tc::tmem_ld32(tm_s + (uint32_t)(i & 1) * BN + h * 64 + 32 + lane_base,
+                                  *reinterpret_cast<uint32_t(*)[32]>(rr + 32));
+                    tc::tmem_ld_wait();
 #pragma unroll
-                for (int cb = 0; cb < BN / 32; ++cb)
-                    tc::tmem_ld32(tm_s + (uint32_t)(i & 1) * BN + cb * 32 + lane_base,
-                                  *reinterpret_cast<uint32_t(*)[32]>(rr + cb * 32));
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    asm volatile("" : "+r"(rr[c]));  // keep every use after the wait
-                    s[c] = __uint_as_float(rr[c]);
-                }
-            }
-            if (!valid) {
-#pragma unroll
-                for (int c = 0; c < BN; ++c) s[c] = kNegInf;
-            } else if (code == 1) {
-#pragma unroll
-                for (int c = 0; c < BN; ++c) s[c] *= a.scale_log2;
-            } else {
-                const int c0 = j * BN;
-                if (m_vec && c0 + BN <= a.n_keys) {
-#pragma unroll
-                    for (int v = 0; v < BN / 8; ++v) {
-                        const uint4 x = *reinterpret_cast<const uint4 *>(mrow + c0 + v * 8);
-                        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const uint16_t mv = (uint16_t)(w[e / 2] >> ((e & 1) * 16));
-                            s[v * 8 + e] = fmaf(s[v * 8 + e], a.scale_log2,
-                                                mask_to_f32(mv, a.mask_bf16) * kLog2e);
-                        }
+                    for (int c = 0; c < 64; ++c) {
+                        asm volatile("" : "+r"(rr[c]));  // keep every use after the wait
+                        s[c] = __uint_as_float(rr[c]);
                     }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < BN; ++c)
-                        s[c] = (c0 + c < a.n_keys)
-                                   ? fmaf(s[c], a.scale_log2, mask_to_f32(mrow[c0 + c], a.mask_bf16) * kLog2e)
-                                   : kNegInf;
                 }
-            }
-            // row max with four independent chains
-            float mq[4] = {s[0], s[1], s[2], s[3]};
+                if (!valid) {
 #pragma unroll
-            for (int c = 4; c < BN; c += 4) {
-                mq[0] = fmaxf(mq[0], s[c]);
-                mq[1] = fmaxf(mq[1], s[c + 1]);
-                mq[2] = fmaxf(mq[2], s[c + 2]);
-                mq[3] = fmaxf(mq[3], s[c + 3]);
+                    for (int c = 0; c < 64; ++c) s[c] = kNegInf;
+                } else if (code == 1) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) s[c] *= a.scale_log2;
+                } else {
+                    const int c0 = j * BN + h * 64;  // key index of s[0]
+                    if (m_vec && c0 + 64 <= a.n_keys) {
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const uint4 x = *reinterpret_cast<const uint4 *>(mrow + j * BN + v * 8);
+                            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const uint16_t mv = (uint16_t)(w[e / 2] >> ((e & 1) * 16));
+                                s[v * 8 + e] = fmaf(s[v * 8 + e], a.scale_log2,
+                                                    mask_to_f32(mv, a.mask_bf16) * kLog2e);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            s[c] = (c0 + c < a.n_keys)
+                                       ? fmaf(s[c], a.scale_log2,
+                                              mask_to_f32(mrow[j * BN + c], a.mask_bf16) * kLog2e)
+                                       : kNegInf;
+                    }
+                }
+                // row max over this half with four independent chains
+                float mq[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+                for (int c = 4; c < 64; c += 4) {
+                    mq[0] = fmaxf(mq[0], s[c]);
+                    mq[1] = fmaxf(mq[1], s[c + 1]);
+                    mq[2] = fmaxf(mq[2], s[c + 2]);
+                    mq[3] = fmaxf(mq[3], s[c + 3]);
+                }
+                mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             }
-            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+            // agree with the other half of the row on the maximum
+            float *xs = xchg + (i & 1) * 2 * BM;
+            xs[h * BM + r] = mx;
+            tc::named_bar(pair_bar, 64);
+            mx = fmaxf(mx, xs[(1 - h) * BM + r]);
+            if (!ok) continue;
             float factor = 1.f;
             bool resc = false;
             if (m_ref == kNegInf) {
@@ -656,10 +667,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 resc = true;
             }
             const float mu = m_ref == kNegInf ? 0.f : m_ref;
-            uint32_t pk[BN / 2];
+            uint32_t pk[32];
             float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < BN; c += 4) {
+            for (int c = 0; c < 64; c += 4) {
                 const float p0 = ex2(s[c] - mu), p1 = ex2(s[c + 1] - mu);
                 const float p2 = ex2(s[c + 2] - mu), p3 = ex2(s[c + 3] - mu);
                 rs[0] += p0;
@@ -670,61 +681,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[c / 2 + 1] = pack2(KV{}, p2, p3);
             }
             l = l * factor + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-            // P.V of the previous tile must be done before O is rescaled, and, when P
-            // lives in shared memory (one buffer), before P is overwritten.  A P kept in
-            // TMEM goes over this tile's own S buffer, which the previous P.V does not
-            // read, so without a rescale the softmax runs ahead of the tensor pipe.
+            // P.V of the previous tile must be done before O is rescaled.  P goes
+            // over this tile's own S buffer, which the previous P.V does not read,
+            // so without a rescale the softmax runs ahead of the tensor pipe.
             // Parity waits are unambiguous: S(i) complete implies every MMA issued
             // before it (P.V up to tile i-2) completed, and P.V(i) cannot complete
             // before P(i) is written.
             const bool any_resc = __any_sync(0xffffffffu, resc);
-            if (i > 0 && (!C::PTM || any_resc)) {
+            if (i > 0 && any_resc) {
                 ok = __all_sync(0xffffffffu, wt.wait(o_done((i - 1) & 1), ((i - 1) >> 1) & 1));
-                if (!ok) break;
+                if (!ok) continue;
                 tc::tc_fence_after();
             }
             if (any_resc) {
 #pragma unroll 1
-                for (int cb = 0; cb < DO / 32; ++cb) {
+                for (int cb = 0; cb < DO / 64; ++cb) {
+                    const uint32_t col = tm_o + h * (DO / 2) + cb * 32 + lane_base;
                     uint32_t rr[32];
-                    tc::tmem_ld32(tm_o + cb * 32 + lane_base, rr);
+                    tc::tmem_ld32(col, rr);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         asm volatile("" : "+r"(rr[e]));
                         rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
                     }
-                    tc::tmem_st32(tm_o + cb * 32 + lane_base, rr);
+                    tc::tmem_st32(col, rr);
                 }
-                tc::tmem_st_wait();
             }
-            if constexpr (C::PTM) {
-                // P over the first BN/2 columns of the S buffer it came from
-#pragma unroll
-                for (int cb = 0; cb < BN / 64; ++cb)
-                    tc::tmem_st32(tm_s + (uint32_t)(i & 1) * BN + cb * 32 + lane_base,
-                                  *reinterpret_cast<const uint32_t(*)[32]>(pk + cb * 32));
-                tc::tmem_st_wait();
-            } else {
-                uint8_t *ps = smem + L::kP;
-#pragma unroll
-                for (int c8 = 0; c8 < BN / 8; ++c8)
-                    *reinterpret_cast<uint4 *>(ps + (c8 / 8) * (BM * 128) + sw128(r, c8 % 8)) =
-                        make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
-                tc::fence_async_smem();
-            }
+            // P over the first 64 columns of the S buffer it came from
+            tc::tmem_st32(tm_s + (uint32_t)(i & 1) * BN + h * 32 + lane_base, pk);
+            tc::tmem_st_wait();
             tc::tc_fence_before();
             tc::mbar_arrive(p_full(i & 1));
+            n_done = i + 1;
         }
 
         // ---- epilogue: both outstanding P.V (tiles n-2 and n-1) must be complete
-        const int n_done = i;
         if (ok && n_done > 0) {
             ok = __all_sync(0xffffffffu, wt.wait(o_done((n_done - 1) & 1), ((n_done - 1) >> 1) & 1));
             if (ok && n_done >= 2)
                 ok = __all_sync(0xffffffffu,
                                 wt.wait(o_done((n_done - 2) & 1), ((n_done - 2) >> 1) & 1));
             tc::tc_fence_after();
+        }
+        // row sum = both halves' partial sums
+        {
+            float *xs = xchg + (n_done & 1) * 2 * BM;
+            xs[h * BM + r] = l;
+            tc::named_bar(pair_bar, 64);
+            l += xs[(1 - h) * BM + r];
         }
         const bool have_o = ok && n_done > 0;
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -733,10 +738,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The ring (or, at head_dim 512, the Q tile) is idle once the last P.V is done.
             uint8_t *stg = smem + (D == 512 ? L::kQ : L::kStages);
 #pragma unroll 1
-            for (int cb = 0; cb < DO / 32; ++cb) {
+            for (int cb = 0; cb < DO / 64; ++cb) {
+                const int box = h * (DO / 64) + cb;
                 uint32_t rr[32];
                 if (have_o) {
-                    tc::tmem_ld32(tm_o + cb * 32 + lane_base, rr);
+                    tc::tmem_ld32(tm_o + box * 32 + lane_base, rr);
                     tc::tmem_ld_wait();
                 } else {
 #pragma unroll
@@ -746,18 +752,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c4 = 0; c4 < 8; ++c4) {
                     asm volatile("" : "+r"(rr[4 * c4]), "+r"(rr[4 * c4 + 1]), "+r"(rr[4 * c4 + 2]),
                                  "+r"(rr[4 * c4 + 3]));
-                    *reinterpret_cast<float4 *>(stg + cb * 16384 + r * 128 + ((c4 ^ (r & 7)) << 4)) =
+                    *reinterpret_cast<float4 *>(stg + box * 16384 + r * 128 + ((c4 ^ (r & 7)) << 4)) =
                         make_float4(__uint_as_float(rr[4 * c4]) * inv, __uint_as_float(rr[4 * c4 + 1]) * inv,
                                     __uint_as_float(rr[4 * c4 + 2]) * inv,
                                     __uint_as_float(rr[4 * c4 + 3]) * inv);
                 }
             }
             tc::fence_async_smem();
-            tc::named_bar(1, BM);
-            if (r == 0 && !*abort_flag) {
+            tc::named_bar(1, kSoftmaxThreads);
+            if (threadIdx.x == 0 && !*abort_flag) {
 #pragma unroll 1
-                for (int cb = 0; cb < DO / 32; ++cb)
-                    tc::tma_store_3d(&tmo, smem_u32(stg + cb * 16384), d_off + cb * 32,
+                for (int box = 0; box < DO / 32; ++box)
+                    tc::tma_store_3d(&tmo, smem_u32(stg + box * 16384), d_off + box * 32,
                                      a.o_rows_dim1 ? q_row0 : q_head0, a.o_rows_dim1 ? q_head0 : q_row0);
                 tc::bulk_commit();
                 tc::bulk_wait0();
@@ -766,18 +772,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             float *dst;
             if (a.splits == 1) {
                 dst = valid ? a.o + t.lane * a.o_lane + (int64_t)head * a.o_head +
-                                  (int64_t)row * a.o_row + d_off
+                                  (int64_t)row * a.o_row + d_off + h * (DO / 2)
                             : nullptr;
             } else {
                 const int64_t unit = ((int64_t)tile_id * a.d_parts + dpart) * a.splits + split;
-                dst = a.ws_o + (unit * BM + r) * DO;
-                a.ws_lse[unit * BM + r] = l > 0.f ? m_ref + __log2f(l) : kNegInf;
+                dst = a.ws_o + (unit * BM + r) * DO + h * (DO / 2);
+                if (h == 0) a.ws_lse[unit * BM + r] = l > 0.f ? m_ref + __log2f(l) : kNegInf;
             }
 #pragma unroll 1
-            for (int cb = 0; cb < DO / 32; ++cb) {
+            for (int cb = 0; cb < DO / 64; ++cb) {
                 uint32_t rr[32];
                 if (have_o) {
-                    tc::tmem_ld32(tm_o + cb * 32 + lane_base, rr);
+                    tc::tmem_ld32(tm_o + h * (DO / 2) + cb * 32 + lane_base, rr);
                     tc::tmem_ld_wait();
                 } else {
 #pragma unroll
@@ -799,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- teardown: TMEM is released only after every role is done with it
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc::tc_fence_after();
         tc::tmem_dealloc<512>(tmem);
     }
@@ -861,7 +867,7 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, int n_keys,
                bool shared_mask) {
     Plan p{};
-    p.bn = head_dim == 128 ? 128 : 64;
+    p.bn = BN;
     p.do_ = head_dim == 512 ? 256 : head_dim;
     p.d_parts = head_dim / p.do_;
     const int group = n_heads / n_kv_heads;

@@ -92,51 +92,49 @@ __global__ void __launch_bounds__(256) pack_attention_kernel(
     }
 }
 
-// Mask: the flat [B][H][R][K] array is cut into 8-element chunks; K is
-// arbitrary, so a chunk may straddle two rows and each element is decided on
-// its own.
+// Mask: every row (b, h, r) is a threshold: columns c < R + min(len_b, W-1-r)
+// are visible (the draft rows, then the history entries inside the window),
+// the rest are hidden.  The flat [B][H][R][K] array is cut into 8-element
+// chunks (16-byte stores); K is arbitrary, so a chunk may straddle rows.
+// IDX is int when the element count fits in 31 bits (cheap index math).
+template <typename IDX>
+__device__ __forceinline__ int mask_threshold(const uint32_t *cache_lengths, const RingGeom &g,
+                                              IDX row) {
+    const int r = (int)(row % g.R);
+    const int b = (int)(row / ((IDX)g.H * g.R));
+    const uint32_t l = cache_lengths[b];
+    const int len = l > (uint32_t)g.W ? g.W : (int)l;
+    const int hist = len < g.W - 1 - r ? len : g.W - 1 - r;
+    return g.R + (hist > 0 ? hist : 0);
+}
+
+template <typename IDX>
 __global__ void __launch_bounds__(256) fill_mask_kernel(const uint32_t *__restrict__ cache_lengths,
                                                         uint16_t *__restrict__ mask, RingGeom g,
                                                         int32_t *status) {
-    const int64_t total = (int64_t)g.B * g.H * g.R * g.K;
-    const int64_t nchunks = (total + 7) / 8;
+    const IDX total = (IDX)g.B * g.H * g.R * g.K;
+    const IDX nchunks = (total + 7) / 8;
     if (blockIdx.x == 0 && threadIdx.x < g.B) {
         if (cache_lengths[threadIdx.x] > (uint32_t)g.W) raise_flag(status, GQA_FLAG_RING_CLAMPED);
     }
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < nchunks; t += stride) {
-        // decompose the chunk's first element once, then step through the 8 elements
-        const int64_t e0 = t * 8;
-        const int64_t row = e0 / g.K;
+    const IDX stride = (IDX)gridDim.x * blockDim.x;
+    for (IDX t = (IDX)blockIdx.x * blockDim.x + threadIdx.x; t < nchunks; t += stride) {
+        const IDX e0 = t * 8;
+        IDX row = e0 / g.K;
         int c = (int)(e0 - row * g.K);
-        int r = (int)(row % g.R);
-        const int64_t bh = row / g.R;
-        int b = (int)(bh / g.H);
-        int hh = (int)(bh - (int64_t)b * g.H);
-        auto len_of = [&](int lane) {
-            const uint32_t l = cache_lengths[lane];
-            return l > (uint32_t)g.W ? g.W : (int)l;
-        };
-        int len = b < g.B ? len_of(b) : 0;
+        const IDX rows = total / g.K;
+        int thr = mask_threshold<IDX>(cache_lengths, g, row);
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int j = c - g.R;
-            const bool visible = c < g.R || (j < len && r + j + 1 < g.W);
-            const uint32_t val = visible ? 0x0000u : 0xff80u;
+            const uint32_t val = c < thr ? 0x0000u : 0xff80u;
             if (i & 1)
                 w[i / 2] |= val << 16;
             else
                 w[i / 2] = val;
             if (++c == g.K) {
                 c = 0;
-                if (++r == g.R) {
-                    r = 0;
-                    if (++hh == g.H) {
-                        hh = 0;
-                        if (++b < g.B) len = len_of(b);
-                    }
-                }
+                if (++row < rows) thr = mask_threshold<IDX>(cache_lengths, g, row);
             }
         }
         if (e0 + 8 <= total) {
@@ -210,11 +208,11 @@ cudaError_t launch_pack_attention(const uint16_t *ring_k, const uint16_t *ring_v
                                   uint16_t *packed_q, uint16_t *packed_k, uint16_t *packed_v,
                                   const gqa_ring_params &p, int32_t *status, cudaStream_t stream) {
     RingGeom g = geom_of(p);
-    // x blocks per slab: enough for about 8 resident CTAs per SM overall, and no
-    // more than one chunk per thread of the largest slab
+    // x blocks per slab: the K/V slabs (nearly all the bytes) alone get about 8
+    // CTAs per SM, and no slab gets more than one chunk per thread
     const int slabs = g.B * g.HK + g.B * g.H;
     const int per_slab = (int)(((int64_t)g.K * (g.D / 8) + 255) / 256);
-    int bx = (sm_count() * 8 + slabs - 1) / slabs;
+    int bx = (sm_count() * 8 + g.B * g.HK - 1) / (g.B * g.HK);
     if (bx > per_slab) bx = per_slab;
     if (bx < 1) bx = 1;
     const dim3 grid(bx, slabs);
@@ -236,8 +234,12 @@ cudaError_t launch_fill_mask(const uint32_t *cache_lengths, uint16_t *mask,
     RingGeom g = geom_of(p);
     int64_t work = ((int64_t)g.B * g.H * g.R * g.K + 7) / 8;
     timing_mark(true, stream);
-    fill_mask_kernel<<<grid_for(work, sm_count()), 256, 0, stream>>>(cache_lengths, mask, g,
-                                                                      status);
+    if ((int64_t)g.B * g.H * g.R * g.K + 8 < INT32_MAX)
+        fill_mask_kernel<int><<<grid_for(work, sm_count()), 256, 0, stream>>>(cache_lengths, mask,
+                                                                               g, status);
+    else
+        fill_mask_kernel<int64_t><<<grid_for(work, sm_count()), 256, 0, stream>>>(cache_lengths,
+                                                                                   mask, g, status);
     timing_mark(false, stream);
     return cudaGetLastError();
 }
