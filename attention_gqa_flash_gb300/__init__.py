@@ -73,6 +73,9 @@ def library() -> ctypes.CDLL:
             "gqa_attn_paged_decode": (i32, [vp, sz, vp, vp, sz, i32, i64, i64, i64, vp, sz, i32,
                                             vp, sz, vp, sz, i32, i32, i32, i32, i32, i32, f32, vp,
                                             sz, vp, vp]),
+            "gqa_attn_paged_decode_noalloc": (i32, [vp, sz, vp, vp, sz, i32, i64, i64, i64, vp, sz,
+                                                    i32, vp, sz, vp, sz, i32, i32, i32, i32, i32,
+                                                    i32, f32, vp, vp]),
             "gqa_ring_params_valid": (i32, [rp]),
             "gqa_pack_attention": (i32, [vp, sz] * 10 + [rp, vp, vp]),
             "gqa_fill_mask": (i32, [vp, sz, vp, sz, rp, vp, vp]),
@@ -96,6 +99,7 @@ def exported_symbols() -> list[str]:
             "gqa_timing_last_ms", "gqa_selftest_bounded_wait", "gqa_kv_pad",
             "gqa_attn_prefill_workspace_size", "gqa_attn_prefill",
             "gqa_attn_paged_decode_workspace_size", "gqa_attn_paged_decode",
+            "gqa_attn_paged_decode_noalloc",
             "gqa_ring_params_valid", "gqa_pack_attention", "gqa_fill_mask",
             "gqa_attn_verify_workspace_size", "gqa_attn_verify", "gqa_commit_kv",
             "gqa_set_mask_rows"]
@@ -257,6 +261,41 @@ def gqa_attn_paged_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch
         _ptr(context_lens), _nbytes(context_lens), _ptr(out), _nbytes(out),
         num_seqs, n_heads, n_kv, d, page_size, num_pages, float(scale),
         _ptr(workspace), _nbytes(workspace), _ptr(status), _stream(stream)))
+    return out
+
+
+GQA_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def gqa_attn_paged_decode_noalloc(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                                  page_table: torch.Tensor, context_lens: torch.Tensor,
+                                  scale: float, out: torch.Tensor, status: torch.Tensor | None = None,
+                                  stream=None) -> torch.Tensor:
+    """Paged decode for callers that cannot provide device scratch: same
+    arguments as gqa_attn_paged_decode, no workspace, and the output buffer
+    must be passed in.  The library keeps its partial results in a fixed
+    16 MiB device array; larger problems are rejected (GQAError)."""
+    _cuda("q", q, (torch.float32,))
+    _contig("q", q)
+    _cuda("k_pages", k_pages, tuple(_KV_DTYPES))
+    _cuda("v_pages", v_pages, (k_pages.dtype,))
+    _cuda("page_table", page_table, (torch.int32,))
+    _cuda("context_lens", context_lens, (torch.int32,))
+    _cuda("out", out, (torch.float32,))
+    for name, t in (("page_table", page_table), ("context_lens", context_lens), ("out", out)):
+        _contig(name, t)
+    num_seqs, n_heads, d = q.shape
+    num_pages, page_size, n_kv, d2 = k_pages.shape
+    if v_pages.shape != k_pages.shape or v_pages.stride() != k_pages.stride() or d2 != d:
+        raise ValueError("K and V pools must share shape and strides")
+    _check(library().gqa_attn_paged_decode_noalloc(
+        _ptr(q), _nbytes(q), _ptr(k_pages), _ptr(v_pages),
+        min(_nbytes(k_pages), _nbytes(v_pages)), _KV_DTYPES[k_pages.dtype],
+        k_pages.stride(0), k_pages.stride(1), k_pages.stride(2),
+        _ptr(page_table), _nbytes(page_table), page_table.shape[1],
+        _ptr(context_lens), _nbytes(context_lens), _ptr(out), _nbytes(out),
+        num_seqs, n_heads, n_kv, d, page_size, num_pages, float(scale),
+        _ptr(status), _stream(stream)))
     return out
 
 

@@ -305,6 +305,38 @@ int gqa_attn_paged_decode(const float *q, size_t q_bytes, const void *k_pages,
     return ok();
 }
 
+// Paged decode for callers that cannot supply a workspace: the split-KV
+// partials go to the library's fixed device array (no allocation anywhere on
+// this path), after which the regular entry point does all validation and the
+// launch.
+int gqa_attn_paged_decode_noalloc(const float *q, size_t q_bytes, const void *k_pages,
+                                  const void *v_pages, size_t pool_bytes, int kv_dtype,
+                                  int64_t page_stride, int64_t token_stride, int64_t head_stride,
+                                  const int32_t *page_table, size_t page_table_bytes,
+                                  int max_pages_per_seq, const int32_t *context_lens,
+                                  size_t context_lens_bytes, float *o, size_t o_bytes,
+                                  int num_seqs, int n_heads, int n_kv_heads, int head_dim,
+                                  int page_size, int num_pages, float scale, int32_t *status,
+                                  gqa_stream_t stream) {
+    if (num_seqs <= 0 || n_heads <= 0 || head_dim <= 0 || max_pages_per_seq <= 0 || page_size <= 0)
+        return fail("paged decode (no-alloc): empty shape");
+    const size_t need =
+        gqa::decode_workspace_bytes(num_seqs, n_heads, head_dim, max_pages_per_seq, page_size);
+    if (need > (size_t)GQA_NOALLOC_SCRATCH_BYTES)
+        return fail("paged decode (no-alloc): this problem needs %zu bytes of scratch "
+                    "(num_seqs x ceil(max_pages_per_seq*page_size/256) x n_heads x (head_dim+1) x 4), "
+                    "more than the fixed %u-byte array; use gqa_attn_paged_decode with a workspace",
+                    need, (unsigned)GQA_NOALLOC_SCRATCH_BYTES);
+    void *scratch = nullptr;
+    const cudaError_t e = gqa::decode_fixed_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_fail("paged decode (no-alloc): scratch address lookup", e);
+    return gqa_attn_paged_decode(q, q_bytes, k_pages, v_pages, pool_bytes, kv_dtype, page_stride,
+                                 token_stride, head_stride, page_table, page_table_bytes,
+                                 max_pages_per_seq, context_lens, context_lens_bytes, o, o_bytes,
+                                 num_seqs, n_heads, n_kv_heads, head_dim, page_size, num_pages,
+                                 scale, scratch, (size_t)GQA_NOALLOC_SCRATCH_BYTES, status, stream);
+}
+
 // ---------------------------------------------------------------------------
 // DFlash2 ring KV
 // ---------------------------------------------------------------------------

@@ -395,3 +395,36 @@ cudaError_t launch_paged_decode(const DecodeProblem &p, void *workspace, cudaStr
 }
 
 }  // namespace gqa
+
+// ---------------------------------------------------------------------------
+// Fixed scratch for gqa_attn_paged_decode_noalloc: callers that cannot give the
+// library a device buffer get the split-KV partials kept here instead.  The
+// array is part of the library's device image; its device address is looked
+// up once per device (with that device current) and cached.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace gqa {
+namespace {
+static __device__ __align__(256) unsigned char g_decode_fixed_scratch[GQA_NOALLOC_SCRATCH_BYTES];
+std::mutex g_fixed_scratch_mu;
+void *g_fixed_scratch_addr[64] = {nullptr};
+}  // namespace
+
+cudaError_t decode_fixed_scratch(void **ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_fixed_scratch_mu);
+    if (!g_fixed_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_fixed_scratch);
+        if (e != cudaSuccess) return e;
+        g_fixed_scratch_addr[dev] = p;
+    }
+    *ptr = g_fixed_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace gqa

@@ -72,5 +72,7 @@ struct DecodeProblem {
 size_t decode_workspace_bytes(int num_seqs, int n_heads, int head_dim, int max_pages_per_seq,
                               int page_size);
 cudaError_t launch_paged_decode(const DecodeProblem &p, void *workspace, cudaStream_t stream);
+// Device address (current device) of the fixed GQA_NOALLOC_SCRATCH_BYTES scratch array.
+cudaError_t decode_fixed_scratch(void **ptr);
 
 }  // namespace gqa

@@ -157,6 +157,39 @@ int gqa_attn_paged_decode(const float *q, size_t q_bytes, const void *k_pages,
                           int num_pages, float scale, void *workspace, size_t workspace_bytes,
                           int32_t *status, gqa_stream_t stream);
 
+/*
+ * Paged decode without a caller-provided workspace.  (The pages have no
+ * counterpart: this entry point exists for callers of this library.)
+ *
+ * Some callers cannot hand the library a device buffer at the moment they
+ * call: a serving engine whose device memory is carved up once at start-up by
+ * its own allocator has no spare allocation to give, and real-time callers
+ * avoid cudaMalloc / cudaFree because those calls can block the host and
+ * synchronise the device.  This variant takes the same arguments as
+ * gqa_attn_paged_decode minus the workspace, allocates nothing, and keeps its
+ * split-KV partial results in a fixed array of GQA_NOALLOC_SCRATCH_BYTES that
+ * lives in the library's device image (every GPU that loads the library holds
+ * it until the process exits).
+ *   - Problems whose scratch need, gqa_attn_paged_decode_workspace_size(...),
+ *     exceeds GQA_NOALLOC_SCRATCH_BYTES are rejected with GQA_INVALID_ARGUMENT.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array and nothing in it needs clearing between
+ *     calls, but calls whose work overlaps on the GPU (two streams, or two
+ *     threads) race on it: serialise them.
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int gqa_attn_paged_decode_noalloc(const float *q, size_t q_bytes, const void *k_pages,
+                                  const void *v_pages, size_t pool_bytes, int kv_dtype,
+                                  int64_t page_stride, int64_t token_stride, int64_t head_stride,
+                                  const int32_t *page_table, size_t page_table_bytes,
+                                  int max_pages_per_seq, const int32_t *context_lens,
+                                  size_t context_lens_bytes, float *o, size_t o_bytes,
+                                  int num_seqs, int n_heads, int n_kv_heads, int head_dim,
+                                  int page_size, int num_pages, float scale, int32_t *status,
+                                  gqa_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* DFlash2 ring KV (mlx-native 0.21.1 dflash2_attention_pack.rs).           */
 /* ------------------------------------------------------------------------ */
