@@ -886,7 +886,9 @@ Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, i
     if (sms <= 0) sms = 148;
     p.splits = 1;
     if (units < sms && p.n_blk > 1) {
-        int s = (sms + units - 1) / units;
+        // one CTA per SM at most: a CTA past the SM count would run as a second wave and
+        // double the time of the whole launch
+        int s = sms / units;
         if (s > p.n_blk) s = p.n_blk;
         p.splits = s;
     }

@@ -357,6 +357,35 @@ def run_reference(args, case) -> None:
 # ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
+# Workloads for profiler captures: the bench's own prefill and verify workloads, and a
+# 16-sequence decode (two 1 GiB page pools) that stays a few GB on the device.
+CAPTURE_CASES = {
+    "prefill_d256": lambda w: w.prefill_d256(seed=0),
+    "prefill_d512": lambda w: w.prefill_d512_prefix(seed=0),
+    "decode_16seq": lambda w: w.paged_decode(num_seqs=16, num_pages=16384, seed=0),
+    "verify": lambda w: w.verify_full(seed=0),
+}
+
+
+def run_capture(name: str, reps: int) -> None:
+    import torch
+    import workloads
+    import attention_gqa_flash_gb300 as g
+    torch.cuda.set_device(0)
+    g.library()
+    c = CAPTURE_CASES[name](workloads)
+    if name.startswith("prefill"):
+        step = setup_prefill(torch, g, c)[0]
+    elif name.startswith("decode"):
+        step = setup_decode(torch, g, c)[0]
+    else:
+        step = setup_verify(torch, g, c)[0]
+    for _ in range(max(1, reps)):
+        step()
+    torch.cuda.synchronize()
+    print(f"capture {name}: {max(1, reps)} calls done", flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -365,7 +394,13 @@ def main() -> None:
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--paths", choices=("all", "main"), default="all")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--capture", choices=tuple(CAPTURE_CASES),
+                    help="run one hot-path call --steps times on a capture-sized workload and "
+                         "exit (for ncu); prints no JSON line")
     args = ap.parse_args()
+    if args.capture:
+        run_capture(args.capture, args.steps)
+        return
     if args.warmup < 3:
         args.warmup = 3
 
