@@ -63,6 +63,7 @@ def library() -> ctypes.CDLL:
             "gqa_device_sm_count": (i32, []),
             "gqa_timing_enable": (i32, [i32]),
             "gqa_timing_last_ms": (f32, []),
+            "gqa_attn_set_cta_pairs": (i32, [i32]),
             "gqa_selftest_bounded_wait": (i32, [vp, i32, vp]),
             "gqa_kv_pad": (ctypes.c_uint32, [ctypes.c_uint32]),
             "gqa_attn_prefill_workspace_size": (sz, [i32] * 5),
@@ -96,7 +97,8 @@ def library() -> ctypes.CDLL:
 def exported_symbols() -> list[str]:
     """Names of the C entry points this binding wraps."""
     return ["gqa_last_error", "gqa_version", "gqa_device_sm_count", "gqa_timing_enable",
-            "gqa_timing_last_ms", "gqa_selftest_bounded_wait", "gqa_kv_pad",
+            "gqa_timing_last_ms", "gqa_attn_set_cta_pairs", "gqa_selftest_bounded_wait",
+            "gqa_kv_pad",
             "gqa_attn_prefill_workspace_size", "gqa_attn_prefill",
             "gqa_attn_paged_decode_workspace_size", "gqa_attn_paged_decode",
             "gqa_attn_paged_decode_noalloc",
@@ -148,6 +150,12 @@ def _ring(p) -> GqaRingParams:
 def gqa_timing_enable(enable: bool) -> None:
     """Record CUDA events around each call's dominant kernel (measurement only)."""
     _check(library().gqa_timing_enable(1 if enable else 0))
+
+
+def gqa_attn_set_cta_pairs(mode: int) -> None:
+    """Prefill tiling: 0 never pair query tiles into two-CTA clusters, 1 pair
+    where measured faster (head_dim 512, the default), 2 pair every eligible shape."""
+    _check(library().gqa_attn_set_cta_pairs(int(mode)))
 
 
 def gqa_timing_last_ms() -> float:

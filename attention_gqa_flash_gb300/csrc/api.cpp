@@ -122,6 +122,12 @@ const char *gqa_version(void) { return "gqa-attn-gb300 0.1.0 (sm_103a)"; }
 
 int gqa_device_sm_count(void) { return gqa::sm_count(); }
 
+int gqa_attn_set_cta_pairs(int mode) {
+    if (mode < 0 || mode > 2) return fail("gqa_attn_set_cta_pairs: mode %d is not 0, 1 or 2", mode);
+    gqa::set_attention_pairs(mode);
+    return ok();
+}
+
 int gqa_timing_enable(int enable) {
     if (enable && !gqa::g_ev_start) {
         cudaError_t e = cudaEventCreate(&gqa::g_ev_start);

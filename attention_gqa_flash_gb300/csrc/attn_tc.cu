@@ -83,8 +83,8 @@ struct Layout {
     static constexpr int kQ = 0;                     // D/64 tiles of [128][64] (head_dim >= 256)
     static constexpr int kStages = kQ + C::QBYTES;   // STAGES x 32 KiB
     static constexpr int kBars = kStages + C::STAGES * kStageBytes;
-    // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], o_done[2], mma_fin
-    static constexpr int kNumBars = 2 * C::STAGES + 8;
+    // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], o_done[2], mma_fin, q_go
+    static constexpr int kNumBars = 2 * C::STAGES + 9;
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kNumVis = kAbort + 4;
@@ -233,13 +233,14 @@ struct Waiter {
     volatile int *abort;
     int32_t *status;
     uint64_t limit_ns;
+    bool honour_abort = true;  // false: only the time limit ends the wait
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
         if (tc::mbar_try_wait(bar, parity)) return true;
         const uint64_t t0 = tc::globaltimer_ns();
         for (uint32_t it = 1;; ++it) {
             if (tc::mbar_try_wait(bar, parity)) return true;
             if ((it & 127) == 0) {
-                if (*abort) return false;
+                if (honour_abort && *abort) return false;
                 if (tc::globaltimer_ns() - t0 > limit_ns) {
                     *abort = 1;
                     raise_flag(status, GQA_FLAG_TIMEOUT);
@@ -270,7 +271,12 @@ __device__ __forceinline__ uint32_t sw128(int r, int c16) {
 }
 
 
-template <int D, class KV>
+// PAIR: the two CTAs of a cluster process two query tiles (two heads of one
+// KV group, same rows, same visible key tiles) with one 256-row MMA per step
+// (cta_group::2).  Each CTA loads only half of every K tile (64 of its keys)
+// and half of every V tile (half of the output columns), so the K/V bytes an
+// SM takes in per tile are halved; the even CTA issues all MMAs.
+template <int D, class KV, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq,
@@ -280,6 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int DO = C::DO, KSUB = C::KSUB, VSUB = C::VSUB, NS = C::STAGES;
     constexpr bool kBf16 = KV::kind == GQA_DTYPE_BF16;
     constexpr int kQStages = D / 64;  // an f32 Q tile crosses the ring 64 columns per stage
+    static_assert(!PAIR || D >= 256, "CTA pairs stage Q in shared memory (head_dim >= 256)");
+    // PAIR: one ring stage holds this CTA's 64 keys x 256 columns of K, or its
+    // 128 keys x 128 output columns of V
+    constexpr int KST = PAIR ? D / 256 : KSUB;  // ring stages per K tile
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
@@ -291,6 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto p_full = [&](int b) { return bar(2 * NS + 3 + b); };
     auto o_done = [&](int b) { return bar(2 * NS + 5 + b); };
     const uint32_t mma_fin = bar(2 * NS + 7);
+    // PAIR, odd CTA: released once the even CTA has seen both Q tiles staged (see the producer)
+    const uint32_t q_go = bar(2 * NS + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlot);
     int *n_vis_smem = reinterpret_cast<int *>(smem + L::kNumVis);
@@ -303,14 +315,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
-    // ---- which unit: (query tile, output half, key split); heavy row tiles first
-    int idx = blockIdx.x;
+    // ---- which unit: (query tile, output half, key split); heavy row tiles first.
+    // A pair takes head tiles 2p and 2p + 1 of the same (lane, KV head, row tile).
+    const uint32_t rank = PAIR ? (blockIdx.x & 1u) : 0u;
+    int idx = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int split = idx % a.splits;
     idx /= a.splits;
     const int dpart = idx % a.d_parts;
     idx /= a.d_parts;
-    const int per_rt = a.lanes * a.n_kv_heads * a.head_tiles;
-    const int tile_id = (a.row_tiles - 1 - idx / per_rt) * per_rt + idx % per_rt;
+    const int hts = PAIR ? a.head_tiles / 2 : a.head_tiles;
+    const int per_rt = a.lanes * a.n_kv_heads * hts;
+    const int pidx = (a.row_tiles - 1 - idx / per_rt) * per_rt + idx % per_rt;
+    const int tile_id = PAIR ? (pidx / hts) * a.head_tiles + (pidx % hts) * 2 + (int)rank : pidx;
     const Tile t = tile_of(a, tile_id);
     const int cg = code_group(a, t);
     const int jb = split * a.blk_per_split;
@@ -326,13 +342,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(full(s), 1);
             tc::mbar_init(empty(s), 1);
         }
-        tc::mbar_init(q_full, kSoftmaxThreads);
+        // PAIR: one arrival per softmax warp of both CTAs, on the even CTA's barrier
+        tc::mbar_init(q_full, PAIR ? 2 * kSoftmaxWarps : kSoftmaxThreads);
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(s_full(b), 1);
-            tc::mbar_init(p_full(b), kSoftmaxThreads);
+            tc::mbar_init(p_full(b), PAIR ? 2 * kSoftmaxWarps : kSoftmaxThreads);
             tc::mbar_init(o_done(b), 1);
         }
         tc::mbar_init(mma_fin, 1);
+        tc::mbar_init(q_go, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -351,11 +369,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) *n_vis_smem = n;
     }
     if (warp == kMmaWarp) {
-        tc::tmem_alloc<512>(smem_u32(tslot));
-        tc::tmem_relinquish();
+        if constexpr (PAIR) {
+            tc::tmem_alloc_pair<512>(smem_u32(tslot));
+            tc::tmem_relinquish_pair();
+        } else {
+            tc::tmem_alloc<512>(smem_u32(tslot));
+            tc::tmem_relinquish();
+        }
     }
     tc::tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        tc::cluster_sync_all();  // the peer's barriers are initialised before any remote arrival
+    else
+        __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t tm_o = tmem;             // O: DO columns
@@ -408,19 +434,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                 next();
                 return true;
             };
+            // PAIR: one stage of this CTA's half of a tile, counted on the even CTA's
+            // full barrier (which expects both halves): K = keys [64 rank, +64) of the
+            // tile, columns [d0, d0 + 256); V = all 128 keys, output columns
+            // [d_off + 128 rank, +128).
+            // A K/V load of the odd CTA completes on the even CTA's full barrier.  When
+            // its ring slot last held this CTA's Q stage, the even CTA's barrier may
+            // still be in the phase of its own Q load; the odd CTA therefore waits,
+            // before its first such load, until the even CTA has seen both Q tiles
+            // staged (which implies its Q phases completed).
+            int pos = a.q_tma ? kQStages : 0;  // ring loads issued so far
+            bool gated = false;
+            auto load_half = [&](int j, bool is_v, int d0) -> bool {
+                if (rank == 1 && !gated && pos >= NS) {
+                    if (!wt.wait(q_go, 0)) return false;
+                    gated = true;
+                }
+                ++pos;
+                if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
+                const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
+                if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), 2 * kStageBytes);
+                const uint32_t fb = tc::mapa_shared(full(stage), 0);
+                if (is_v) {
+                    const int c1 = a.v_rows_dim1 ? j * BN : head_idx;
+                    const int c2 = a.v_rows_dim1 ? head_idx : j * BN;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        tc::tma_load_3d_pair(dst + c * (BN * 128), &tmv, fb,
+                                             d_off + (int)rank * 128 + c * 64, c1, c2);
+                } else {
+                    const int kr = j * BN + (int)rank * (BN / 2);
+                    const int c1 = a.k_rows_dim1 ? kr : head_idx;
+                    const int c2 = a.k_rows_dim1 ? head_idx : kr;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        tc::tma_load_3d_pair(dst + c * (BN / 2 * 128), &tmk, fb, d0 + c * 64, c1, c2);
+                }
+                next();
+                return true;
+            };
             // the MMA issuer consumes K of tile v+1 before V of tile v: K0, K1, V0, K2, V1, ...
-            for (int ks = 0; ks < KSUB && ok && n_vis > 0; ++ks) ok = load(tile_at(0), false, ks * 128);
-            for (int v = 0; ok && v < n_vis; ++v) {
-                for (int ks = 0; ks < KSUB && ok && v + 1 < n_vis; ++ks)
-                    ok = load(tile_at(v + 1), false, ks * 128);
-                for (int vs = 0; vs < VSUB && ok; ++vs) ok = load(tile_at(v), true, d_off + vs * 128);
+            if constexpr (PAIR) {
+                for (int ks = 0; ks < KST && ok && n_vis > 0; ++ks) ok = load_half(tile_at(0), false, ks * 256);
+                for (int v = 0; ok && v < n_vis; ++v) {
+                    for (int ks = 0; ks < KST && ok && v + 1 < n_vis; ++ks)
+                        ok = load_half(tile_at(v + 1), false, ks * 256);
+                    if (ok) ok = load_half(tile_at(v), true, 0);
+                }
+            } else {
+                for (int ks = 0; ks < KSUB && ok && n_vis > 0; ++ks) ok = load(tile_at(0), false, ks * 128);
+                for (int v = 0; ok && v < n_vis; ++v) {
+                    for (int ks = 0; ks < KSUB && ok && v + 1 < n_vis; ++ks)
+                        ok = load(tile_at(v + 1), false, ks * 128);
+                    for (int vs = 0; vs < VSUB && ok; ++vs) ok = load(tile_at(v), true, d_off + vs * 128);
+                }
             }
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc_qk = tc::idesc_f16(BM, BN, kBf16, false);
-            const uint32_t idesc_pv = tc::idesc_f16(BM, 128, kBf16, true);
+        // (PAIR: the even CTA issues for both; the odd CTA's MMA warp only
+        // takes part in the TMEM allocation)
+        if (lane == 0 && rank == 0) {
+            const uint32_t idesc_qk = tc::idesc_f16(PAIR ? 2 * BM : BM, BN, kBf16, false);
+            const uint32_t idesc_pv = tc::idesc_f16(PAIR ? 2 * BM : BM, PAIR ? DO : 128, kBf16, true);
             int stage = a.q_tma ? kQStages % NS : 0;
             uint32_t round = a.q_tma ? kQStages / NS : 0;
             auto next = [&]() {
@@ -430,7 +506,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             // S(v) = Q K^T into buffer v & 1
+            auto issue_s_pair = [&](int v) -> bool {
+                const uint32_t d_tm = tm_s + (uint32_t)(v & 1) * BN;
+                for (int ks = 0; ks < KST; ++ks) {
+                    if (!wt.wait(full(stage), round & 1)) return false;
+                    tc::tc_fence_after();
+                    const uint32_t kb = sbase + L::kStages + stage * kStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const int dq = ks * 256 + kk * 16;
+                        const uint64_t db = tc::smem_desc_sw128(
+                            kb + (kk / 4) * (BN / 2 * 128) + (kk % 4) * 32, 16, 1024);
+                        const uint64_t da = tc::smem_desc_sw128(
+                            sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16, 1024);
+                        tc::mma_f16_ss_pair(d_tm, da, db, idesc_qk, (ks | kk) != 0);
+                    }
+                    tc::mma_commit_pair(empty(stage));
+                    next();
+                }
+                tc::mma_commit_pair(s_full(v & 1));
+                return true;
+            };
             auto issue_s = [&](int v) -> bool {
+                if constexpr (PAIR) return issue_s_pair(v);
                 const uint32_t d_tm = tm_s + (uint32_t)(v & 1) * BN;
                 for (int ks = 0; ks < KSUB; ++ks) {
                     if (!wt.wait(full(stage), round & 1)) return false;
@@ -458,11 +556,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             bool ok = wt.wait(q_full, 0);
             tc::tc_fence_after();
+            if constexpr (PAIR) {
+                if (ok) tc::mbar_arrive_cluster(tc::mapa_shared(q_go, 1));
+            }
             if (ok && n_vis > 0) ok = issue_s(0);
             for (int i = 0; ok && i < n_vis; ++i) {
                 if (i + 1 < n_vis && !(ok = issue_s(i + 1))) break;
                 if (!(ok = wt.wait(p_full(i & 1), (i >> 1) & 1))) break;
                 tc::tc_fence_after();
+                if constexpr (PAIR) {
+                    // one stage: this CTA's and the peer's halves of V(i), N = DO
+                    if (!(ok = wt.wait(full(stage), round & 1))) break;
+                    tc::tc_fence_after();
+                    const uint32_t vb = sbase + L::kStages + stage * kStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
+                        tc::mma_f16_ts_pair(tm_o, tm_s + (uint32_t)(i & 1) * BN + kk * 8, db, idesc_pv,
+                                            (i | kk) != 0);
+                    }
+                    tc::mma_commit_pair(empty(stage));
+                    next();
+                    tc::mma_commit_pair(o_done(i & 1));
+                    continue;
+                }
                 // the VSUB stages of V(i) follow each other in the ring
                 int st[VSUB];
 #pragma unroll
@@ -487,8 +604,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mma_commit(o_done(i & 1));
             }
             // every MMA of this thread has finished before TMEM can be released
-            tc::mma_commit(mma_fin);
-            wt.wait(mma_fin, 0);
+            // (this wait ignores the abort flag: only the time limit ends it)
+            if constexpr (PAIR)
+                tc::mma_commit_pair(mma_fin);
+            else
+                tc::mma_commit(mma_fin);
+            const Waiter fin{abort_flag, a.status, kWaitLimitNs, false};
+            fin.wait(mma_fin, 0);
         }
         __syncwarp();
     } else {
@@ -578,7 +700,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
             tc::fence_async_smem();
         tc::tc_fence_before();
-        tc::mbar_arrive(q_full);
+        if constexpr (PAIR) {
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(q_full, 0));
+        } else {
+            tc::mbar_arrive(q_full);
+        }
 
         // ---- key tiles: this thread owns columns [h*64, h*64 + 64) of every tile
         const uint16_t *mrow = valid ? a.mask + t.lane * a.m_lane + (int64_t)head * a.m_head +
@@ -712,7 +839,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tmem_st32(tm_s + (uint32_t)(i & 1) * BN + h * 32 + lane_base, pk);
             tc::tmem_st_wait();
             tc::tc_fence_before();
-            tc::mbar_arrive(p_full(i & 1));
+            if constexpr (PAIR) {
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(p_full(i & 1), 0));
+            } else {
+                tc::mbar_arrive(p_full(i & 1));
+            }
             n_done = i + 1;
         }
 
@@ -802,12 +934,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // ---- teardown: TMEM is released only after every role is done with it
+    // ---- teardown: TMEM is released only after every role (of both CTAs of a
+    // pair) is done with it
     tc::tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        tc::cluster_sync_all();
+    else
+        __syncthreads();
     if (warp == kMmaWarp) {
         tc::tc_fence_after();
-        tc::tmem_dealloc<512>(tmem);
+        if constexpr (PAIR)
+            tc::tmem_dealloc_pair<512>(tmem);
+        else
+            tc::tmem_dealloc<512>(tmem);
     }
 }
 
@@ -858,11 +997,23 @@ struct Plan {
     int bn, do_, d_parts;
     int rows_per_head, heads_per_tile, row_tiles, head_tiles, tiles;
     int n_blk, code_cols, code_groups, splits, bps;
-    bool shared_mask;
+    bool shared_mask, pair;
     size_t codes_bytes, part_o_bytes, part_lse_bytes;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// 0: never pair; 1: pair where it measured faster (head_dim 512); 2: pair every eligible shape
+int g_pair_mode = 1;
+
+// CTA pairs need two query tiles that see the same key tiles: one head each,
+// 128 rows each, the same rows, a mask shared by all heads, an even number of
+// head tiles per KV group, and Q staged in shared memory (head_dim >= 256).
+bool pairable(int rows, int n_heads, int n_kv_heads, int head_dim, bool shared_mask) {
+    const int group = n_heads / n_kv_heads;
+    if (g_pair_mode == 0 || (g_pair_mode == 1 && head_dim != 512)) return false;
+    return shared_mask && head_dim >= 256 && rows >= BM && group % 2 == 0;
+}
 
 Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, int n_keys,
                bool shared_mask) {
@@ -881,9 +1032,13 @@ Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, i
     p.code_cols = (n_keys + 63) / 64;
     p.shared_mask = shared_mask;
     p.code_groups = shared_mask ? lanes * p.row_tiles : p.tiles;
-    const int units = p.tiles * p.d_parts;
+    p.pair = p.heads_per_tile == 1 && p.rows_per_head == BM &&
+             pairable(rows, n_heads, n_kv_heads, head_dim, shared_mask);
+    // a pair occupies two SMs
+    const int units = p.tiles * p.d_parts / (p.pair ? 2 : 1);
     int sms = sm_count();
     if (sms <= 0) sms = 148;
+    if (p.pair) sms /= 2;
     p.splits = 1;
     if (units < sms && p.n_blk > 1) {
         // one CTA per SM at most: a CTA past the SM count would run as a second wave and
@@ -947,10 +1102,10 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
     return r == CUDA_SUCCESS;
 }
 
-template <int D, class KV>
+template <int D, class KV, bool PAIR>
 cudaError_t run_attn(const AttnArgs &a, const CUtensorMap *maps, int units, int tiles,
                      cudaStream_t stream) {
-    auto kern = attn_kernel<D, KV>;
+    auto kern = attn_kernel<D, KV, PAIR>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -959,7 +1114,24 @@ cudaError_t run_attn(const AttnArgs &a, const CUtensorMap *maps, int units, int 
         configured = true;
     }
     timing_mark(true, stream);
-    kern<<<units, kThreads, Layout<D>::kBytes, stream>>>(a, maps[0], maps[1], maps[2], maps[3]);
+    if constexpr (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(units);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = Layout<D>::kBytes;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, maps[0], maps[1], maps[2], maps[3]);
+        if (e != cudaSuccess) return e;
+    } else {
+        kern<<<units, kThreads, Layout<D>::kBytes, stream>>>(a, maps[0], maps[1], maps[2], maps[3]);
+    }
     timing_mark(false, stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.splits == 1) return e;
@@ -976,8 +1148,18 @@ cudaError_t launch_bounded_wait_selftest(int32_t *status, int timeout_ms, cudaSt
 }
 
 size_t prefill_workspace_bytes(int rows, int n_heads, int n_kv_heads, int head_dim, int kv_pad) {
-    return plan_bytes(make_plan(1, rows, n_heads, n_kv_heads, head_dim, kv_pad, true));
+    // sized for either tiling, so that changing the pairing mode never
+    // invalidates a workspace the caller already holds
+    const int saved = g_pair_mode;
+    g_pair_mode = 2;
+    const size_t with = plan_bytes(make_plan(1, rows, n_heads, n_kv_heads, head_dim, kv_pad, true));
+    g_pair_mode = 0;
+    const size_t without = plan_bytes(make_plan(1, rows, n_heads, n_kv_heads, head_dim, kv_pad, true));
+    g_pair_mode = saved;
+    return with > without ? with : without;
 }
+
+void set_attention_pairs(int mode) { g_pair_mode = mode; }
 
 size_t verify_workspace_bytes(const gqa_ring_params &p) {
     return plan_bytes(make_plan((int)p.lanes, (int)p.rows, (int)p.q_heads, (int)p.kv_heads,
@@ -1034,8 +1216,9 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
         a.kv_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     a.k_rows_dim1 = rows_first(heads, p.k_row_stride, p.k_head_stride) ? 1 : 0;
     a.v_rows_dim1 = rows_first(heads, p.v_row_stride, p.v_head_stride) ? 1 : 0;
+    // CTA pairs load K in boxes of 64 keys (each CTA half of a tile)
     if (!make_map(&maps[0], p.k, kvt, 2, p.head_dim, p.kv_rows, heads, p.k_row_stride,
-                  p.k_head_stride, 64, pl.bn) ||
+                  p.k_head_stride, 64, pl.pair ? pl.bn / 2 : pl.bn) ||
         !make_map(&maps[1], p.v, kvt, 2, p.head_dim, p.kv_rows, heads, p.v_row_stride,
                   p.v_head_stride, 64, pl.bn))
         return cudaErrorInvalidValue;
@@ -1056,18 +1239,25 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     classify_kernel<<<dim3(pl.code_groups, pl.code_cols), BM, 0, stream>>>(a, const_cast<uint8_t *>(a.codes));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // CTAs launched: a pair is two CTAs, one per query tile, so the count is the same
     const int units = pl.tiles * pl.d_parts * pl.splits;
     const bool bf = a.kv_bf16;
     switch (p.head_dim) {
         case 128:
-            return bf ? run_attn<128, BF16>(a, maps, units, pl.tiles, stream)
-                      : run_attn<128, F16>(a, maps, units, pl.tiles, stream);
+            return bf ? run_attn<128, BF16, false>(a, maps, units, pl.tiles, stream)
+                      : run_attn<128, F16, false>(a, maps, units, pl.tiles, stream);
         case 256:
-            return bf ? run_attn<256, BF16>(a, maps, units, pl.tiles, stream)
-                      : run_attn<256, F16>(a, maps, units, pl.tiles, stream);
+            if (pl.pair)
+                return bf ? run_attn<256, BF16, true>(a, maps, units, pl.tiles, stream)
+                          : run_attn<256, F16, true>(a, maps, units, pl.tiles, stream);
+            return bf ? run_attn<256, BF16, false>(a, maps, units, pl.tiles, stream)
+                      : run_attn<256, F16, false>(a, maps, units, pl.tiles, stream);
         case 512:
-            return bf ? run_attn<512, BF16>(a, maps, units, pl.tiles, stream)
-                      : run_attn<512, F16>(a, maps, units, pl.tiles, stream);
+            if (pl.pair)
+                return bf ? run_attn<512, BF16, true>(a, maps, units, pl.tiles, stream)
+                          : run_attn<512, F16, true>(a, maps, units, pl.tiles, stream);
+            return bf ? run_attn<512, BF16, false>(a, maps, units, pl.tiles, stream)
+                      : run_attn<512, F16, false>(a, maps, units, pl.tiles, stream);
         default:
             return cudaErrorInvalidValue;
     }

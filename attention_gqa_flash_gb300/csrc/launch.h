@@ -52,6 +52,7 @@ struct AttnProblem {
 size_t prefill_workspace_bytes(int rows, int n_heads, int n_kv_heads, int head_dim, int kv_pad);
 size_t verify_workspace_bytes(const gqa_ring_params &p);
 cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t stream);
+void set_attention_pairs(int mode);
 cudaError_t launch_bounded_wait_selftest(int32_t *status, int timeout_ms, cudaStream_t stream);
 
 // decode.cu

@@ -92,6 +92,21 @@ float gqa_timing_last_ms(void);
  */
 int gqa_selftest_bounded_wait(int32_t *status, int timeout_ms, gqa_stream_t stream);
 
+/*
+ * Tiling mode of gqa_attn_prefill (no counterpart on the pages: a choice of
+ * this implementation).  A CTA pair runs two query tiles that see the same
+ * key tiles (two heads of one KV group, 128 rows each, head_dim 256 or 512,
+ * a mask shared by all heads) as one two-CTA cluster whose tensor cores share
+ * each K/V tile, so each SM loads half of every K and V tile.
+ *   mode 0  never pair
+ *   mode 1  pair where it measured faster on GB300: head_dim 512 (default)
+ *   mode 2  pair every eligible shape
+ * All modes give the same result up to f32 summation order.  Process-wide,
+ * not synchronised with launches in flight on other threads.  Returns
+ * GQA_OK, or GQA_INVALID_ARGUMENT for a mode outside 0..2.
+ */
+int gqa_attn_set_cta_pairs(int mode);
+
 /* ------------------------------------------------------------------------ */
 /* Prefill (mlx-native 0.18.0 flash_attn_prefill_tensor.rs: module doc,     */
 /* FlashAttnPrefillTensorParams, kv_pad, dispatch_flash_attn_prefill_tensor_f16). */

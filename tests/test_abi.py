@@ -99,3 +99,16 @@ def test_page_math_matches_the_fixed_page_capability():
     pages = lambda tokens: -(-tokens * per_token // page_bytes)
     assert pages(17) == ex["tokens_17_physical_pages"]
     assert pages(ex["maximum_context_tokens"]) == ex["maximum_pages"]
+
+
+def test_cta_pair_mode_is_validated_and_keeps_workspace_size(g):
+    lib = g.library()
+    assert lib.gqa_attn_set_cta_pairs(3) == 1
+    assert "mode 3" in lib.gqa_last_error().decode()
+    sizes = []
+    for mode in (0, 1, 2):
+        assert lib.gqa_attn_set_cta_pairs(mode) == 0
+        # a shape that pairs in mode 2 and splits its keys: the workspace must not depend on the mode
+        sizes.append(g.gqa_attn_prefill_workspace_size(128, 2, 1, 256, 4032))
+    lib.gqa_attn_set_cta_pairs(1)
+    assert len(set(sizes)) == 1 and sizes[0] > 0

@@ -19,6 +19,15 @@ def lib():
     return g
 
 
+@pytest.fixture(params=[2, 0], ids=["cta_pairs", "single_ctas"])
+def pairs_mode(request, lib):
+    """Run a test with two-CTA clusters on for every eligible shape (mode 2) and
+    off (mode 0); shapes that cannot pair take the single-CTA kernel either way."""
+    lib.gqa_attn_set_cta_pairs(request.param)
+    yield request.param
+    lib.gqa_attn_set_cta_pairs(1)
+
+
 def _run(g, c, q=None, k=None, v=None, mask=None):
     import torch
     from gpu_helpers import dev, new_status
@@ -49,8 +58,11 @@ def test_tiny_prefill_full(lib):
     (130, 130, 2, 1, 512, 0, "f16"),       # d512 in two output halves, ragged tail
     (96, 500, 8, 2, 256, 404, "bf16"),     # bf16 K/V, few rows, prefix
     (64, 64, 4, 2, 128, 0, "bf16"),
+    (256, 384, 8, 2, 256, 128, "bf16"),    # two pairs per KV head, bf16, prefix
+    (128, 4000, 2, 1, 256, 3872, "f16"),   # one pair, keys split across many clusters
+    (300, 700, 4, 2, 512, 400, "f16"),     # d512 pairs, ragged rows and keys
 ])
-def test_prefill_shapes(lib, rows, kv_len, h, hk, d, pos0, dtype):
+def test_prefill_shapes(lib, pairs_mode, rows, kv_len, h, hk, d, pos0, dtype):
     from gpu_helpers import assert_attention_close
     c = workloads.prefill(rows=rows, kv_len=kv_len, n_heads=h, n_kv_heads=hk, head_dim=d,
                           position0=pos0, q_std=d ** -0.5, scale=1.0, kv_dtype=dtype,
@@ -92,7 +104,7 @@ def _sampled_pairs(c, n=48, seed=0):
     return np.stack([rows, heads], axis=1).astype(np.int32)
 
 
-def test_full_size_d256_sampled(lib):
+def test_full_size_d256_sampled(lib, pairs_mode):
     from gpu_helpers import assert_attention_close
     c = workloads.prefill_d256()
     got = _run(lib, c)
@@ -102,7 +114,7 @@ def test_full_size_d256_sampled(lib):
     assert_attention_close(got[pairs[:, 0], pairs[:, 1]], ref, "prefill d256 full size")
 
 
-def test_full_size_d512_prefix_sampled(lib):
+def test_full_size_d512_prefix_sampled(lib, pairs_mode):
     from gpu_helpers import assert_attention_close
     c = workloads.prefill_d512_prefix()
     got = _run(lib, c)
