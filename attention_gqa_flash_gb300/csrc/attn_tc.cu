@@ -234,11 +234,17 @@ struct Waiter {
     int32_t *status;
     uint64_t limit_ns;
     bool honour_abort = true;  // false: only the time limit ends the wait
+    // CLUSTER: poll without suspending, acquire at cluster scope (phases completed
+    // by the other CTA of a pair)
+    template <bool CLUSTER = false>
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
-        if (tc::mbar_try_wait(bar, parity)) return true;
+        auto try_once = [&]() {
+            return CLUSTER ? tc::mbar_test_wait_cluster(bar, parity) : tc::mbar_try_wait(bar, parity);
+        };
+        if (try_once()) return true;
         const uint64_t t0 = tc::globaltimer_ns();
         for (uint32_t it = 1;; ++it) {
-            if (tc::mbar_try_wait(bar, parity)) return true;
+            if (try_once()) return true;
             if ((it & 127) == 0) {
                 if (honour_abort && *abort) return false;
                 if (tc::globaltimer_ns() - t0 > limit_ns) {
@@ -346,7 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_init(q_full, PAIR ? 2 * kSoftmaxWarps : kSoftmaxThreads);
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(s_full(b), 1);
-            tc::mbar_init(p_full(b), PAIR ? 2 * kSoftmaxWarps : kSoftmaxThreads);
+            // PAIR: one local arrival per softmax warp; the even CTA's barrier also
+            // takes the odd CTA's relayed arrival
+            tc::mbar_init(p_full(b), PAIR ? kSoftmaxWarps + (rank == 0 ? 1 : 0) : kSoftmaxThreads);
             tc::mbar_init(o_done(b), 1);
         }
         tc::mbar_init(mma_fin, 1);
@@ -447,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool gated = false;
             auto load_half = [&](int j, bool is_v, int d0) -> bool {
                 if (rank == 1 && !gated && pos >= NS) {
-                    if (!wt.wait(q_go, 0)) return false;
+                    if (!wt.template wait<true>(q_go, 0)) return false;
                     gated = true;
                 }
                 ++pos;
@@ -509,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_s_pair = [&](int v) -> bool {
                 const uint32_t d_tm = tm_s + (uint32_t)(v & 1) * BN;
                 for (int ks = 0; ks < KST; ++ks) {
-                    if (!wt.wait(full(stage), round & 1)) return false;
+                    if (!wt.template wait<true>(full(stage), round & 1)) return false;
                     tc::tc_fence_after();
                     const uint32_t kb = sbase + L::kStages + stage * kStageBytes;
 #pragma unroll
@@ -554,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mma_commit(s_full(v & 1));
                 return true;
             };
-            bool ok = wt.wait(q_full, 0);
+            bool ok = wt.template wait<PAIR>(q_full, 0);
             tc::tc_fence_after();
             if constexpr (PAIR) {
                 if (ok) tc::mbar_arrive_cluster(tc::mapa_shared(q_go, 1));
@@ -562,11 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && n_vis > 0) ok = issue_s(0);
             for (int i = 0; ok && i < n_vis; ++i) {
                 if (i + 1 < n_vis && !(ok = issue_s(i + 1))) break;
-                if (!(ok = wt.wait(p_full(i & 1), (i >> 1) & 1))) break;
+                if (!(ok = wt.template wait<PAIR>(p_full(i & 1), (i >> 1) & 1))) break;
                 tc::tc_fence_after();
                 if constexpr (PAIR) {
                     // one stage: this CTA's and the peer's halves of V(i), N = DO
-                    if (!(ok = wt.wait(full(stage), round & 1))) break;
+                    if (!(ok = wt.template wait<true>(full(stage), round & 1))) break;
                     tc::tc_fence_after();
                     const uint32_t vb = sbase + L::kStages + stage * kStageBytes;
 #pragma unroll
@@ -611,6 +619,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::mma_commit(mma_fin);
             const Waiter fin{abort_flag, a.status, kWaitLimitNs, false};
             fin.wait(mma_fin, 0);
+        }
+        if constexpr (PAIR) {
+            // odd CTA: forward each tile's "P written" from this CTA's softmax warps to
+            // the even CTA's barrier with one arrival, so that the softmax warps
+            // themselves only arrive locally.  Every phase is seen in turn: P(i + 2)
+            // needs S(i + 2), which the even CTA issues only after this arrival for P(i).
+            // The P stores were complete (tcgen05.wait::st) before the warps arrived
+            // locally, so the forwarded arrival needs no release.
+            if (lane == 0 && rank == 1) {
+                for (int i = 0; i < n_vis; ++i) {
+                    if (!wt.template wait<true>(p_full(i & 1), (i >> 1) & 1)) break;
+                    tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(p_full(i & 1), 0));
+                }
+            }
         }
         __syncwarp();
     } else {
@@ -841,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tc_fence_before();
             if constexpr (PAIR) {
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(p_full(i & 1), 0));
+                if (lane == 0) tc::mbar_arrive(p_full(i & 1));
             } else {
                 tc::mbar_arrive(p_full(i & 1));
             }

@@ -37,6 +37,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-suspending test with acquire at cluster scope, for phases completed by
+// the other CTA of a pair (its arrivals or its TMA loads): a suspended
+// try_wait was measured to notice such completions ~1.5k cycles late.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -212,6 +227,14 @@ __device__ __forceinline__ void cluster_sync_all() {
 // arrive on an mbarrier given by its shared::cluster address (this CTA's or the peer's)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+// Arrive without release semantics.  For signals whose data is already
+// complete when the arrive is issued (e.g. tensor-memory stores finished by
+// tcgen05.wait::st before a local barrier the signalling thread waited on):
+// inside a busy CTA the release form was measured to block for 1-2k cycles.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
 // tiled load into this CTA's shared memory whose completion is counted on the
