@@ -745,6 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) ok = __all_sync(0xffffffffu, wt.wait(s_full(i & 1), (i >> 1) & 1));
             float s[64];
             float mx = kNegInf;
+            float sc = 1.f;  // factor still to apply to s (log2 domain)
             if (ok) {
                 tc::tc_fence_after();
                 {
@@ -764,8 +765,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 64; ++c) s[c] = kNegInf;
                 } else if (code == 1) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) s[c] *= a.scale_log2;
+                    // no mask: s stays unscaled; the scale is applied inside the exponent
+                    // argument below, and the row maximum is taken on the raw scores
+                    sc = a.scale_log2;
                 } else {
                     const int c0 = j * BN + h * 64;  // key index of s[0]
                     if (m_vec && c0 + 64 <= a.n_keys) {
@@ -789,16 +791,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        : kNegInf;
                     }
                 }
-                // row max over this half with four independent chains
+                // row max of sc * s over this half (four chains of three-input max; with
+                // a negative scale the maximum comes from the smallest raw score)
                 float mq[4] = {s[0], s[1], s[2], s[3]};
+                if (sc >= 0.f) {
 #pragma unroll
-                for (int c = 4; c < 64; c += 4) {
-                    mq[0] = fmaxf(mq[0], s[c]);
-                    mq[1] = fmaxf(mq[1], s[c + 1]);
-                    mq[2] = fmaxf(mq[2], s[c + 2]);
-                    mq[3] = fmaxf(mq[3], s[c + 3]);
+                    for (int c = 4; c < 60; c += 8)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) mq[k] = fmax3(mq[k], s[c + k], s[c + 4 + k]);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) mq[k] = fmaxf(mq[k], s[60 + k]);
+                    mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+                } else {
+#pragma unroll
+                    for (int c = 4; c < 60; c += 8)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) mq[k] = fmin3(mq[k], s[c + k], s[c + 4 + k]);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) mq[k] = fminf(mq[k], s[60 + k]);
+                    mx = fmin3(mq[0], mq[1], fminf(mq[2], mq[3]));
                 }
-                mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+                mx *= sc;
             }
             // agree with the other half of the row on the maximum
             float *xs = xchg + (i & 1) * 2 * BM;
@@ -815,21 +828,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = mx;
                 resc = true;
             }
-            const float mu = m_ref == kNegInf ? 0.f : m_ref;
+            const float nmu = m_ref == kNegInf ? 0.f : -m_ref;
             uint32_t pk[32];
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};
+            float ra0 = 0.f, ra1 = 0.f, rb0 = 0.f, rb1 = 0.f;
 #pragma unroll
             for (int c = 0; c < 64; c += 4) {
-                const float p0 = ex2(s[c] - mu), p1 = ex2(s[c + 1] - mu);
-                const float p2 = ex2(s[c + 2] - mu), p3 = ex2(s[c + 3] - mu);
-                rs[0] += p0;
-                rs[1] += p1;
-                rs[2] += p2;
-                rs[3] += p3;
+                // p = 2^(sc * s - mu): one packed FMA per two arguments
+                float x0, x1, x2, x3;
+                ffma2(x0, x1, s[c], s[c + 1], sc, sc, nmu, nmu);
+                ffma2(x2, x3, s[c + 2], s[c + 3], sc, sc, nmu, nmu);
+                const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+                fadd2(ra0, ra1, ra0, ra1, p0, p1);
+                fadd2(rb0, rb1, rb0, rb1, p2, p3);
                 pk[c / 2] = pack2(KV{}, p0, p1);
                 pk[c / 2 + 1] = pack2(KV{}, p2, p3);
             }
-            l = l * factor + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+            l = l * factor + ((ra0 + ra1) + (rb0 + rb1));
             // P.V of the previous tile must be done before O is rescaled.  P goes
             // over this tile's own S buffer, which the previous P.V does not read,
             // so without a rescale the softmax runs ahead of the tensor pipe.
