@@ -48,8 +48,14 @@ constexpr int BM = 128;                  // query rows per tile (TMEM lanes)
 constexpr int BN = 128;                  // keys per tile
 constexpr int kSoftmaxWarps = 8;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;  // warps 10 and 11 only complete their warpgroup
+constexpr int kThreads = 384;
+// Register split: the launch gives every thread the same count (at most 168 with
+// three warps per SM sub-partition); the softmax warpgroups then raise theirs so
+// that their 64 scores, 32 packed P words and the rest stay in registers, and
+// the producer / MMA warpgroup lowers its own.  Sum: 256 x 224 + 128 x 56 = 64512,
+// within 384 x 168 = 64512 (checked against the compiled count before launch).
+constexpr int kSoftmaxRegs = 224, kControlRegs = 56;
 constexpr int kStageBytes = 32768;       // 128 rows x 128 columns of 16-bit, or 128 x 64 f32
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
@@ -398,244 +404,251 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_vis = *n_vis_smem;
     auto tile_at = [&](int v) { return jb + (list[v] & 0x7fff); };
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            tc::prefetch_tmap(&tmk);
-            tc::prefetch_tmap(&tmv);
-            int stage = 0;
-            uint32_t round = 0;
-            auto next = [&]() {
-                if (++stage == NS) {
-                    stage = 0;
-                    ++round;
+    // Register split per warpgroup (every warp of a warpgroup executes its
+    // setmaxnreg): warps 8-11 (producer, MMA issuer, two idle) lower theirs, the
+    // softmax warpgroups raise theirs.
+    if (warp >= kSoftmaxWarps) {
+        tc::setmaxnreg_dec<kControlRegs>();
+        if (warp == kProducerWarp) {
+            // ------------------------------------------------------------ producer
+            if (lane == 0) {
+                tc::prefetch_tmap(&tmk);
+                tc::prefetch_tmap(&tmv);
+                int stage = 0;
+                uint32_t round = 0;
+                auto next = [&]() {
+                    if (++stage == NS) {
+                        stage = 0;
+                        ++round;
+                    }
+                };
+                bool ok = true;
+                // f32 Q tile first (consumed by the softmax warps): [128 rows][32 f32] boxes
+                if (a.q_tma) {
+                    tc::prefetch_tmap(&tmq);
+                    for (int qs = 0; qs < kQStages && ok; ++qs) {
+                        if (!(ok = wt.wait(empty(stage), (round & 1) ^ 1))) break;
+                        const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
+                        tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
+#pragma unroll
+                        for (int b = 0; b < 2; ++b)
+                            tc::tma_load_3d(dst + b * 16384, &tmq, full(stage), qs * 64 + b * 32,
+                                            a.q_rows_dim1 ? q_row0 : q_head0,
+                                            a.q_rows_dim1 ? q_head0 : q_row0);
+                        next();
+                    }
                 }
-            };
-            bool ok = true;
-            // f32 Q tile first (consumed by the softmax warps): [128 rows][32 f32] boxes
-            if (a.q_tma) {
-                tc::prefetch_tmap(&tmq);
-                for (int qs = 0; qs < kQStages && ok; ++qs) {
-                    if (!(ok = wt.wait(empty(stage), (round & 1) ^ 1))) break;
+                // one stage: two boxes of [BN rows][64 columns] of K or V starting at column d0
+                auto load = [&](int j, bool is_v, int d0) -> bool {
+                    if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
                     const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
                     tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
-#pragma unroll
-                    for (int b = 0; b < 2; ++b)
-                        tc::tma_load_3d(dst + b * 16384, &tmq, full(stage), qs * 64 + b * 32,
-                                        a.q_rows_dim1 ? q_row0 : q_head0,
-                                        a.q_rows_dim1 ? q_head0 : q_row0);
-                    next();
-                }
-            }
-            // one stage: two boxes of [BN rows][64 columns] of K or V starting at column d0
-            auto load = [&](int j, bool is_v, int d0) -> bool {
-                if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
-                const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
-                tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
-                const int rows_dim1 = is_v ? a.v_rows_dim1 : a.k_rows_dim1;
-                const int c1 = rows_dim1 ? j * BN : head_idx;
-                const int c2 = rows_dim1 ? head_idx : j * BN;
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    tc::tma_load_3d(dst + c * (BN * 128), is_v ? (const void *)&tmv : (const void *)&tmk,
-                                    full(stage), d0 + c * 64, c1, c2);
-                next();
-                return true;
-            };
-            // PAIR: one stage of this CTA's half of a tile, counted on the even CTA's
-            // full barrier (which expects both halves): K = keys [64 rank, +64) of the
-            // tile, columns [d0, d0 + 256); V = all 128 keys, output columns
-            // [d_off + 128 rank, +128).
-            // A K/V load of the odd CTA completes on the even CTA's full barrier.  When
-            // its ring slot last held this CTA's Q stage, the even CTA's barrier may
-            // still be in the phase of its own Q load; the odd CTA therefore waits,
-            // before its first such load, until the even CTA has seen both Q tiles
-            // staged (which implies its Q phases completed).
-            int pos = a.q_tma ? kQStages : 0;  // ring loads issued so far
-            bool gated = false;
-            auto load_half = [&](int j, bool is_v, int d0) -> bool {
-                if (rank == 1 && !gated && pos >= NS) {
-                    if (!wt.template wait<true>(q_go, 0)) return false;
-                    gated = true;
-                }
-                ++pos;
-                if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
-                const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
-                if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), 2 * kStageBytes);
-                const uint32_t fb = tc::mapa_shared(full(stage), 0);
-                if (is_v) {
-                    const int c1 = a.v_rows_dim1 ? j * BN : head_idx;
-                    const int c2 = a.v_rows_dim1 ? head_idx : j * BN;
+                    const int rows_dim1 = is_v ? a.v_rows_dim1 : a.k_rows_dim1;
+                    const int c1 = rows_dim1 ? j * BN : head_idx;
+                    const int c2 = rows_dim1 ? head_idx : j * BN;
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
-                        tc::tma_load_3d_pair(dst + c * (BN * 128), &tmv, fb,
-                                             d_off + (int)rank * 128 + c * 64, c1, c2);
+                        tc::tma_load_3d(dst + c * (BN * 128), is_v ? (const void *)&tmv : (const void *)&tmk,
+                                        full(stage), d0 + c * 64, c1, c2);
+                    next();
+                    return true;
+                };
+                // PAIR: one stage of this CTA's half of a tile, counted on the even CTA's
+                // full barrier (which expects both halves): K = keys [64 rank, +64) of the
+                // tile, columns [d0, d0 + 256); V = all 128 keys, output columns
+                // [d_off + 128 rank, +128).
+                // A K/V load of the odd CTA completes on the even CTA's full barrier.  When
+                // its ring slot last held this CTA's Q stage, the even CTA's barrier may
+                // still be in the phase of its own Q load; the odd CTA therefore waits,
+                // before its first such load, until the even CTA has seen both Q tiles
+                // staged (which implies its Q phases completed).
+                int pos = a.q_tma ? kQStages : 0;  // ring loads issued so far
+                bool gated = false;
+                auto load_half = [&](int j, bool is_v, int d0) -> bool {
+                    if (rank == 1 && !gated && pos >= NS) {
+                        if (!wt.template wait<true>(q_go, 0)) return false;
+                        gated = true;
+                    }
+                    ++pos;
+                    if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
+                    const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
+                    if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), 2 * kStageBytes);
+                    const uint32_t fb = tc::mapa_shared(full(stage), 0);
+                    if (is_v) {
+                        const int c1 = a.v_rows_dim1 ? j * BN : head_idx;
+                        const int c2 = a.v_rows_dim1 ? head_idx : j * BN;
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            tc::tma_load_3d_pair(dst + c * (BN * 128), &tmv, fb,
+                                                 d_off + (int)rank * 128 + c * 64, c1, c2);
+                    } else {
+                        const int kr = j * BN + (int)rank * (BN / 2);
+                        const int c1 = a.k_rows_dim1 ? kr : head_idx;
+                        const int c2 = a.k_rows_dim1 ? head_idx : kr;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            tc::tma_load_3d_pair(dst + c * (BN / 2 * 128), &tmk, fb, d0 + c * 64, c1, c2);
+                    }
+                    next();
+                    return true;
+                };
+                // the MMA issuer consumes K of tile v+1 before V of tile v: K0, K1, V0, K2, V1, ...
+                if constexpr (PAIR) {
+                    for (int ks = 0; ks < KST && ok && n_vis > 0; ++ks) ok = load_half(tile_at(0), false, ks * 256);
+                    for (int v = 0; ok && v < n_vis; ++v) {
+                        for (int ks = 0; ks < KST && ok && v + 1 < n_vis; ++ks)
+                            ok = load_half(tile_at(v + 1), false, ks * 256);
+                        if (ok) ok = load_half(tile_at(v), true, 0);
+                    }
                 } else {
-                    const int kr = j * BN + (int)rank * (BN / 2);
-                    const int c1 = a.k_rows_dim1 ? kr : head_idx;
-                    const int c2 = a.k_rows_dim1 ? head_idx : kr;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        tc::tma_load_3d_pair(dst + c * (BN / 2 * 128), &tmk, fb, d0 + c * 64, c1, c2);
-                }
-                next();
-                return true;
-            };
-            // the MMA issuer consumes K of tile v+1 before V of tile v: K0, K1, V0, K2, V1, ...
-            if constexpr (PAIR) {
-                for (int ks = 0; ks < KST && ok && n_vis > 0; ++ks) ok = load_half(tile_at(0), false, ks * 256);
-                for (int v = 0; ok && v < n_vis; ++v) {
-                    for (int ks = 0; ks < KST && ok && v + 1 < n_vis; ++ks)
-                        ok = load_half(tile_at(v + 1), false, ks * 256);
-                    if (ok) ok = load_half(tile_at(v), true, 0);
-                }
-            } else {
-                for (int ks = 0; ks < KSUB && ok && n_vis > 0; ++ks) ok = load(tile_at(0), false, ks * 128);
-                for (int v = 0; ok && v < n_vis; ++v) {
-                    for (int ks = 0; ks < KSUB && ok && v + 1 < n_vis; ++ks)
-                        ok = load(tile_at(v + 1), false, ks * 128);
-                    for (int vs = 0; vs < VSUB && ok; ++vs) ok = load(tile_at(v), true, d_off + vs * 128);
+                    for (int ks = 0; ks < KSUB && ok && n_vis > 0; ++ks) ok = load(tile_at(0), false, ks * 128);
+                    for (int v = 0; ok && v < n_vis; ++v) {
+                        for (int ks = 0; ks < KSUB && ok && v + 1 < n_vis; ++ks)
+                            ok = load(tile_at(v + 1), false, ks * 128);
+                        for (int vs = 0; vs < VSUB && ok; ++vs) ok = load(tile_at(v), true, d_off + vs * 128);
+                    }
                 }
             }
-        }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        // (PAIR: the even CTA issues for both; the odd CTA's MMA warp only
-        // takes part in the TMEM allocation)
-        if (lane == 0 && rank == 0) {
-            const uint32_t idesc_qk = tc::idesc_f16(PAIR ? 2 * BM : BM, BN, kBf16, false);
-            const uint32_t idesc_pv = tc::idesc_f16(PAIR ? 2 * BM : BM, PAIR ? DO : 128, kBf16, true);
-            int stage = a.q_tma ? kQStages % NS : 0;
-            uint32_t round = a.q_tma ? kQStages / NS : 0;
-            auto next = [&]() {
-                if (++stage == NS) {
-                    stage = 0;
-                    ++round;
-                }
-            };
-            // S(v) = Q K^T into buffer v & 1
-            auto issue_s_pair = [&](int v) -> bool {
-                const uint32_t d_tm = tm_s + (uint32_t)(v & 1) * BN;
-                for (int ks = 0; ks < KST; ++ks) {
-                    if (!wt.template wait<true>(full(stage), round & 1)) return false;
-                    tc::tc_fence_after();
-                    const uint32_t kb = sbase + L::kStages + stage * kStageBytes;
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        const int dq = ks * 256 + kk * 16;
-                        const uint64_t db = tc::smem_desc_sw128(
-                            kb + (kk / 4) * (BN / 2 * 128) + (kk % 4) * 32, 16, 1024);
-                        const uint64_t da = tc::smem_desc_sw128(
-                            sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16, 1024);
-                        tc::mma_f16_ss_pair(d_tm, da, db, idesc_qk, (ks | kk) != 0);
+        } else if (warp == kMmaWarp) {
+            // ------------------------------------------------------------ MMA issuer
+            // (PAIR: the even CTA issues for both; the odd CTA's MMA warp only
+            // takes part in the TMEM allocation)
+            if (lane == 0 && rank == 0) {
+                const uint32_t idesc_qk = tc::idesc_f16(PAIR ? 2 * BM : BM, BN, kBf16, false);
+                const uint32_t idesc_pv = tc::idesc_f16(PAIR ? 2 * BM : BM, PAIR ? DO : 128, kBf16, true);
+                int stage = a.q_tma ? kQStages % NS : 0;
+                uint32_t round = a.q_tma ? kQStages / NS : 0;
+                auto next = [&]() {
+                    if (++stage == NS) {
+                        stage = 0;
+                        ++round;
                     }
-                    tc::mma_commit_pair(empty(stage));
-                    next();
-                }
-                tc::mma_commit_pair(s_full(v & 1));
-                return true;
-            };
-            auto issue_s = [&](int v) -> bool {
-                if constexpr (PAIR) return issue_s_pair(v);
-                const uint32_t d_tm = tm_s + (uint32_t)(v & 1) * BN;
-                for (int ks = 0; ks < KSUB; ++ks) {
-                    if (!wt.wait(full(stage), round & 1)) return false;
-                    tc::tc_fence_after();
-                    const uint32_t kb = sbase + L::kStages + stage * kStageBytes;
+                };
+                // S(v) = Q K^T into buffer v & 1
+                auto issue_s_pair = [&](int v) -> bool {
+                    const uint32_t d_tm = tm_s + (uint32_t)(v & 1) * BN;
+                    for (int ks = 0; ks < KST; ++ks) {
+                        if (!wt.template wait<true>(full(stage), round & 1)) return false;
+                        tc::tc_fence_after();
+                        const uint32_t kb = sbase + L::kStages + stage * kStageBytes;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const int dq = ks * 128 + kk * 16;
-                        const uint64_t db =
-                            tc::smem_desc_sw128(kb + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
-                        if constexpr (C::QTM) {
-                            tc::mma_f16_ts(d_tm, tm_q + dq / 2, db, idesc_qk, (ks | kk) != 0);
-                        } else {
+                        for (int kk = 0; kk < 16; ++kk) {
+                            const int dq = ks * 256 + kk * 16;
+                            const uint64_t db = tc::smem_desc_sw128(
+                                kb + (kk / 4) * (BN / 2 * 128) + (kk % 4) * 32, 16, 1024);
                             const uint64_t da = tc::smem_desc_sw128(
-                                sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16,
-                                1024);
-                            tc::mma_f16_ss(d_tm, da, db, idesc_qk, (ks | kk) != 0);
+                                sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16, 1024);
+                            tc::mma_f16_ss_pair(d_tm, da, db, idesc_qk, (ks | kk) != 0);
                         }
+                        tc::mma_commit_pair(empty(stage));
+                        next();
                     }
-                    tc::mma_commit(empty(stage));
-                    next();
-                }
-                tc::mma_commit(s_full(v & 1));
-                return true;
-            };
-            bool ok = wt.template wait<PAIR>(q_full, 0);
-            tc::tc_fence_after();
-            if constexpr (PAIR) {
-                if (ok) tc::mbar_arrive_cluster(tc::mapa_shared(q_go, 1));
-            }
-            if (ok && n_vis > 0) ok = issue_s(0);
-            for (int i = 0; ok && i < n_vis; ++i) {
-                if (i + 1 < n_vis && !(ok = issue_s(i + 1))) break;
-                if (!(ok = wt.template wait<PAIR>(p_full(i & 1), (i >> 1) & 1))) break;
+                    tc::mma_commit_pair(s_full(v & 1));
+                    return true;
+                };
+                auto issue_s = [&](int v) -> bool {
+                    if constexpr (PAIR) return issue_s_pair(v);
+                    const uint32_t d_tm = tm_s + (uint32_t)(v & 1) * BN;
+                    for (int ks = 0; ks < KSUB; ++ks) {
+                        if (!wt.wait(full(stage), round & 1)) return false;
+                        tc::tc_fence_after();
+                        const uint32_t kb = sbase + L::kStages + stage * kStageBytes;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const int dq = ks * 128 + kk * 16;
+                            const uint64_t db =
+                                tc::smem_desc_sw128(kb + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
+                            if constexpr (C::QTM) {
+                                tc::mma_f16_ts(d_tm, tm_q + dq / 2, db, idesc_qk, (ks | kk) != 0);
+                            } else {
+                                const uint64_t da = tc::smem_desc_sw128(
+                                    sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16,
+                                    1024);
+                                tc::mma_f16_ss(d_tm, da, db, idesc_qk, (ks | kk) != 0);
+                            }
+                        }
+                        tc::mma_commit(empty(stage));
+                        next();
+                    }
+                    tc::mma_commit(s_full(v & 1));
+                    return true;
+                };
+                bool ok = wt.template wait<PAIR>(q_full, 0);
                 tc::tc_fence_after();
                 if constexpr (PAIR) {
-                    // one stage: this CTA's and the peer's halves of V(i), N = DO
-                    if (!(ok = wt.template wait<true>(full(stage), round & 1))) break;
+                    if (ok) tc::mbar_arrive_cluster(tc::mapa_shared(q_go, 1));
+                }
+                if (ok && n_vis > 0) ok = issue_s(0);
+                for (int i = 0; ok && i < n_vis; ++i) {
+                    if (i + 1 < n_vis && !(ok = issue_s(i + 1))) break;
+                    if (!(ok = wt.template wait<PAIR>(p_full(i & 1), (i >> 1) & 1))) break;
                     tc::tc_fence_after();
-                    const uint32_t vb = sbase + L::kStages + stage * kStageBytes;
+                    if constexpr (PAIR) {
+                        // one stage: this CTA's and the peer's halves of V(i), N = DO
+                        if (!(ok = wt.template wait<true>(full(stage), round & 1))) break;
+                        tc::tc_fence_after();
+                        const uint32_t vb = sbase + L::kStages + stage * kStageBytes;
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
-                        tc::mma_f16_ts_pair(tm_o, tm_s + (uint32_t)(i & 1) * BN + kk * 8, db, idesc_pv,
-                                            (i | kk) != 0);
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
+                            tc::mma_f16_ts_pair(tm_o, tm_s + (uint32_t)(i & 1) * BN + kk * 8, db, idesc_pv,
+                                                (i | kk) != 0);
+                        }
+                        tc::mma_commit_pair(empty(stage));
+                        next();
+                        tc::mma_commit_pair(o_done(i & 1));
+                        continue;
                     }
-                    tc::mma_commit_pair(empty(stage));
-                    next();
-                    tc::mma_commit_pair(o_done(i & 1));
-                    continue;
-                }
-                // the VSUB stages of V(i) follow each other in the ring
-                int st[VSUB];
-#pragma unroll
-                for (int vs = 0; vs < VSUB; ++vs) {
-                    if (ok) ok = wt.wait(full(stage), round & 1);
-                    st[vs] = stage;
-                    next();
-                }
-                if (!ok) break;
-                tc::tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
+                    // the VSUB stages of V(i) follow each other in the ring
+                    int st[VSUB];
 #pragma unroll
                     for (int vs = 0; vs < VSUB; ++vs) {
-                        const uint32_t vb = sbase + L::kStages + st[vs] * kStageBytes;
-                        const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
-                        tc::mma_f16_ts(tm_o + vs * 128, tm_s + (uint32_t)(i & 1) * BN + kk * 8, db,
-                                       idesc_pv, (i | kk) != 0);
+                        if (ok) ok = wt.wait(full(stage), round & 1);
+                        st[vs] = stage;
+                        next();
                     }
+                    if (!ok) break;
+                    tc::tc_fence_after();
 #pragma unroll
-                for (int vs = 0; vs < VSUB; ++vs) tc::mma_commit(empty(st[vs]));
-                tc::mma_commit(o_done(i & 1));
+                    for (int kk = 0; kk < BN / 16; ++kk)
+#pragma unroll
+                        for (int vs = 0; vs < VSUB; ++vs) {
+                            const uint32_t vb = sbase + L::kStages + st[vs] * kStageBytes;
+                            const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
+                            tc::mma_f16_ts(tm_o + vs * 128, tm_s + (uint32_t)(i & 1) * BN + kk * 8, db,
+                                           idesc_pv, (i | kk) != 0);
+                        }
+#pragma unroll
+                    for (int vs = 0; vs < VSUB; ++vs) tc::mma_commit(empty(st[vs]));
+                    tc::mma_commit(o_done(i & 1));
+                }
+                // every MMA of this thread has finished before TMEM can be released
+                // (this wait ignores the abort flag: only the time limit ends it)
+                if constexpr (PAIR)
+                    tc::mma_commit_pair(mma_fin);
+                else
+                    tc::mma_commit(mma_fin);
+                const Waiter fin{abort_flag, a.status, kWaitLimitNs, false};
+                fin.wait(mma_fin, 0);
             }
-            // every MMA of this thread has finished before TMEM can be released
-            // (this wait ignores the abort flag: only the time limit ends it)
-            if constexpr (PAIR)
-                tc::mma_commit_pair(mma_fin);
-            else
-                tc::mma_commit(mma_fin);
-            const Waiter fin{abort_flag, a.status, kWaitLimitNs, false};
-            fin.wait(mma_fin, 0);
-        }
-        if constexpr (PAIR) {
-            // odd CTA: forward each tile's "P written" from this CTA's softmax warps to
-            // the even CTA's barrier with one arrival, so that the softmax warps
-            // themselves only arrive locally.  Every phase is seen in turn: P(i + 2)
-            // needs S(i + 2), which the even CTA issues only after this arrival for P(i).
-            // The P stores were complete (tcgen05.wait::st) before the warps arrived
-            // locally, so the forwarded arrival needs no release.
-            if (lane == 0 && rank == 1) {
-                for (int i = 0; i < n_vis; ++i) {
-                    if (!wt.template wait<true>(p_full(i & 1), (i >> 1) & 1)) break;
-                    tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(p_full(i & 1), 0));
+            if constexpr (PAIR) {
+                // odd CTA: forward each tile's "P written" from this CTA's softmax warps to
+                // the even CTA's barrier with one arrival, so that the softmax warps
+                // themselves only arrive locally.  Every phase is seen in turn: P(i + 2)
+                // needs S(i + 2), which the even CTA issues only after this arrival for P(i).
+                // The P stores were complete (tcgen05.wait::st) before the warps arrived
+                // locally, so the forwarded arrival needs no release.
+                if (lane == 0 && rank == 1) {
+                    for (int i = 0; i < n_vis; ++i) {
+                        if (!wt.template wait<true>(p_full(i & 1), (i >> 1) & 1)) break;
+                        tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(p_full(i & 1), 0));
+                    }
                 }
             }
+            __syncwarp();
         }
-        __syncwarp();
     } else {
+        tc::setmaxnreg_inc<kSoftmaxRegs>();
         // ------------------------------------------------------------ softmax
         // warp w: rows 32 (w % 4) .. + 31 (TMEM lanes), column half h = w / 4
         const int r = (warp & 3) * 32 + lane;
@@ -1147,6 +1160,14 @@ cudaError_t run_attn(const AttnArgs &a, const CUtensorMap *maps, int units, int 
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Layout<D>::kBytes);
         if (e != cudaSuccess) return e;
+        // the register split must fit in what the block is launched with, or the
+        // softmax warpgroups' increase would wait forever
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        if (2 * 128 * kSoftmaxRegs + 128 * kControlRegs > kThreads * fa.numRegs ||
+            kSoftmaxRegs < fa.numRegs || kControlRegs > fa.numRegs)
+            return cudaErrorInvalidConfiguration;
         configured = true;
     }
     timing_mark(true, stream);

@@ -290,6 +290,20 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
 }
 
 // ---------------------------------------------------------------------------
+// register redistribution between warpgroups (every warp of a warpgroup
+// executes the same instruction; an increase waits until decreases elsewhere
+// in the CTA have released enough registers)
+// ---------------------------------------------------------------------------
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------
 // descriptors
 // ---------------------------------------------------------------------------
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA's
