@@ -290,7 +290,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int c16) {
 // SM takes in per tile are halved; the even CTA issues all MMAs.
 template <int D, class KV, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
+    attn_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq,
                 const __grid_constant__ CUtensorMap tmo) {
     using C = Cfg<D>;
@@ -748,6 +748,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : nullptr;
         const bool m_vec = valid && (reinterpret_cast<uintptr_t>(mrow) & 15) == 0;
         float m_ref = kNegInf, l = 0.f;
+        // parameters read every tile, held in registers: a kernel-parameter read
+        // that misses the constant cache (shared with this large kernel's
+        // instructions) costs an L2 round trip on the critical path
+        float scale_log2 = a.scale_log2;
+        int n_keys = a.n_keys, mask_bf16 = a.mask_bf16;
+        asm volatile("" : "+f"(scale_log2), "+r"(n_keys), "+r"(mask_bf16));
         int n_done = 0;  // tiles whose P this thread has handed to the MMA issuer
         // Both warps of a row pair run every iteration and every pair barrier, even
         // after a failed wait (they then skip the work), so neither can be left at
@@ -780,10 +786,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else if (code == 1) {
                     // no mask: s stays unscaled; the scale is applied inside the exponent
                     // argument below, and the row maximum is taken on the raw scores
-                    sc = a.scale_log2;
+                    sc = scale_log2;
                 } else {
                     const int c0 = j * BN + h * 64;  // key index of s[0]
-                    if (m_vec && c0 + 64 <= a.n_keys) {
+                    if (m_vec && c0 + 64 <= n_keys) {
 #pragma unroll
                         for (int v = 0; v < 8; ++v) {
                             const uint4 x = *reinterpret_cast<const uint4 *>(mrow + j * BN + v * 8);
@@ -791,16 +797,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const uint16_t mv = (uint16_t)(w[e / 2] >> ((e & 1) * 16));
-                                s[v * 8 + e] = fmaf(s[v * 8 + e], a.scale_log2,
-                                                    mask_to_f32(mv, a.mask_bf16) * kLog2e);
+                                s[v * 8 + e] = fmaf(s[v * 8 + e], scale_log2,
+                                                    mask_to_f32(mv, mask_bf16) * kLog2e);
                             }
                         }
                     } else {
 #pragma unroll
                         for (int c = 0; c < 64; ++c)
-                            s[c] = (c0 + c < a.n_keys)
-                                       ? fmaf(s[c], a.scale_log2,
-                                              mask_to_f32(mrow[j * BN + c], a.mask_bf16) * kLog2e)
+                            s[c] = (c0 + c < n_keys)
+                                       ? fmaf(s[c], scale_log2,
+                                              mask_to_f32(mrow[j * BN + c], mask_bf16) * kLog2e)
                                        : kNegInf;
                     }
                 }
@@ -918,36 +924,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O -> shared memory ([128 rows][32 f32] boxes, 128-byte swizzle) -> TMA store.
             // The ring (or, at head_dim 512, the Q tile) is idle once the last P.V is done.
             uint8_t *stg = smem + (D == 512 ? L::kQ : L::kStages);
-#pragma unroll 1
-            for (int cb = 0; cb < DO / 64; ++cb) {
-                const int box = h * (DO / 64) + cb;
-                uint32_t rr[32];
-                if (have_o) {
-                    tc::tmem_ld32(tm_o + box * 32 + lane_base, rr);
-                    tc::tmem_ld_wait();
-                } else {
+            // each half of the rows' threads stages its DO/64 boxes; a box goes out as
+            // soon as its 128 writers are done, and the issuing thread waits only until
+            // the stores have read shared memory
+            constexpr int NCB = DO / 64;
+            uint32_t rr[NCB][32];
+            if (have_o) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[e] = 0u;
-                }
+                for (int cb = 0; cb < NCB; ++cb) tc::tmem_ld32(tm_o + (h * NCB + cb) * 32 + lane_base, rr[cb]);
+                tc::tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int cb = 0; cb < NCB; ++cb)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[cb][e] = 0u;
+            }
+            const bool issuer = threadIdx.x == h * (kSoftmaxThreads / 2);
+#pragma unroll
+            for (int cb = 0; cb < NCB; ++cb) {
+                const int box = h * NCB + cb;
 #pragma unroll
                 for (int c4 = 0; c4 < 8; ++c4) {
-                    asm volatile("" : "+r"(rr[4 * c4]), "+r"(rr[4 * c4 + 1]), "+r"(rr[4 * c4 + 2]),
-                                 "+r"(rr[4 * c4 + 3]));
+                    asm volatile("" : "+r"(rr[cb][4 * c4]), "+r"(rr[cb][4 * c4 + 1]), "+r"(rr[cb][4 * c4 + 2]),
+                                 "+r"(rr[cb][4 * c4 + 3]));
                     *reinterpret_cast<float4 *>(stg + box * 16384 + r * 128 + ((c4 ^ (r & 7)) << 4)) =
-                        make_float4(__uint_as_float(rr[4 * c4]) * inv, __uint_as_float(rr[4 * c4 + 1]) * inv,
-                                    __uint_as_float(rr[4 * c4 + 2]) * inv,
-                                    __uint_as_float(rr[4 * c4 + 3]) * inv);
+                        make_float4(__uint_as_float(rr[cb][4 * c4]) * inv, __uint_as_float(rr[cb][4 * c4 + 1]) * inv,
+                                    __uint_as_float(rr[cb][4 * c4 + 2]) * inv,
+                                    __uint_as_float(rr[cb][4 * c4 + 3]) * inv);
                 }
-            }
-            tc::fence_async_smem();
-            tc::named_bar(1, kSoftmaxThreads);
-            if (threadIdx.x == 0 && !*abort_flag) {
-#pragma unroll 1
-                for (int box = 0; box < DO / 32; ++box)
+                tc::fence_async_smem();
+                tc::named_bar(6 + h, kSoftmaxThreads / 2);
+                if (issuer && !*abort_flag)
                     tc::tma_store_3d(&tmo, smem_u32(stg + box * 16384), d_off + box * 32,
                                      a.o_rows_dim1 ? q_row0 : q_head0, a.o_rows_dim1 ? q_head0 : q_row0);
+            }
+            if (issuer) {
                 tc::bulk_commit();
-                tc::bulk_wait0();
+                tc::bulk_wait_read0();
             }
         } else if (ok) {
             float *dst;
