@@ -154,7 +154,7 @@ def gqa_timing_enable(enable: bool) -> None:
 
 def gqa_attn_set_cta_pairs(mode: int) -> None:
     """Prefill tiling: 0 never pair query tiles into two-CTA clusters, 1 pair
-    where measured faster (head_dim 512, the default), 2 pair every eligible shape."""
+    where measured faster (head_dim 256 and 512, the default), 2 pair every eligible shape."""
     _check(library().gqa_attn_set_cta_pairs(int(mode)))
 
 

@@ -37,6 +37,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"
@@ -60,11 +62,12 @@ constexpr int kStageBytes = 32768;       // 128 rows x 128 columns of 16-bit, or
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-// key tiles one CTA may visit (the list of visible tiles lives in shared memory)
-constexpr int kMaxListTiles = 256;
+// key tiles one unit may visit (its list of visible tiles lives in shared
+// memory, double-buffered so that the next unit's list is built ahead)
+constexpr int kMaxListTiles = 128;
 // shared memory left for the Q tile and the ring after barriers, the row-max
-// exchange and the tile list (the dynamic shared memory base is 1024-aligned)
-constexpr int kSmemBudget = 232448 - 256 - 2048 - 2 * kMaxListTiles;
+// exchange and the two tile lists (the dynamic shared memory base is 1024-aligned)
+constexpr int kSmemBudget = 232448 - 256 - 2048 - 2 * 2 * kMaxListTiles;
 
 // Per head_dim: KSUB stages per K tile, VSUB per V tile (DO output columns),
 // Q in TMEM only at head_dim 128 (at 256 and 512, O and two S buffers fill
@@ -89,14 +92,15 @@ struct Layout {
     static constexpr int kQ = 0;                     // D/64 tiles of [128][64] (head_dim >= 256)
     static constexpr int kStages = kQ + C::QBYTES;   // STAGES x 32 KiB
     static constexpr int kBars = kStages + C::STAGES * kStageBytes;
-    // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], o_done[2], mma_fin, q_go
-    static constexpr int kNumBars = 2 * C::STAGES + 9;
+    // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], o_done[2], mma_fin,
+    // list_full[2], list_free[2], o_free
+    static constexpr int kNumBars = 2 * C::STAGES + 13;
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 4;
-    static constexpr int kNumVis = kAbort + 4;
+    static constexpr int kNumVis = kAbort + 4;     // visible tiles of the unit in each list buffer
     static constexpr int kXchg = kNumVis + 8;      // row-max exchange: [2 tiles][2 halves][128] f32
-    static constexpr int kList = kXchg + 2 * 2 * BM * 4;  // visible key tiles: uint16 each
-    static constexpr int kEnd = kList + 2 * kMaxListTiles;
+    static constexpr int kList = kXchg + 2 * 2 * BM * 4;  // two lists of visible key tiles (uint16)
+    static constexpr int kEnd = kList + 2 * 2 * kMaxListTiles;
     static constexpr int kBytes = kEnd;
     static_assert(kBytes <= 232448, "shared memory overflow");
 };
@@ -107,15 +111,16 @@ struct AttnArgs {
     int64_t q_row, q_head, q_lane;
     int kv_bf16;
     int k_rows_dim1, v_rows_dim1;  // tensor map is {d, rows, heads} (1) or {d, heads, rows} (0)
-    // prefill tiles of one head and 128 rows move Q (f32) in and O out by TMA
-    int q_tma, o_tma, q_rows_dim1, o_rows_dim1;
+    // prefill tiles of one head and 128 rows move Q (f32) in by TMA
+    int q_tma, q_rows_dim1;
+    int o_tma, o_rows_dim1;  // O out by TMA (prefill tiles of one head and 128 rows, no key split)
     const uint16_t *mask;
     int mask_bf16;
     int64_t m_row, m_head, m_lane;
     float *o;
     int64_t o_row, o_head, o_lane;
     int lanes, rows, n_heads, n_kv_heads, group, n_keys;
-    int rows_per_head, heads_per_tile, row_tiles, head_tiles;
+    int rows_per_head, heads_per_tile, row_tiles, head_tiles, tiles_total;
     int n_blk;  // key tiles of BN
     int splits, blk_per_split, d_parts;
     float scale_log2;
@@ -283,11 +288,58 @@ __device__ __forceinline__ uint32_t sw128(int r, int c16) {
 }
 
 
-// PAIR: the two CTAs of a cluster process two query tiles (two heads of one
-// KV group, same rows, same visible key tiles) with one 256-row MMA per step
-// (cta_group::2).  Each CTA loads only half of every K tile (64 of its keys)
-// and half of every V tile (half of the output columns), so the K/V bytes an
-// SM takes in per tile are halved; the even CTA issues all MMAs.
+// One unit of work: a query tile (one head's 128 rows for prefill, a KV group's
+// heads for verify), one output half (head_dim 512) and one key split.
+struct Unit {
+    Tile t;
+    int tile_id, dpart, split, cg, jb, je, d_off, head_idx, q_head0, q_row0;
+};
+
+// Unit u of the heavy-first order (row tiles from the last, which see the most
+// keys under a causal mask).  PAIR: u counts pairs of head tiles 2p, 2p + 1 of
+// one (lane, KV head, row tile); `rank` picks this CTA's tile of the pair.
+__device__ __forceinline__ Unit unit_of(const AttnArgs &a, int u, bool pair, uint32_t rank, int d_out) {
+    Unit n;
+    n.split = u % a.splits;
+    u /= a.splits;
+    n.dpart = u % a.d_parts;
+    u /= a.d_parts;
+    const int hts = pair ? a.head_tiles / 2 : a.head_tiles;
+    const int per_rt = a.lanes * a.n_kv_heads * hts;
+    const int pidx = (a.row_tiles - 1 - u / per_rt) * per_rt + u % per_rt;
+    n.tile_id = pair ? (pidx / hts) * a.head_tiles + (pidx % hts) * 2 + (int)rank : pidx;
+    n.t = tile_of(a, n.tile_id);
+    n.cg = code_group(a, n.t);
+    n.d_off = n.dpart * d_out;
+    n.jb = n.split * a.blk_per_split;
+    n.je = min(a.n_blk, n.jb + a.blk_per_split);
+    n.head_idx = n.t.lane * a.n_kv_heads + n.t.kh;
+    n.q_head0 = n.t.kh * a.group + n.t.ht * a.heads_per_tile;
+    n.q_row0 = n.t.rt * a.rows_per_head;
+    return n;
+}
+
+// The k-th unit of work slot `slot` of `slots` (a slot is a CTA, or a CTA pair):
+// slots take the heavy-first units in snake order (0..S-1, then S-1..0, ...), so
+// that each slot's total work is close to the mean; -1 when the slot is done.
+__device__ __forceinline__ int slot_unit(int k, int slot, int slots, int units) {
+    const int u = k * slots + ((k & 1) ? slots - 1 - slot : slot);
+    return u < units ? u : -1;
+}
+
+// Persistent tcgen05 attention: each CTA (or CTA pair) owns a TMEM allocation,
+// its barriers and its ring for the whole launch and runs the units of its slot
+// back to back.  The producer builds the next unit's tile list and prefetches
+// its Q and K/V while the current unit finishes; the softmax warps convert the
+// next unit's Q before writing the current unit's O, so that the next unit's
+// first Q.K^T products overlap that epilogue.  Ring positions and the phases of
+// the S / P / O barriers continue across units.
+//
+// PAIR: the two CTAs of a cluster process two query tiles (two heads of one KV
+// group, same rows, same visible key tiles) with one 256-row MMA per step
+// (cta_group::2).  Each CTA loads only half of every K tile (64 of its keys) and
+// half of every V tile (half of the output columns), so the K/V bytes an SM takes
+// in per tile are halved; the even CTA issues all MMAs.
 template <int D, class KV, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmk,
@@ -299,9 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kBf16 = KV::kind == GQA_DTYPE_BF16;
     constexpr int kQStages = D / 64;  // an f32 Q tile crosses the ring 64 columns per stage
     static_assert(!PAIR || D >= 256, "CTA pairs stage Q in shared memory (head_dim >= 256)");
-    // PAIR: one ring stage holds this CTA's 64 keys x 256 columns of K, or its
-    // 128 keys x 128 output columns of V
-    constexpr int KST = PAIR ? D / 256 : KSUB;  // ring stages per K tile
+    // ring stages per K and per V tile (PAIR: one stage holds this CTA's 64 keys x
+    // 256 columns of K, or its 128 keys x 128 output columns of V)
+    constexpr int KST = PAIR ? D / 256 : KSUB;
+    constexpr int VST = PAIR ? 1 : VSUB;
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
@@ -313,13 +366,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto p_full = [&](int b) { return bar(2 * NS + 3 + b); };
     auto o_done = [&](int b) { return bar(2 * NS + 5 + b); };
     const uint32_t mma_fin = bar(2 * NS + 7);
-    // PAIR, odd CTA: released once the even CTA has seen both Q tiles staged (see the producer)
-    const uint32_t q_go = bar(2 * NS + 8);
+    auto list_full = [&](int b) { return bar(2 * NS + 8 + b); };
+    auto list_free = [&](int b) { return bar(2 * NS + 10 + b); };
+    const uint32_t o_free = bar(2 * NS + 12);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlot);
-    int *n_vis_smem = reinterpret_cast<int *>(smem + L::kNumVis);
+    volatile int *n_vis_smem = reinterpret_cast<volatile int *>(smem + L::kNumVis);
     float *xchg = reinterpret_cast<float *>(smem + L::kXchg);
-    uint16_t *list = reinterpret_cast<uint16_t *>(smem + L::kList);
+    uint16_t *lists = reinterpret_cast<uint16_t *>(smem + L::kList);
     const Waiter wt{abort_flag, a.status, kWaitLimitNs};
     // the swizzled layouts below assume a 1024-byte aligned shared-memory base
     if (sbase & 1023u) {
@@ -327,60 +381,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
-    // ---- which unit: (query tile, output half, key split); heavy row tiles first.
-    // A pair takes head tiles 2p and 2p + 1 of the same (lane, KV head, row tile).
     const uint32_t rank = PAIR ? (blockIdx.x & 1u) : 0u;
-    int idx = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int split = idx % a.splits;
-    idx /= a.splits;
-    const int dpart = idx % a.d_parts;
-    idx /= a.d_parts;
-    const int hts = PAIR ? a.head_tiles / 2 : a.head_tiles;
-    const int per_rt = a.lanes * a.n_kv_heads * hts;
-    const int pidx = (a.row_tiles - 1 - idx / per_rt) * per_rt + idx % per_rt;
-    const int tile_id = PAIR ? (pidx / hts) * a.head_tiles + (pidx % hts) * 2 + (int)rank : pidx;
-    const Tile t = tile_of(a, tile_id);
-    const int cg = code_group(a, t);
-    const int jb = split * a.blk_per_split;
-    const int je = min(a.n_blk, jb + a.blk_per_split);
-    const int d_off = dpart * DO;
-    const int head_idx = t.lane * a.n_kv_heads + t.kh;
-    const int q_head0 = t.kh * a.group + t.ht * a.heads_per_tile;  // TMA paths: one head
-    const int q_row0 = t.rt * a.rows_per_head;
+    const int slot = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int slots = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const int units = a.tiles_total * a.d_parts * a.splits / (PAIR ? 2 : 1);
+    // ring positions taken by one unit's loads: Q (f32, by TMA) and K, V of every visible tile
+    const int q_pos = a.q_tma ? kQStages : 0;
+    auto unit_positions = [&](int nv) { return q_pos + nv * (KST + VST); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        // PAIR: a stage is free again only once both CTAs are done with it (each
+        // CTA's softmax releases its Q stages in both CTAs; the MMA releases K/V
+        // stages with two commits), so that the odd CTA's loads, which complete on
+        // the even CTA's full barrier, never land in a phase of the even CTA's own
+        // Q load
         for (int s = 0; s < NS; ++s) {
             tc::mbar_init(full(s), 1);
-            tc::mbar_init(empty(s), 1);
+            tc::mbar_init(empty(s), PAIR ? 2 : 1);
         }
         // PAIR: one arrival per softmax warp of both CTAs, on the even CTA's barrier
         tc::mbar_init(q_full, PAIR ? 2 * kSoftmaxWarps : kSoftmaxThreads);
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(s_full(b), 1);
-            // PAIR: one local arrival per softmax warp; the even CTA's barrier also
-            // takes the odd CTA's relayed arrival
+            // one arrival per softmax warp; the even CTA's barrier also takes the odd
+            // CTA's relayed arrival
             tc::mbar_init(p_full(b), PAIR ? kSoftmaxWarps + (rank == 0 ? 1 : 0) : kSoftmaxThreads);
             tc::mbar_init(o_done(b), 1);
+            tc::mbar_init(list_full(b), 1);
+            // softmax warps + the MMA issuer (even CTA) or the relay (odd CTA)
+            tc::mbar_init(list_free(b), kSoftmaxWarps + 1);
         }
         tc::mbar_init(mma_fin, 1);
-        tc::mbar_init(q_go, 1);
+        tc::mbar_init(o_free, kSoftmaxWarps + ((PAIR && rank == 0) ? 1 : 0));
         *abort_flag = 0;
         tc::fence_mbar_init();
-    }
-    if (warp == kProducerWarp) {
-        // visible key tiles of this unit in order: (j - jb) | 0x8000 when the mask applies
-        int n = 0;
-        for (int base = jb; base < je; base += 32) {
-            const int j = base + lane;
-            const int code = j < je ? tile_code(a, cg, j) : 0;
-            const unsigned vis = __ballot_sync(0xffffffffu, code != 0);
-            if (code)
-                list[n + __popc(vis & ((1u << lane) - 1u))] =
-                    (uint16_t)((j - jb) | (code == 2 ? 0x8000 : 0));
-            n += __popc(vis);
-        }
-        if (lane == 0) *n_vis_smem = n;
     }
     if (warp == kMmaWarp) {
         if constexpr (PAIR) {
@@ -401,8 +436,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tm_o = tmem;             // O: DO columns
     const uint32_t tm_s = tmem + C::kColS;  // S: two buffers of BN columns (P over S)
     const uint32_t tm_q = tmem + C::kColQ;  // Q: D/2 columns (head_dim 128)
-    const int n_vis = *n_vis_smem;
-    auto tile_at = [&](int v) { return jb + (list[v] & 0x7fff); };
 
     // Register split per warpgroup (every warp of a warpgroup executes its
     // setmaxnreg): warps 8-11 (producer, MMA issuer, two idle) lower theirs, the
@@ -414,6 +447,122 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 tc::prefetch_tmap(&tmk);
                 tc::prefetch_tmap(&tmv);
+                if (a.q_tma) tc::prefetch_tmap(&tmq);
+            }
+            int stage = 0;
+            uint32_t round = 0;
+            auto next = [&]() {
+                if (++stage == NS) {
+                    stage = 0;
+                    ++round;
+                }
+            };
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int uid = slot_unit(k, slot, slots, units);
+                if (uid < 0) break;
+                const Unit un = unit_of(a, uid, PAIR, rank, DO);
+                const int b = k & 1;
+                uint16_t *list = lists + b * kMaxListTiles;
+                // the list buffer of unit k - 2 must have been read by every role
+                if (k >= 2) ok = __all_sync(0xffffffffu, wt.wait(list_free(b), ((k - 2) >> 1) & 1));
+                if (!ok) break;
+                // visible key tiles in order: (j - jb) | 0x8000 when the mask applies
+                int n = 0;
+                for (int base = un.jb; base < un.je; base += 32) {
+                    const int j = base + lane;
+                    const int code = j < un.je ? tile_code(a, un.cg, j) : 0;
+                    const unsigned vis = __ballot_sync(0xffffffffu, code != 0);
+                    if (code)
+                        list[n + __popc(vis & ((1u << lane) - 1u))] =
+                            (uint16_t)((j - un.jb) | (code == 2 ? 0x8000 : 0));
+                    n += __popc(vis);
+                }
+                if (lane == 0) n_vis_smem[b] = n;
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(list_full(b));
+                auto tile_at = [&](int v) { return un.jb + (list[v] & 0x7fff); };
+                if (lane == 0) {
+                    // f32 Q tile first (consumed by the softmax warps): [128 rows][32 f32]
+                    // boxes, completing on this CTA's own barrier
+                    for (int qs = 0; qs < (n > 0 ? q_pos : 0) && ok; ++qs) {
+                        if (!(ok = wt.wait(empty(stage), (round & 1) ^ 1))) break;
+                        const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
+                        tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
+#pragma unroll
+                        for (int bx = 0; bx < 2; ++bx)
+                            tc::tma_load_3d(dst + bx * 16384, &tmq, full(stage), qs * 64 + bx * 32,
+                                            a.q_rows_dim1 ? un.q_row0 : un.q_head0,
+                                            a.q_rows_dim1 ? un.q_head0 : un.q_row0);
+                        next();
+                    }
+                    // one stage of K or V: two boxes of [BN rows][64 columns] from column d0
+                    auto load = [&](int j, bool is_v, int d0) -> bool {
+                        if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
+                        const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
+                        tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
+                        const int rows_dim1 = is_v ? a.v_rows_dim1 : a.k_rows_dim1;
+                        const int c1 = rows_dim1 ? j * BN : un.head_idx;
+                        const int c2 = rows_dim1 ? un.head_idx : j * BN;
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            tc::tma_load_3d(dst + c * (BN * 128), is_v ? (const void *)&tmv : (const void *)&tmk,
+                                            full(stage), d0 + c * 64, c1, c2);
+                        next();
+                        return true;
+                    };
+                    // PAIR: one stage of this CTA's half of a tile, counted on the even CTA's
+                    // full barrier (which expects both halves): K = keys [64 rank, +64) of
+                    // the tile, columns [d0, d0 + 256); V = all 128 keys, output columns
+                    // [d_off + 128 rank, +128)
+                    auto load_half = [&](int j, bool is_v, int d0) -> bool {
+                        if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
+                        const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
+                        if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), 2 * kStageBytes);
+                        const uint32_t fb = tc::mapa_shared(full(stage), 0);
+                        if (is_v) {
+                            const int c1 = a.v_rows_dim1 ? j * BN : un.head_idx;
+                            const int c2 = a.v_rows_dim1 ? un.head_idx : j * BN;
+#pragma unroll
+                            for (int c = 0; c < 2; ++c)
+                                tc::tma_load_3d_pair(dst + c * (BN * 128), &tmv, fb,
+                                                     un.d_off + (int)rank * 128 + c * 64, c1, c2);
+                        } else {
+                            const int kr = j * BN + (int)rank * (BN / 2);
+                            const int c1 = a.k_rows_dim1 ? kr : un.head_idx;
+                            const int c2 = a.k_rows_dim1 ? un.head_idx : kr;
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                tc::tma_load_3d_pair(dst + c * (BN / 2 * 128), &tmk, fb, d0 + c * 64, c1, c2);
+                        }
+                        next();
+                        return true;
+                    };
+                    // the MMA issuer consumes K of tile v+1 before V of tile v: K0, K1, V0, K2, V1, ...
+                    if constexpr (PAIR) {
+                        for (int ks = 0; ks < KST && ok && n > 0; ++ks) ok = load_half(tile_at(0), false, ks * 256);
+                        for (int v = 0; ok && v < n; ++v) {
+                            for (int ks = 0; ks < KST && ok && v + 1 < n; ++ks)
+                                ok = load_half(tile_at(v + 1), false, ks * 256);
+                            if (ok) ok = load_half(tile_at(v), true, 0);
+                        }
+                    } else {
+                        for (int ks = 0; ks < KSUB && ok && n > 0; ++ks) ok = load(tile_at(0), false, ks * 128);
+                        for (int v = 0; ok && v < n; ++v) {
+                            for (int ks = 0; ks < KSUB && ok && v + 1 < n; ++ks)
+                                ok = load(tile_at(v + 1), false, ks * 128);
+                            for (int vs = 0; vs < VSUB && ok; ++vs) ok = load(tile_at(v), true, un.d_off + vs * 128);
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+            }
+        } else if (warp == kMmaWarp) {
+            // ------------------------------------------------------------ MMA issuer
+            // (PAIR: the even CTA issues for both; the odd CTA's MMA warp relays)
+            if (lane == 0 && rank == 0) {
+                const uint32_t idesc_qk = tc::idesc_f16(PAIR ? 2 * BM : BM, BN, kBf16, false);
+                const uint32_t idesc_pv = tc::idesc_f16(PAIR ? 2 * BM : BM, PAIR ? DO : 128, kBf16, true);
                 int stage = 0;
                 uint32_t round = 0;
                 auto next = [&]() {
@@ -422,205 +571,116 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++round;
                     }
                 };
-                bool ok = true;
-                // f32 Q tile first (consumed by the softmax warps): [128 rows][32 f32] boxes
-                if (a.q_tma) {
-                    tc::prefetch_tmap(&tmq);
-                    for (int qs = 0; qs < kQStages && ok; ++qs) {
-                        if (!(ok = wt.wait(empty(stage), (round & 1) ^ 1))) break;
-                        const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
-                        tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
-#pragma unroll
-                        for (int b = 0; b < 2; ++b)
-                            tc::tma_load_3d(dst + b * 16384, &tmq, full(stage), qs * 64 + b * 32,
-                                            a.q_rows_dim1 ? q_row0 : q_head0,
-                                            a.q_rows_dim1 ? q_head0 : q_row0);
-                        next();
-                    }
-                }
-                // one stage: two boxes of [BN rows][64 columns] of K or V starting at column d0
-                auto load = [&](int j, bool is_v, int d0) -> bool {
-                    if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
-                    const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
-                    tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
-                    const int rows_dim1 = is_v ? a.v_rows_dim1 : a.k_rows_dim1;
-                    const int c1 = rows_dim1 ? j * BN : head_idx;
-                    const int c2 = rows_dim1 ? head_idx : j * BN;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        tc::tma_load_3d(dst + c * (BN * 128), is_v ? (const void *)&tmv : (const void *)&tmk,
-                                        full(stage), d0 + c * 64, c1, c2);
-                    next();
-                    return true;
-                };
-                // PAIR: one stage of this CTA's half of a tile, counted on the even CTA's
-                // full barrier (which expects both halves): K = keys [64 rank, +64) of the
-                // tile, columns [d0, d0 + 256); V = all 128 keys, output columns
-                // [d_off + 128 rank, +128).
-                // A K/V load of the odd CTA completes on the even CTA's full barrier.  When
-                // its ring slot last held this CTA's Q stage, the even CTA's barrier may
-                // still be in the phase of its own Q load; the odd CTA therefore waits,
-                // before its first such load, until the even CTA has seen both Q tiles
-                // staged (which implies its Q phases completed).
-                int pos = a.q_tma ? kQStages : 0;  // ring loads issued so far
-                bool gated = false;
-                auto load_half = [&](int j, bool is_v, int d0) -> bool {
-                    if (rank == 1 && !gated && pos >= NS) {
-                        if (!wt.template wait<true>(q_go, 0)) return false;
-                        gated = true;
-                    }
-                    ++pos;
-                    if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
-                    const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
-                    if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), 2 * kStageBytes);
-                    const uint32_t fb = tc::mapa_shared(full(stage), 0);
-                    if (is_v) {
-                        const int c1 = a.v_rows_dim1 ? j * BN : head_idx;
-                        const int c2 = a.v_rows_dim1 ? head_idx : j * BN;
-#pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            tc::tma_load_3d_pair(dst + c * (BN * 128), &tmv, fb,
-                                                 d_off + (int)rank * 128 + c * 64, c1, c2);
-                    } else {
-                        const int kr = j * BN + (int)rank * (BN / 2);
-                        const int c1 = a.k_rows_dim1 ? kr : head_idx;
-                        const int c2 = a.k_rows_dim1 ? head_idx : kr;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            tc::tma_load_3d_pair(dst + c * (BN / 2 * 128), &tmk, fb, d0 + c * 64, c1, c2);
-                    }
-                    next();
-                    return true;
-                };
-                // the MMA issuer consumes K of tile v+1 before V of tile v: K0, K1, V0, K2, V1, ...
-                if constexpr (PAIR) {
-                    for (int ks = 0; ks < KST && ok && n_vis > 0; ++ks) ok = load_half(tile_at(0), false, ks * 256);
-                    for (int v = 0; ok && v < n_vis; ++v) {
-                        for (int ks = 0; ks < KST && ok && v + 1 < n_vis; ++ks)
-                            ok = load_half(tile_at(v + 1), false, ks * 256);
-                        if (ok) ok = load_half(tile_at(v), true, 0);
-                    }
-                } else {
-                    for (int ks = 0; ks < KSUB && ok && n_vis > 0; ++ks) ok = load(tile_at(0), false, ks * 128);
-                    for (int v = 0; ok && v < n_vis; ++v) {
-                        for (int ks = 0; ks < KSUB && ok && v + 1 < n_vis; ++ks)
-                            ok = load(tile_at(v + 1), false, ks * 128);
-                        for (int vs = 0; vs < VSUB && ok; ++vs) ok = load(tile_at(v), true, d_off + vs * 128);
-                    }
-                }
-            }
-        } else if (warp == kMmaWarp) {
-            // ------------------------------------------------------------ MMA issuer
-            // (PAIR: the even CTA issues for both; the odd CTA's MMA warp only
-            // takes part in the TMEM allocation)
-            if (lane == 0 && rank == 0) {
-                const uint32_t idesc_qk = tc::idesc_f16(PAIR ? 2 * BM : BM, BN, kBf16, false);
-                const uint32_t idesc_pv = tc::idesc_f16(PAIR ? 2 * BM : BM, PAIR ? DO : 128, kBf16, true);
-                int stage = a.q_tma ? kQStages % NS : 0;
-                uint32_t round = a.q_tma ? kQStages / NS : 0;
-                auto next = [&]() {
-                    if (++stage == NS) {
-                        stage = 0;
-                        ++round;
-                    }
-                };
-                // S(v) = Q K^T into buffer v & 1
-                auto issue_s_pair = [&](int v) -> bool {
-                    const uint32_t d_tm = tm_s + (uint32_t)(v & 1) * BN;
+                // S(g) = Q K^T into buffer g & 1
+                auto issue_s = [&](int g) -> bool {
+                    const uint32_t d_tm = tm_s + (uint32_t)(g & 1) * BN;
                     for (int ks = 0; ks < KST; ++ks) {
-                        if (!wt.template wait<true>(full(stage), round & 1)) return false;
+                        if (!wt.template wait<PAIR>(full(stage), round & 1)) return false;
                         tc::tc_fence_after();
                         const uint32_t kb = sbase + L::kStages + stage * kStageBytes;
+                        if constexpr (PAIR) {
 #pragma unroll
-                        for (int kk = 0; kk < 16; ++kk) {
-                            const int dq = ks * 256 + kk * 16;
-                            const uint64_t db = tc::smem_desc_sw128(
-                                kb + (kk / 4) * (BN / 2 * 128) + (kk % 4) * 32, 16, 1024);
-                            const uint64_t da = tc::smem_desc_sw128(
-                                sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16, 1024);
-                            tc::mma_f16_ss_pair(d_tm, da, db, idesc_qk, (ks | kk) != 0);
-                        }
-                        tc::mma_commit_pair(empty(stage));
-                        next();
-                    }
-                    tc::mma_commit_pair(s_full(v & 1));
-                    return true;
-                };
-                auto issue_s = [&](int v) -> bool {
-                    if constexpr (PAIR) return issue_s_pair(v);
-                    const uint32_t d_tm = tm_s + (uint32_t)(v & 1) * BN;
-                    for (int ks = 0; ks < KSUB; ++ks) {
-                        if (!wt.wait(full(stage), round & 1)) return false;
-                        tc::tc_fence_after();
-                        const uint32_t kb = sbase + L::kStages + stage * kStageBytes;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const int dq = ks * 128 + kk * 16;
-                            const uint64_t db =
-                                tc::smem_desc_sw128(kb + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
-                            if constexpr (C::QTM) {
-                                tc::mma_f16_ts(d_tm, tm_q + dq / 2, db, idesc_qk, (ks | kk) != 0);
-                            } else {
+                            for (int kk = 0; kk < 16; ++kk) {
+                                const int dq = ks * 256 + kk * 16;
+                                const uint64_t db = tc::smem_desc_sw128(
+                                    kb + (kk / 4) * (BN / 2 * 128) + (kk % 4) * 32, 16, 1024);
                                 const uint64_t da = tc::smem_desc_sw128(
-                                    sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16,
-                                    1024);
-                                tc::mma_f16_ss(d_tm, da, db, idesc_qk, (ks | kk) != 0);
+                                    sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16, 1024);
+                                tc::mma_f16_ss_pair(d_tm, da, db, idesc_qk, (ks | kk) != 0);
                             }
+                            // two arrivals: see the empty barriers' count
+                            tc::mma_commit_pair(empty(stage));
+                            tc::mma_commit_pair(empty(stage));
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const int dq = ks * 128 + kk * 16;
+                                const uint64_t db =
+                                    tc::smem_desc_sw128(kb + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
+                                if constexpr (C::QTM) {
+                                    tc::mma_f16_ts(d_tm, tm_q + dq / 2, db, idesc_qk, (ks | kk) != 0);
+                                } else {
+                                    const uint64_t da = tc::smem_desc_sw128(
+                                        sbase + L::kQ + (dq / 64) * (BM * 128) + ((dq % 64) / 16) * 32, 16,
+                                        1024);
+                                    tc::mma_f16_ss(d_tm, da, db, idesc_qk, (ks | kk) != 0);
+                                }
+                            }
+                            tc::mma_commit(empty(stage));
                         }
-                        tc::mma_commit(empty(stage));
                         next();
                     }
-                    tc::mma_commit(s_full(v & 1));
+                    if constexpr (PAIR)
+                        tc::mma_commit_pair(s_full(g & 1));
+                    else
+                        tc::mma_commit(s_full(g & 1));
                     return true;
                 };
-                bool ok = wt.template wait<PAIR>(q_full, 0);
-                tc::tc_fence_after();
-                if constexpr (PAIR) {
-                    if (ok) tc::mbar_arrive_cluster(tc::mapa_shared(q_go, 1));
-                }
-                if (ok && n_vis > 0) ok = issue_s(0);
-                for (int i = 0; ok && i < n_vis; ++i) {
-                    if (i + 1 < n_vis && !(ok = issue_s(i + 1))) break;
-                    if (!(ok = wt.template wait<PAIR>(p_full(i & 1), (i >> 1) & 1))) break;
+                bool ok = true;
+                int g = 0;        // global index of the unit's first tile
+                int with_o = 0;   // units so far that produced O (one o_free phase each)
+                for (int k = 0; ok; ++k) {
+                    if (slot_unit(k, slot, slots, units) < 0) break;
+                    const int b = k & 1;
+                    if (!(ok = wt.wait(list_full(b), (k >> 1) & 1))) break;
+                    const int n = n_vis_smem[b];
+                    tc::mbar_arrive(list_free(b));
+                    if (n == 0) continue;  // no visible key: no loads, no Q, no O
+                    for (int q = 0; q < q_pos; ++q) next();  // the Q stages are the softmax's
+                    if (!(ok = wt.template wait<PAIR>(q_full, (with_o & 1)))) break;
                     tc::tc_fence_after();
-                    if constexpr (PAIR) {
-                        // one stage: this CTA's and the peer's halves of V(i), N = DO
-                        if (!(ok = wt.template wait<true>(full(stage), round & 1))) break;
+                    ok = issue_s(g);
+                    for (int i = 0; ok && i < n; ++i) {
+                        const int gi = g + i;
+                        if (i + 1 < n && !(ok = issue_s(gi + 1))) break;
+                        if (!(ok = wt.template wait<PAIR>(p_full(gi & 1), (gi >> 1) & 1))) break;
+                        // the first P.V of a unit overwrites O: the previous unit's O must
+                        // have been read out of TMEM
+                        if (i == 0 && with_o > 0 && !(ok = wt.template wait<PAIR>(o_free, (with_o - 1) & 1)))
+                            break;
                         tc::tc_fence_after();
-                        const uint32_t vb = sbase + L::kStages + stage * kStageBytes;
+                        if constexpr (PAIR) {
+                            // one stage: this CTA's and the peer's halves of V, N = DO
+                            if (!(ok = wt.template wait<true>(full(stage), round & 1))) break;
+                            tc::tc_fence_after();
+                            const uint32_t vb = sbase + L::kStages + stage * kStageBytes;
 #pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk) {
-                            const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
-                            tc::mma_f16_ts_pair(tm_o, tm_s + (uint32_t)(i & 1) * BN + kk * 8, db, idesc_pv,
-                                                (i | kk) != 0);
+                            for (int kk = 0; kk < BN / 16; ++kk) {
+                                const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
+                                tc::mma_f16_ts_pair(tm_o, tm_s + (uint32_t)(gi & 1) * BN + kk * 8, db, idesc_pv,
+                                                    (i | kk) != 0);
+                            }
+                            tc::mma_commit_pair(empty(stage));
+                            tc::mma_commit_pair(empty(stage));
+                            next();
+                            tc::mma_commit_pair(o_done(gi & 1));
+                            continue;
                         }
-                        tc::mma_commit_pair(empty(stage));
-                        next();
-                        tc::mma_commit_pair(o_done(i & 1));
-                        continue;
-                    }
-                    // the VSUB stages of V(i) follow each other in the ring
-                    int st[VSUB];
-#pragma unroll
-                    for (int vs = 0; vs < VSUB; ++vs) {
-                        if (ok) ok = wt.wait(full(stage), round & 1);
-                        st[vs] = stage;
-                        next();
-                    }
-                    if (!ok) break;
-                    tc::tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
+                        // the VSUB stages of V follow each other in the ring
+                        int st[VSUB];
 #pragma unroll
                         for (int vs = 0; vs < VSUB; ++vs) {
-                            const uint32_t vb = sbase + L::kStages + st[vs] * kStageBytes;
-                            const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
-                            tc::mma_f16_ts(tm_o + vs * 128, tm_s + (uint32_t)(i & 1) * BN + kk * 8, db,
-                                           idesc_pv, (i | kk) != 0);
+                            if (ok) ok = wt.wait(full(stage), round & 1);
+                            st[vs] = stage;
+                            next();
                         }
+                        if (!ok) break;
+                        tc::tc_fence_after();
 #pragma unroll
-                    for (int vs = 0; vs < VSUB; ++vs) tc::mma_commit(empty(st[vs]));
-                    tc::mma_commit(o_done(i & 1));
+                        for (int kk = 0; kk < BN / 16; ++kk)
+#pragma unroll
+                            for (int vs = 0; vs < VSUB; ++vs) {
+                                const uint32_t vb = sbase + L::kStages + st[vs] * kStageBytes;
+                                const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
+                                tc::mma_f16_ts(tm_o + vs * 128, tm_s + (uint32_t)(gi & 1) * BN + kk * 8, db,
+                                               idesc_pv, (i | kk) != 0);
+                            }
+#pragma unroll
+                        for (int vs = 0; vs < VSUB; ++vs) tc::mma_commit(empty(st[vs]));
+                        tc::mma_commit(o_done(gi & 1));
+                    }
+                    g += n;
+                    ++with_o;
                 }
                 // every MMA of this thread has finished before TMEM can be released
                 // (this wait ignores the abort flag: only the time limit ends it)
@@ -632,16 +692,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fin.wait(mma_fin, 0);
             }
             if constexpr (PAIR) {
-                // odd CTA: forward each tile's "P written" from this CTA's softmax warps to
-                // the even CTA's barrier with one arrival, so that the softmax warps
-                // themselves only arrive locally.  Every phase is seen in turn: P(i + 2)
-                // needs S(i + 2), which the even CTA issues only after this arrival for P(i).
-                // The P stores were complete (tcgen05.wait::st) before the warps arrived
-                // locally, so the forwarded arrival needs no release.
+                // odd CTA: forward each tile's "P written" and each unit's "O read out"
+                // from this CTA's softmax warps to the even CTA's barriers with one
+                // arrival each, so that the softmax warps only arrive locally.  Every
+                // phase is seen in turn: P(g + 2) needs S(g + 2), which the even CTA
+                // issues only after this arrival for P(g), and a unit's O is read out
+                // only after all its P.V, which follow the previous forward of O.  The
+                // tensor-memory accesses behind each signal are complete
+                // (tcgen05.wait::st / ::ld) before the warps arrive locally, so the
+                // forwarded arrival needs no release.
                 if (lane == 0 && rank == 1) {
-                    for (int i = 0; i < n_vis; ++i) {
-                        if (!wt.template wait<true>(p_full(i & 1), (i >> 1) & 1)) break;
-                        tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(p_full(i & 1), 0));
+                    bool ok = true;
+                    int g = 0, with_o = 0;
+                    for (int k = 0; ok; ++k) {
+                        if (slot_unit(k, slot, slots, units) < 0) break;
+                        const int b = k & 1;
+                        if (!(ok = wt.wait(list_full(b), (k >> 1) & 1))) break;
+                        const int n = n_vis_smem[b];
+                        tc::mbar_arrive(list_free(b));
+                        for (int i = 0; ok && i < n; ++i) {
+                            const int gi = g + i;
+                            if (!(ok = wt.template wait<true>(p_full(gi & 1), (gi >> 1) & 1))) break;
+                            tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(p_full(gi & 1), 0));
+                        }
+                        if (!ok || n == 0) continue;
+                        if (!(ok = wt.template wait<true>(o_free, with_o & 1))) break;
+                        tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(o_free, 0));
+                        g += n;
+                        ++with_o;
                     }
                 }
             }
@@ -655,283 +733,339 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = warp >> 2;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const int pair_bar = 2 + (warp & 3);  // named barrier of warps w and w + 4
-        int head = 0, row = 0;
-        const bool valid = row_of(a, t, r, head, row);
-        bool ok = true;
-
-        // ---- Q: this thread's 32 columns of each 64-column block, as f16/bf16
-        auto put_q = [&](int cb, const uint32_t(&w)[16]) {
-            if constexpr (C::QTM) {
-                tc::tmem_st16(tm_q + cb * 32 + h * 16 + lane_base, w);
-            } else {
-                uint8_t *qs = smem + L::kQ + cb * (BM * 128);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(qs + sw128(r, h * 4 + c)) =
-                        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-            }
-        };
-        if (a.q_tma) {
-            // f32 Q arrives by TMA through the first kQStages ring stages; half h
-            // converts box h (32 columns)
-            int stage = 0;
-            uint32_t round = 0;
-            for (int qs = 0; qs < kQStages; ++qs) {
-                if (ok) ok = wt.wait(full(stage), round & 1);
-                ok = __all_sync(0xffffffffu, ok);
-                if (ok) {
-                    const uint8_t *src = smem + L::kStages + stage * kStageBytes + h * 16384;
-                    uint32_t w[16];
-#pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const float4 x =
-                            *reinterpret_cast<const float4 *>(src + r * 128 + ((c4 ^ (r & 7)) << 4));
-                        w[c4 * 2] = pack2(KV{}, x.x, x.y);
-                        w[c4 * 2 + 1] = pack2(KV{}, x.z, x.w);
-                    }
-                    put_q(qs, w);
-                }
-                tc::named_bar(1, kSoftmaxThreads);  // every softmax thread is done with this stage
-                if (threadIdx.x == 0) tc::mbar_arrive(empty(stage));
-                if (++stage == NS) {
-                    stage = 0;
-                    ++round;
-                }
-            }
-        } else {
-            // each thread reads its half of its own row
-#pragma unroll 1
-            for (int cb = 0; cb < D / 64; ++cb) {
-                uint32_t w[16];
-                if (valid && a.q_f32) {
-                    const float *src = static_cast<const float *>(a.q) + t.lane * a.q_lane +
-                                       (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64 + h * 32;
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const float4 x = ld_nc_f4(src + v * 4);
-                        w[2 * v] = pack2(KV{}, x.x, x.y);
-                        w[2 * v + 1] = pack2(KV{}, x.z, x.w);
-                    }
-                } else if (valid) {
-                    const uint16_t *src = static_cast<const uint16_t *>(a.q) + t.lane * a.q_lane +
-                                          (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64 + h * 32;
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const uint4 x = ld_nc_v4(src + v * 8);
-                        w[4 * v] = x.x;
-                        w[4 * v + 1] = x.y;
-                        w[4 * v + 2] = x.z;
-                        w[4 * v + 3] = x.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int v = 0; v < 16; ++v) w[v] = 0u;
-                }
-                put_q(cb, w);
-            }
-        }
-        if constexpr (C::QTM)
-            tc::tmem_st_wait();
-        else
-            tc::fence_async_smem();
-        tc::tc_fence_before();
-        if constexpr (PAIR) {
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(q_full, 0));
-        } else {
-            tc::mbar_arrive(q_full);
-        }
-
-        // ---- key tiles: this thread owns columns [h*64, h*64 + 64) of every tile
-        const uint16_t *mrow = valid ? a.mask + t.lane * a.m_lane + (int64_t)head * a.m_head +
-                                           (int64_t)row * a.m_row + h * 64
-                                     : nullptr;
-        const bool m_vec = valid && (reinterpret_cast<uintptr_t>(mrow) & 15) == 0;
-        float m_ref = kNegInf, l = 0.f;
         // parameters read every tile, held in registers: a kernel-parameter read
         // that misses the constant cache (shared with this large kernel's
         // instructions) costs an L2 round trip on the critical path
         float scale_log2 = a.scale_log2;
         int n_keys = a.n_keys, mask_bf16 = a.mask_bf16;
         asm volatile("" : "+f"(scale_log2), "+r"(n_keys), "+r"(mask_bf16));
-        int n_done = 0;  // tiles whose P this thread has handed to the MMA issuer
-        // Both warps of a row pair run every iteration and every pair barrier, even
-        // after a failed wait (they then skip the work), so neither can be left at
-        // a barrier its partner never reaches.
-        for (int i = 0; i < n_vis; ++i) {
-            const int j = tile_at(i);
-            const int code = (list[i] & 0x8000) ? 2 : 1;
-            if (ok) ok = __all_sync(0xffffffffu, wt.wait(s_full(i & 1), (i >> 1) & 1));
-            float s[64];
-            float mx = kNegInf;
-            float sc = 1.f;  // factor still to apply to s (log2 domain)
-            if (ok) {
-                tc::tc_fence_after();
-                {
-                    uint32_t rr[64];
-                    tc::tmem_ld32(tm_s + (uint32_t)(i & 1) * BN + h * 64 + lane_base,
-                                  *reinterpret_cast<uint32_t(*)[32]>(rr));
-                    tc::tmem_ld32(tm_s + (uint32_t)(i & 1) * BN + h * 64 + 32 + lane_base,
-                                  *reinterpret_cast<uint32_t(*)[32]>(rr + 32));
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        asm volatile("" : "+r"(rr[c]));  // keep every use after the wait
-                        s[c] = __uint_as_float(rr[c]);
-                    }
-                }
-                if (!valid) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) s[c] = kNegInf;
-                } else if (code == 1) {
-                    // no mask: s stays unscaled; the scale is applied inside the exponent
-                    // argument below, and the row maximum is taken on the raw scores
-                    sc = scale_log2;
+        bool ok = true;
+        // PAIR, odd CTA: this CTA's full barriers complete a phase only for its own Q
+        // loads (its K/V loads complete on the even CTA's barriers), so the parity of
+        // its Q waits is the count of earlier Q uses of the slot, kept per slot here
+        uint32_t q_uses = 0;
+
+        // ---- release a ring slot this CTA's softmax is done with (PAIR: in both CTAs)
+        auto release_slot = [&](int stage) {
+            tc::mbar_arrive(empty(stage));
+            // PAIR: the other CTA's producer reloads this slot only once both CTAs'
+            // Q stages in it are consumed
+            if constexpr (PAIR) tc::mbar_arrive_cluster_relaxed(tc::mapa_shared(empty(stage), rank ^ 1));
+        };
+        // ---- Q of unit `un` (ring positions from qpos when it arrives by TMA): this
+        // thread's 32 columns of each 64-column block, as f16/bf16.  With `hold`, the
+        // f32 stages are kept (not released) to stage the previous unit's O.
+        auto convert_q = [&](const Unit &un, int qpos, bool hold) {
+            int head = 0, row = 0;
+            const bool valid = row_of(a, un.t, r, head, row);
+            auto put_q = [&](int cb, const uint32_t(&w)[16]) {
+                if constexpr (C::QTM) {
+                    tc::tmem_st16(tm_q + cb * 32 + h * 16 + lane_base, w);
                 } else {
-                    const int c0 = j * BN + h * 64;  // key index of s[0]
-                    if (m_vec && c0 + 64 <= n_keys) {
+                    uint8_t *qs = smem + L::kQ + cb * (BM * 128);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(qs + sw128(r, h * 4 + c)) =
+                            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                }
+            };
+            if (a.q_tma) {
+                // f32 Q arrives by TMA through kQStages ring stages; half h converts box h
+                for (int qs = 0; qs < kQStages; ++qs) {
+                    const int stage = (qpos + qs) % NS;
+                    const uint32_t round = (uint32_t)((qpos + qs) / NS);
+                    const uint32_t parity = (PAIR && rank == 1) ? (q_uses >> stage) & 1u : round & 1u;
+                    q_uses ^= 1u << stage;
+                    if (ok) ok = wt.wait(full(stage), parity);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (ok) {
+                        const uint8_t *src = smem + L::kStages + stage * kStageBytes + h * 16384;
+                        uint32_t w[16];
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4) {
+                            const float4 x =
+                                *reinterpret_cast<const float4 *>(src + r * 128 + ((c4 ^ (r & 7)) << 4));
+                            w[c4 * 2] = pack2(KV{}, x.x, x.y);
+                            w[c4 * 2 + 1] = pack2(KV{}, x.z, x.w);
+                        }
+                        put_q(qs, w);
+                    }
+                    tc::named_bar(1, kSoftmaxThreads);  // every softmax thread is done with this stage
+                    if (threadIdx.x == 0 && !hold) release_slot(stage);
+                }
+            } else {
+                // each thread reads its half of its own row
+#pragma unroll 1
+                for (int cb = 0; cb < D / 64; ++cb) {
+                    uint32_t w[16];
+                    if (valid && a.q_f32) {
+                        const float *src = static_cast<const float *>(a.q) + un.t.lane * a.q_lane +
+                                           (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64 + h * 32;
 #pragma unroll
                         for (int v = 0; v < 8; ++v) {
-                            const uint4 x = *reinterpret_cast<const uint4 *>(mrow + j * BN + v * 8);
-                            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+                            const float4 x = ld_nc_f4(src + v * 4);
+                            w[2 * v] = pack2(KV{}, x.x, x.y);
+                            w[2 * v + 1] = pack2(KV{}, x.z, x.w);
+                        }
+                    } else if (valid) {
+                        const uint16_t *src = static_cast<const uint16_t *>(a.q) + un.t.lane * a.q_lane +
+                                              (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64 +
+                                              h * 32;
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const uint16_t mv = (uint16_t)(w[e / 2] >> ((e & 1) * 16));
-                                s[v * 8 + e] = fmaf(s[v * 8 + e], scale_log2,
-                                                    mask_to_f32(mv, mask_bf16) * kLog2e);
-                            }
+                        for (int v = 0; v < 4; ++v) {
+                            const uint4 x = ld_nc_v4(src + v * 8);
+                            w[4 * v] = x.x;
+                            w[4 * v + 1] = x.y;
+                            w[4 * v + 2] = x.z;
+                            w[4 * v + 3] = x.w;
                         }
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            s[c] = (c0 + c < n_keys)
-                                       ? fmaf(s[c], scale_log2,
-                                              mask_to_f32(mrow[j * BN + c], mask_bf16) * kLog2e)
-                                       : kNegInf;
+                        for (int v = 0; v < 16; ++v) w[v] = 0u;
                     }
-                }
-                // row max of sc * s over this half (four chains of three-input max; with
-                // a negative scale the maximum comes from the smallest raw score)
-                float mq[4] = {s[0], s[1], s[2], s[3]};
-                if (sc >= 0.f) {
-#pragma unroll
-                    for (int c = 4; c < 60; c += 8)
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) mq[k] = fmax3(mq[k], s[c + k], s[c + 4 + k]);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) mq[k] = fmaxf(mq[k], s[60 + k]);
-                    mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
-                } else {
-#pragma unroll
-                    for (int c = 4; c < 60; c += 8)
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) mq[k] = fmin3(mq[k], s[c + k], s[c + 4 + k]);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) mq[k] = fminf(mq[k], s[60 + k]);
-                    mx = fmin3(mq[0], mq[1], fminf(mq[2], mq[3]));
-                }
-                mx *= sc;
-            }
-            // agree with the other half of the row on the maximum
-            float *xs = xchg + (i & 1) * 2 * BM;
-            xs[h * BM + r] = mx;
-            tc::named_bar(pair_bar, 64);
-            mx = fmaxf(mx, xs[(1 - h) * BM + r]);
-            if (!ok) continue;
-            float factor = 1.f;
-            bool resc = false;
-            if (m_ref == kNegInf) {
-                m_ref = mx;
-            } else if (mx > m_ref + kRescaleThreshold) {
-                factor = ex2(m_ref - mx);
-                m_ref = mx;
-                resc = true;
-            }
-            const float nmu = m_ref == kNegInf ? 0.f : -m_ref;
-            uint32_t pk[32];
-            float ra0 = 0.f, ra1 = 0.f, rb0 = 0.f, rb1 = 0.f;
-#pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-                // p = 2^(sc * s - mu): one packed FMA per two arguments
-                float x0, x1, x2, x3;
-                ffma2(x0, x1, s[c], s[c + 1], sc, sc, nmu, nmu);
-                ffma2(x2, x3, s[c + 2], s[c + 3], sc, sc, nmu, nmu);
-                const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-                fadd2(ra0, ra1, ra0, ra1, p0, p1);
-                fadd2(rb0, rb1, rb0, rb1, p2, p3);
-                pk[c / 2] = pack2(KV{}, p0, p1);
-                pk[c / 2 + 1] = pack2(KV{}, p2, p3);
-            }
-            l = l * factor + ((ra0 + ra1) + (rb0 + rb1));
-            // P.V of the previous tile must be done before O is rescaled.  P goes
-            // over this tile's own S buffer, which the previous P.V does not read,
-            // so without a rescale the softmax runs ahead of the tensor pipe.
-            // Parity waits are unambiguous: S(i) complete implies every MMA issued
-            // before it (P.V up to tile i-2) completed, and P.V(i) cannot complete
-            // before P(i) is written.
-            const bool any_resc = __any_sync(0xffffffffu, resc);
-            if (i > 0 && any_resc) {
-                ok = __all_sync(0xffffffffu, wt.wait(o_done((i - 1) & 1), ((i - 1) >> 1) & 1));
-                if (!ok) continue;
-                tc::tc_fence_after();
-            }
-            if (any_resc) {
-#pragma unroll 1
-                for (int cb = 0; cb < DO / 64; ++cb) {
-                    const uint32_t col = tm_o + h * (DO / 2) + cb * 32 + lane_base;
-                    uint32_t rr[32];
-                    tc::tmem_ld32(col, rr);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        asm volatile("" : "+r"(rr[e]));
-                        rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
-                    }
-                    tc::tmem_st32(col, rr);
+                    put_q(cb, w);
                 }
             }
-            // P over the first 64 columns of the S buffer it came from
-            tc::tmem_st32(tm_s + (uint32_t)(i & 1) * BN + h * 32 + lane_base, pk);
-            tc::tmem_st_wait();
+            if constexpr (C::QTM)
+                tc::tmem_st_wait();
+            else
+                tc::fence_async_smem();
             tc::tc_fence_before();
             if constexpr (PAIR) {
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(p_full(i & 1));
+                if (lane == 0) tc::mbar_arrive_cluster(tc::mapa_shared(q_full, 0));
             } else {
-                tc::mbar_arrive(p_full(i & 1));
+                tc::mbar_arrive(q_full);
             }
-            n_done = i + 1;
-        }
+        };
 
-        // ---- epilogue: both outstanding P.V (tiles n-2 and n-1) must be complete
-        if (ok && n_done > 0) {
-            ok = __all_sync(0xffffffffu, wt.wait(o_done((n_done - 1) & 1), ((n_done - 1) >> 1) & 1));
-            if (ok && n_done >= 2)
-                ok = __all_sync(0xffffffffu,
-                                wt.wait(o_done((n_done - 2) & 1), ((n_done - 2) >> 1) & 1));
-            tc::tc_fence_after();
+        int k = 0;
+        int uid = slot_unit(0, slot, slots, units);
+        Unit cur{};
+        int cur_n = 0, cur_pos = 0;  // visible tiles and first ring position of unit k
+        if (uid >= 0) {
+            cur = unit_of(a, uid, PAIR, rank, DO);
+            ok = __all_sync(0xffffffffu, wt.wait(list_full(0), 0));
+            cur_n = ok ? n_vis_smem[0] : 0;
+            if (ok && cur_n > 0) convert_q(cur, 0, false);
         }
-        // row sum = both halves' partial sums
-        {
-            float *xs = xchg + (n_done & 1) * 2 * BM;
-            xs[h * BM + r] = l;
-            tc::named_bar(pair_bar, 64);
-            l += xs[(1 - h) * BM + r];
-        }
-        const bool have_o = ok && n_done > 0;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        if (a.o_tma) {
-            // O -> shared memory ([128 rows][32 f32] boxes, 128-byte swizzle) -> TMA store.
-            // The ring (or, at head_dim 512, the Q tile) is idle once the last P.V is done.
-            uint8_t *stg = smem + (D == 512 ? L::kQ : L::kStages);
-            // each half of the rows' threads stages its DO/64 boxes; a box goes out as
-            // soon as its 128 writers are done, and the issuing thread waits only until
-            // the stores have read shared memory
+        int g = 0;  // global index of the current unit's first tile
+        while (uid >= 0 && ok) {
+            const uint16_t *list = lists + (k & 1) * kMaxListTiles;
+            int head = 0, row = 0;
+            const bool valid = row_of(a, cur.t, r, head, row);
+            const uint16_t *mrow = valid ? a.mask + cur.t.lane * a.m_lane + (int64_t)head * a.m_head +
+                                               (int64_t)row * a.m_row + h * 64
+                                         : nullptr;
+            const bool m_vec = valid && (reinterpret_cast<uintptr_t>(mrow) & 15) == 0;
+            float m_ref = kNegInf, l = 0.f;
+            int n_done = 0;  // tiles whose P this thread has handed to the MMA issuer
+            // ---- key tiles: this thread owns columns [h*64, h*64 + 64) of every tile.
+            // Both warps of a row pair run every iteration and every pair barrier, even
+            // after a failed wait (they then skip the work), so neither can be left at
+            // a barrier its partner never reaches.
+            for (int i = 0; i < cur_n; ++i) {
+                const int gi = g + i;
+                const int j = cur.jb + (list[i] & 0x7fff);
+                const int code = (list[i] & 0x8000) ? 2 : 1;
+                if (ok) ok = __all_sync(0xffffffffu, wt.wait(s_full(gi & 1), (gi >> 1) & 1));
+                float s[64];
+                float mx = kNegInf;
+                float sc = 1.f;  // factor still to apply to s (log2 domain)
+                if (ok) {
+                    tc::tc_fence_after();
+                    {
+                        uint32_t rr[64];
+                        tc::tmem_ld32(tm_s + (uint32_t)(gi & 1) * BN + h * 64 + lane_base,
+                                      *reinterpret_cast<uint32_t(*)[32]>(rr));
+                        tc::tmem_ld32(tm_s + (uint32_t)(gi & 1) * BN + h * 64 + 32 + lane_base,
+                                      *reinterpret_cast<uint32_t(*)[32]>(rr + 32));
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            asm volatile("" : "+r"(rr[c]));  // keep every use after the wait
+                            s[c] = __uint_as_float(rr[c]);
+                        }
+                    }
+                    if (!valid) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) s[c] = kNegInf;
+                    } else if (code == 1) {
+                        // no mask: s stays unscaled; the scale is applied inside the exponent
+                        // argument below, and the row maximum is taken on the raw scores
+                        sc = scale_log2;
+                    } else {
+                        const int c0 = j * BN + h * 64;  // key index of s[0]
+                        if (m_vec && c0 + 64 <= n_keys) {
+#pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                const uint4 x = *reinterpret_cast<const uint4 *>(mrow + j * BN + v * 8);
+                                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const uint16_t mv = (uint16_t)(w[e / 2] >> ((e & 1) * 16));
+                                    s[v * 8 + e] = fmaf(s[v * 8 + e], scale_log2,
+                                                        mask_to_f32(mv, mask_bf16) * kLog2e);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 64; ++c)
+                                s[c] = (c0 + c < n_keys)
+                                           ? fmaf(s[c], scale_log2,
+                                                  mask_to_f32(mrow[j * BN + c], mask_bf16) * kLog2e)
+                                           : kNegInf;
+                        }
+                    }
+                    // row max of sc * s over this half (four chains of three-input max; with
+                    // a negative scale the maximum comes from the smallest raw score)
+                    float mq[4] = {s[0], s[1], s[2], s[3]};
+                    if (sc >= 0.f) {
+#pragma unroll
+                        for (int c = 4; c < 60; c += 8)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) mq[k] = fmax3(mq[k], s[c + k], s[c + 4 + k]);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) mq[k] = fmaxf(mq[k], s[60 + k]);
+                        mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+                    } else {
+#pragma unroll
+                        for (int c = 4; c < 60; c += 8)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) mq[k] = fmin3(mq[k], s[c + k], s[c + 4 + k]);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) mq[k] = fminf(mq[k], s[60 + k]);
+                        mx = fmin3(mq[0], mq[1], fminf(mq[2], mq[3]));
+                    }
+                    mx *= sc;
+                }
+                // agree with the other half of the row on the maximum
+                float *xs = xchg + (gi & 1) * 2 * BM;
+                xs[h * BM + r] = mx;
+                tc::named_bar(pair_bar, 64);
+                mx = fmaxf(mx, xs[(1 - h) * BM + r]);
+                if (!ok) continue;
+                float factor = 1.f;
+                bool resc = false;
+                if (m_ref == kNegInf) {
+                    m_ref = mx;
+                } else if (mx > m_ref + kRescaleThreshold) {
+                    factor = ex2(m_ref - mx);
+                    m_ref = mx;
+                    resc = true;
+                }
+                const float nmu = m_ref == kNegInf ? 0.f : -m_ref;
+                uint32_t pk[32];
+                float ra0 = 0.f, ra1 = 0.f, rb0 = 0.f, rb1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; c += 4) {
+                    // p = 2^(sc * s - mu): one packed FMA per two arguments
+                    float x0, x1, x2, x3;
+                    ffma2(x0, x1, s[c], s[c + 1], sc, sc, nmu, nmu);
+                    ffma2(x2, x3, s[c + 2], s[c + 3], sc, sc, nmu, nmu);
+                    const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+                    fadd2(ra0, ra1, ra0, ra1, p0, p1);
+                    fadd2(rb0, rb1, rb0, rb1, p2, p3);
+                    pk[c / 2] = pack2(KV{}, p0, p1);
+                    pk[c / 2 + 1] = pack2(KV{}, p2, p3);
+                }
+                l = l * factor + ((ra0 + ra1) + (rb0 + rb1));
+                // P.V of the previous tile must be done before O is rescaled.  P goes
+                // over this tile's own S buffer, which the previous P.V does not read,
+                // so without a rescale the softmax runs ahead of the tensor pipe.
+                // Parity waits are unambiguous: S(i) complete implies every MMA issued
+                // before it (P.V up to tile i-2) completed, and P.V(i) cannot complete
+                // before P(i) is written.
+                const bool any_resc = __any_sync(0xffffffffu, resc);
+                if (i > 0 && any_resc) {
+                    ok = __all_sync(0xffffffffu, wt.wait(o_done((gi - 1) & 1), ((gi - 1) >> 1) & 1));
+                    if (!ok) continue;
+                    tc::tc_fence_after();
+                }
+                if (any_resc) {
+#pragma unroll 1
+                    for (int cb = 0; cb < DO / 64; ++cb) {
+                        const uint32_t col = tm_o + h * (DO / 2) + cb * 32 + lane_base;
+                        uint32_t rr[32];
+                        tc::tmem_ld32(col, rr);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            asm volatile("" : "+r"(rr[e]));
+                            rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
+                        }
+                        tc::tmem_st32(col, rr);
+                    }
+                }
+                // P over the first 64 columns of the S buffer it came from
+                tc::tmem_st32(tm_s + (uint32_t)(gi & 1) * BN + h * 32 + lane_base, pk);
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
+                if constexpr (PAIR) {
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(p_full(gi & 1));
+                } else {
+                    tc::mbar_arrive(p_full(gi & 1));
+                }
+                n_done = i + 1;
+            }
+            // ---- unit k's tile list is no longer read
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(list_free(k & 1));
+            // ---- the next unit's Q is converted before this unit's epilogue, so that its
+            // first Q.K^T products overlap the epilogue (all of unit k's S are complete:
+            // nothing reads the Q staging area any more)
+            const int nuid = slot_unit(k + 1, slot, slots, units);
+            Unit nxt{};
+            int nxt_n = 0;
+            const int nxt_pos = cur_pos + (cur_n > 0 ? unit_positions(cur_n) : 0);
+            // O goes out by TMA, staged in shared memory.  head_dim <= 256: in the ring
+            // slots of the next unit's f32 Q, held until the stores have read them
+            // (512 D >= 512 DO bytes; the next Q is converted first, so its first Q.K^T
+            // overlaps this epilogue), or after the last unit in the idle ring.  head_dim
+            // 512 (its 8 Q stages cycle through a 3-stage ring and cannot be held): in
+            // the Q tile area (128 KiB), before the next unit's Q is converted.
+            constexpr bool kHoldQ = kQStages <= NS;
+            const bool stage_o = a.o_tma && cur_n > 0;
+            int o_slot0 = 0;       // first ring position of the staging area
+            bool hold_q = false;   // staging in the next unit's Q slots
+            if (nuid >= 0 && ok) {
+                nxt = unit_of(a, nuid, PAIR, rank, DO);
+                ok = __all_sync(0xffffffffu, wt.wait(list_full((k + 1) & 1), ((k + 1) >> 1) & 1));
+                nxt_n = ok ? n_vis_smem[(k + 1) & 1] : 0;
+                if constexpr (kHoldQ) {
+                    hold_q = stage_o && nxt_n > 0;
+                    if (ok && nxt_n > 0) convert_q(nxt, nxt_pos, hold_q);
+                    o_slot0 = nxt_pos;
+                }
+            }
+            const bool use_stage = stage_o && (!kHoldQ || hold_q || nuid < 0);
+
+            // ---- epilogue of unit k: both outstanding P.V (tiles n-2 and n-1) must be complete
+            if (ok && n_done > 0) {
+                const int ga = g + n_done - 1;
+                ok = __all_sync(0xffffffffu, wt.wait(o_done(ga & 1), (ga >> 1) & 1));
+                if (ok && n_done >= 2)
+                    ok = __all_sync(0xffffffffu, wt.wait(o_done((ga - 1) & 1), ((ga - 1) >> 1) & 1));
+                tc::tc_fence_after();
+            }
+            // row sum = both halves' partial sums (the second barrier keeps the next
+            // unit's first row-max exchange, which reuses this buffer, behind the reads)
+            {
+                float *xs = xchg + ((g + n_done) & 1) * 2 * BM;
+                xs[h * BM + r] = l;
+                tc::named_bar(pair_bar, 64);
+                l += xs[(1 - h) * BM + r];
+                tc::named_bar(pair_bar, 64);
+            }
+            const bool have_o = ok && n_done > 0;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            // all of this thread's O columns out of TMEM, then O may be overwritten
             constexpr int NCB = DO / 64;
             uint32_t rr[NCB][32];
             if (have_o) {
 #pragma unroll
-                for (int cb = 0; cb < NCB; ++cb) tc::tmem_ld32(tm_o + (h * NCB + cb) * 32 + lane_base, rr[cb]);
+                for (int cb = 0; cb < NCB; ++cb) tc::tmem_ld32(tm_o + h * (DO / 2) + cb * 32 + lane_base, rr[cb]);
                 tc::tmem_ld_wait();
             } else {
 #pragma unroll
@@ -939,60 +1073,85 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) rr[cb][e] = 0u;
             }
-            const bool issuer = threadIdx.x == h * (kSoftmaxThreads / 2);
+            if (cur_n > 0) {
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(o_free);
+            }
+            if (ok && use_stage) {
+                // [128 rows][32 f32] boxes (128-byte swizzle), two per 32 KiB slot; each half
+                // of the rows' threads stages its DO/64 boxes, and a box goes out as soon as
+                // its 128 writers are done
+                const bool issuer = threadIdx.x == h * (kSoftmaxThreads / 2);
 #pragma unroll
-            for (int cb = 0; cb < NCB; ++cb) {
-                const int box = h * NCB + cb;
+                for (int cb = 0; cb < NCB; ++cb) {
+                    const int box = h * NCB + cb;
+                    uint8_t *stg = kHoldQ ? smem + L::kStages + ((o_slot0 + box / 2) % NS) * kStageBytes +
+                                                (box & 1) * 16384
+                                          : smem + L::kQ + box * 16384;
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    asm volatile("" : "+r"(rr[cb][4 * c4]), "+r"(rr[cb][4 * c4 + 1]), "+r"(rr[cb][4 * c4 + 2]),
-                                 "+r"(rr[cb][4 * c4 + 3]));
-                    *reinterpret_cast<float4 *>(stg + box * 16384 + r * 128 + ((c4 ^ (r & 7)) << 4)) =
-                        make_float4(__uint_as_float(rr[cb][4 * c4]) * inv, __uint_as_float(rr[cb][4 * c4 + 1]) * inv,
-                                    __uint_as_float(rr[cb][4 * c4 + 2]) * inv,
-                                    __uint_as_float(rr[cb][4 * c4 + 3]) * inv);
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        asm volatile("" : "+r"(rr[cb][4 * c4]), "+r"(rr[cb][4 * c4 + 1]), "+r"(rr[cb][4 * c4 + 2]),
+                                     "+r"(rr[cb][4 * c4 + 3]));
+                        *reinterpret_cast<float4 *>(stg + r * 128 + ((c4 ^ (r & 7)) << 4)) =
+                            make_float4(__uint_as_float(rr[cb][4 * c4]) * inv, __uint_as_float(rr[cb][4 * c4 + 1]) * inv,
+                                        __uint_as_float(rr[cb][4 * c4 + 2]) * inv,
+                                        __uint_as_float(rr[cb][4 * c4 + 3]) * inv);
+                    }
+                    tc::fence_async_smem();
+                    tc::named_bar(6 + h, kSoftmaxThreads / 2);
+                    if (issuer && !*abort_flag)
+                        tc::tma_store_3d(&tmo, smem_u32(stg), cur.d_off + box * 32,
+                                         a.o_rows_dim1 ? cur.q_row0 : cur.q_head0,
+                                         a.o_rows_dim1 ? cur.q_head0 : cur.q_row0);
                 }
-                tc::fence_async_smem();
-                tc::named_bar(6 + h, kSoftmaxThreads / 2);
-                if (issuer && !*abort_flag)
-                    tc::tma_store_3d(&tmo, smem_u32(stg + box * 16384), d_off + box * 32,
-                                     a.o_rows_dim1 ? q_row0 : q_head0, a.o_rows_dim1 ? q_head0 : q_row0);
-            }
-            if (issuer) {
-                tc::bulk_commit();
-                tc::bulk_wait_read0();
-            }
-        } else if (ok) {
-            float *dst;
-            if (a.splits == 1) {
-                dst = valid ? a.o + t.lane * a.o_lane + (int64_t)head * a.o_head +
-                                  (int64_t)row * a.o_row + d_off + h * (DO / 2)
-                            : nullptr;
-            } else {
-                const int64_t unit = ((int64_t)tile_id * a.d_parts + dpart) * a.splits + split;
-                dst = a.ws_o + (unit * BM + r) * DO + h * (DO / 2);
-                if (h == 0) a.ws_lse[unit * BM + r] = l > 0.f ? m_ref + __log2f(l) : kNegInf;
-            }
-#pragma unroll 1
-            for (int cb = 0; cb < DO / 64; ++cb) {
-                uint32_t rr[32];
-                if (have_o) {
-                    tc::tmem_ld32(tm_o + h * (DO / 2) + cb * 32 + lane_base, rr);
-                    tc::tmem_ld_wait();
+                if (issuer) {
+                    tc::bulk_commit();
+                    tc::bulk_wait_read0();
+                }
+            } else if (ok) {
+                float *dst;
+                if (a.splits == 1) {
+                    dst = valid ? a.o + cur.t.lane * a.o_lane + (int64_t)head * a.o_head +
+                                      (int64_t)row * a.o_row + cur.d_off + h * (DO / 2)
+                                : nullptr;
                 } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[e] = 0u;
+                    const int64_t unit = ((int64_t)cur.tile_id * a.d_parts + cur.dpart) * a.splits + cur.split;
+                    dst = a.ws_o + (unit * BM + r) * DO + h * (DO / 2);
+                    if (h == 0) a.ws_lse[unit * BM + r] = l > 0.f ? m_ref + __log2f(l) : kNegInf;
                 }
                 if (dst) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        asm volatile("" : "+r"(rr[e]), "+r"(rr[e + 1]), "+r"(rr[e + 2]), "+r"(rr[e + 3]));
-                        *reinterpret_cast<float4 *>(dst + cb * 32 + e) =
-                            make_float4(__uint_as_float(rr[e]) * inv, __uint_as_float(rr[e + 1]) * inv,
-                                        __uint_as_float(rr[e + 2]) * inv, __uint_as_float(rr[e + 3]) * inv);
-                    }
+                    for (int cb = 0; cb < NCB; ++cb)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            asm volatile("" : "+r"(rr[cb][e]), "+r"(rr[cb][e + 1]), "+r"(rr[cb][e + 2]),
+                                         "+r"(rr[cb][e + 3]));
+                            *reinterpret_cast<float4 *>(dst + cb * 32 + e) =
+                                make_float4(__uint_as_float(rr[cb][e]) * inv, __uint_as_float(rr[cb][e + 1]) * inv,
+                                            __uint_as_float(rr[cb][e + 2]) * inv,
+                                            __uint_as_float(rr[cb][e + 3]) * inv);
+                        }
                 }
             }
+            // the held Q slots of the next unit go back to the producer once both row
+            // halves' stores have read them
+            if (hold_q) {
+                tc::named_bar(1, kSoftmaxThreads);
+                if (threadIdx.x == 0)
+                    for (int qs = 0; qs < kQStages; ++qs) release_slot((nxt_pos + qs) % NS);
+            }
+            if constexpr (!kHoldQ) {
+                // head_dim 512: the staged O has been read out of the Q area; now the next Q
+                if (use_stage) tc::named_bar(1, kSoftmaxThreads);
+                if (nuid >= 0 && ok && nxt_n > 0) convert_q(nxt, nxt_pos, false);
+            }
+            g += cur_n;
+            cur = nxt;
+            cur_n = nxt_n;
+            cur_pos = nxt_pos;
+            uid = nuid;
+            ++k;
         }
     }
 
@@ -1065,7 +1224,8 @@ struct Plan {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// 0: never pair; 1: pair where it measured faster (head_dim 512); 2: pair every eligible shape
+// 0: never pair; 1: pair where it measured faster (head_dim 256 and 512, i.e. every
+// shape that can pair today); 2: pair every eligible shape
 int g_pair_mode = 1;
 
 // CTA pairs need two query tiles that see the same key tiles: one head each,
@@ -1073,7 +1233,7 @@ int g_pair_mode = 1;
 // head tiles per KV group, and Q staged in shared memory (head_dim >= 256).
 bool pairable(int rows, int n_heads, int n_kv_heads, int head_dim, bool shared_mask) {
     const int group = n_heads / n_kv_heads;
-    if (g_pair_mode == 0 || (g_pair_mode == 1 && head_dim != 512)) return false;
+    if (g_pair_mode == 0 || (g_pair_mode == 1 && head_dim < 256)) return false;
     return shared_mask && head_dim >= 256 && rows >= BM && group % 2 == 0;
 }
 
@@ -1265,6 +1425,7 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     a.heads_per_tile = pl.heads_per_tile;
     a.row_tiles = pl.row_tiles;
     a.head_tiles = pl.head_tiles;
+    a.tiles_total = pl.tiles;
     a.n_blk = pl.n_blk;
     a.splits = pl.splits;
     a.blk_per_split = pl.bps;
@@ -1299,7 +1460,8 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
         a.q_tma = 1;
         a.q_rows_dim1 = rows_first(p.n_heads, p.q_row_stride, p.q_head_stride) ? 1 : 0;
     }
-    if (single_head_tiles && pl.splits == 1 &&
+    // O out by TMA, staged where the next unit's f32 Q arrives (so only with Q by TMA)
+    if (a.q_tma && pl.splits == 1 &&
         make_map(&maps[3], p.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.head_dim, p.rows, p.n_heads,
                  p.o_row_stride, p.o_head_stride, 32, BM)) {
         a.o_tma = 1;
@@ -1309,25 +1471,29 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     classify_kernel<<<dim3(pl.code_groups, pl.code_cols), BM, 0, stream>>>(a, const_cast<uint8_t *>(a.codes));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // CTAs launched: a pair is two CTAs, one per query tile, so the count is the same
-    const int units = pl.tiles * pl.d_parts * pl.splits;
+    // persistent launch: one CTA (or CTA pair) per SM (or SM pair) at most; each runs
+    // the units of its slot back to back
+    const int units = pl.tiles * pl.d_parts * pl.splits;  // query tiles x output halves x key splits
+    int sms = sm_count();
+    if (sms <= 0) sms = 148;
+    const int ctas = pl.pair ? 2 * std::min(units / 2, sms / 2) : std::min(units, sms);
     const bool bf = a.kv_bf16;
     switch (p.head_dim) {
         case 128:
-            return bf ? run_attn<128, BF16, false>(a, maps, units, pl.tiles, stream)
-                      : run_attn<128, F16, false>(a, maps, units, pl.tiles, stream);
+            return bf ? run_attn<128, BF16, false>(a, maps, ctas, pl.tiles, stream)
+                      : run_attn<128, F16, false>(a, maps, ctas, pl.tiles, stream);
         case 256:
             if (pl.pair)
-                return bf ? run_attn<256, BF16, true>(a, maps, units, pl.tiles, stream)
-                          : run_attn<256, F16, true>(a, maps, units, pl.tiles, stream);
-            return bf ? run_attn<256, BF16, false>(a, maps, units, pl.tiles, stream)
-                      : run_attn<256, F16, false>(a, maps, units, pl.tiles, stream);
+                return bf ? run_attn<256, BF16, true>(a, maps, ctas, pl.tiles, stream)
+                          : run_attn<256, F16, true>(a, maps, ctas, pl.tiles, stream);
+            return bf ? run_attn<256, BF16, false>(a, maps, ctas, pl.tiles, stream)
+                      : run_attn<256, F16, false>(a, maps, ctas, pl.tiles, stream);
         case 512:
             if (pl.pair)
-                return bf ? run_attn<512, BF16, true>(a, maps, units, pl.tiles, stream)
-                          : run_attn<512, F16, true>(a, maps, units, pl.tiles, stream);
-            return bf ? run_attn<512, BF16, false>(a, maps, units, pl.tiles, stream)
-                      : run_attn<512, F16, false>(a, maps, units, pl.tiles, stream);
+                return bf ? run_attn<512, BF16, true>(a, maps, ctas, pl.tiles, stream)
+                          : run_attn<512, F16, true>(a, maps, ctas, pl.tiles, stream);
+            return bf ? run_attn<512, BF16, false>(a, maps, ctas, pl.tiles, stream)
+                      : run_attn<512, F16, false>(a, maps, ctas, pl.tiles, stream);
         default:
             return cudaErrorInvalidValue;
     }

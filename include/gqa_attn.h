@@ -99,7 +99,7 @@ int gqa_selftest_bounded_wait(int32_t *status, int timeout_ms, gqa_stream_t stre
  * a mask shared by all heads) as one two-CTA cluster whose tensor cores share
  * each K/V tile, so each SM loads half of every K and V tile.
  *   mode 0  never pair
- *   mode 1  pair where it measured faster on GB300: head_dim 512 (default)
+ *   mode 1  pair where it measured faster on GB300: head_dim 256 and 512 (default)
  *   mode 2  pair every eligible shape
  * All modes give the same result up to f32 summation order.  Process-wide,
  * not synchronised with launches in flight on other threads.  Returns
