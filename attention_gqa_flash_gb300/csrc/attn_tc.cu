@@ -793,8 +793,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::named_bar(1, kSoftmaxThreads);  // every softmax thread is done with this stage
                     if (threadIdx.x == 0 && !hold) release_slot(stage);
                 }
+            } else if (!a.q_f32) {
+                // 16-bit Q: each thread reads its half of its own row with all loads in
+                // flight at once, then stores the blocks
+                uint4 x[D / 64][4];
+#pragma unroll
+                for (int cb = 0; cb < D / 64; ++cb)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        x[cb][v] = valid ? ld_nc_v4(static_cast<const uint16_t *>(a.q) + un.t.lane * a.q_lane +
+                                                    (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64 +
+                                                    h * 32 + v * 8)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int cb = 0; cb < D / 64; ++cb) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        w[4 * v] = x[cb][v].x;
+                        w[4 * v + 1] = x[cb][v].y;
+                        w[4 * v + 2] = x[cb][v].z;
+                        w[4 * v + 3] = x[cb][v].w;
+                    }
+                    put_q(cb, w);
+                }
             } else {
-                // each thread reads its half of its own row
+                // f32 Q without TMA: each thread reads its half of its own row
 #pragma unroll 1
                 for (int cb = 0; cb < D / 64; ++cb) {
                     uint32_t w[16];
@@ -896,10 +920,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sc = scale_log2;
                     } else {
                         const int c0 = j * BN + h * 64;  // key index of s[0]
+                        const uint16_t *mt = mrow + j * BN;
                         if (m_vec && c0 + 64 <= n_keys) {
 #pragma unroll
                             for (int v = 0; v < 8; ++v) {
-                                const uint4 x = *reinterpret_cast<const uint4 *>(mrow + j * BN + v * 8);
+                                const uint4 x = *reinterpret_cast<const uint4 *>(mt + v * 8);
                                 const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) {
@@ -909,11 +934,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                             }
                         } else {
+                            // the row ends inside this half (or the row is not 16-byte
+                            // aligned): loads at clamped, valid indices, all independent so
+                            // that their latencies overlap
+                            uint16_t mv[64];
+#pragma unroll
+                            for (int c = 0; c < 64; ++c) mv[c] = mt[min(c0 + c, n_keys - 1) - c0];
 #pragma unroll
                             for (int c = 0; c < 64; ++c)
                                 s[c] = (c0 + c < n_keys)
-                                           ? fmaf(s[c], scale_log2,
-                                                  mask_to_f32(mrow[j * BN + c], mask_bf16) * kLog2e)
+                                           ? fmaf(s[c], scale_log2, mask_to_f32(mv[c], mask_bf16) * kLog2e)
                                            : kNegInf;
                         }
                     }
