@@ -64,6 +64,8 @@ def _load():
                 getattr(lib, name).restype = i32
             lib.orc_pack_attention.argtypes = [vp] * 11
             lib.orc_fill_mask.argtypes = [vp, vp, vp]
+            lib.orc_verify_ring_attention.restype = i32
+            lib.orc_verify_ring_attention.argtypes = [vp] * 8 + [dbl, vp]
             lib.orc_commit_kv.argtypes = [vp] * 7
             lib.orc_ring_geometry_valid.restype = i32
             lib.orc_ring_geometry_valid.argtypes = [vp]
@@ -268,6 +270,26 @@ def pack_attention(ring_k, ring_v, cur_q, cur_k, cur_v, cache_lengths, write_pos
     if rc != 0:
         raise ValueError("invalid ring geometry")
     return pq, pk, pv
+
+
+def verify_ring_attention(ring_k, ring_v, cur_q, cur_k, cur_v, cache_lengths, write_positions,
+                          g, scale: float) -> np.ndarray:
+    """Verify attention read straight from the ring (keys: the current rows, then every
+    visible ring slot in slot order): float64 [lanes, rows, q_heads, d]."""
+    g = _geom(g)
+    B, H, HK, D, R, W, K, _ = (int(x) for x in g)
+    args = [_c(ring_k, np.uint16), _c(ring_v, np.uint16), _c(cur_q, np.float32),
+            _c(cur_k, np.float32), _c(cur_v, np.float32), _c(cache_lengths, np.uint32),
+            _c(write_positions, np.uint32)]
+    if args[0].shape != (B, HK, W, D) or args[2].shape != (B, R, H, D) or \
+            args[3].shape != (B, R, HK, D):
+        raise ValueError("ring shapes")
+    out = np.zeros((B, R, H, D), np.float64)
+    rc = _load().orc_verify_ring_attention(*[_ptr(a) for a in args], _ptr(g), float(scale),
+                                           _ptr(out))
+    if rc != 0:
+        raise ValueError("invalid ring geometry" if rc == 1 else "out of memory")
+    return out
 
 
 def fill_mask(cache_lengths, g) -> np.ndarray:

@@ -418,6 +418,78 @@ int orc_commit_kv(const float *new_k, const float *new_v, const uint32_t *commit
 }
 
 /*
+ * Verify attention read straight from the ring [DF, the pack and mask
+ * dispatchers taken together]: for lane b, query head qh (KV head
+ * qh / (q_heads / kv_heads)) and draft row r, the keys are
+ *   - the rows current rows c, bf16(cur_k[b][c][kh]) / bf16(cur_v[b][c][kh]),
+ *     all visible, and
+ *   - every ring slot s whose history index j = (write_position - 1 - s) mod w
+ *     satisfies j < min(cache_length, w) and r + j + 1 < w,
+ * and the query is bf16(cur_q[b][r][qh]).  This is the same set of (key,
+ * value, visibility) the packed layout holds, visited in ring order instead
+ * of newest first.  out: double [b][r][h][d].
+ */
+int orc_verify_ring_attention(const uint16_t *ring_k, const uint16_t *ring_v, const float *cur_q,
+                              const float *cur_k, const float *cur_v,
+                              const uint32_t *cache_lengths, const uint32_t *write_positions,
+                              const uint32_t *g, double scale, double *out)
+{
+    if (!orc_ring_geometry_valid(g))
+        return 1;
+    const int64_t B = g[0], H = g[1], HK = g[2], D = g[3], R = g[4], W = g[5];
+    const int64_t group = H / HK, nk = R + W;
+    int bad = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t qh = 0; qh < H; ++qh) {
+            const int64_t kh = qh / group;
+            const int64_t len = cache_lengths[b] < W ? cache_lengths[b] : W;
+            const int64_t wp = write_positions[b] % W;
+            uint16_t *cur = (uint16_t *)malloc(sizeof(uint16_t) * 2 * R * D);
+            const uint16_t **krow = (const uint16_t **)malloc(sizeof(void *) * nk);
+            const uint16_t **vrow = (const uint16_t **)malloc(sizeof(void *) * nk);
+            double *s = (double *)malloc(sizeof(double) * nk);
+            double *q = (double *)malloc(sizeof(double) * D);
+            if (!cur || !krow || !vrow || !s || !q) {
+#pragma omp atomic write
+                bad = 1;
+            } else {
+                for (int64_t c = 0; c < R; ++c)
+                    for (int64_t e = 0; e < D; ++e) {
+                        cur[c * D + e] = orc_f32_to_bf16(cur_k[((b * R + c) * HK + kh) * D + e]);
+                        cur[(R + c) * D + e] = orc_f32_to_bf16(cur_v[((b * R + c) * HK + kh) * D + e]);
+                    }
+                for (int64_t r = 0; r < R; ++r) {
+                    int n = 0;
+                    for (int64_t c = 0; c < R; ++c) {
+                        krow[n] = cur + c * D;
+                        vrow[n] = cur + (R + c) * D;
+                        ++n;
+                    }
+                    for (int64_t slot = 0; slot < W; ++slot) {
+                        const int64_t j = ((wp - 1 - slot) % W + W) % W;
+                        if (j < len && r + j + 1 < W) {
+                            krow[n] = ring_k + ((b * HK + kh) * W + slot) * D;
+                            vrow[n] = ring_v + ((b * HK + kh) * W + slot) * D;
+                            ++n;
+                        }
+                    }
+                    for (int64_t e = 0; e < D; ++e)
+                        q[e] = widen_bf16(orc_f32_to_bf16(cur_q[((b * R + r) * H + qh) * D + e]));
+                    attention_row(q, (int)D, krow, vrow, ORC_BF16, n, NULL, scale, s,
+                                  out + ((b * R + r) * H + qh) * D);
+                }
+            }
+            free(cur);
+            free(krow);
+            free(vrow);
+            free(s);
+            free(q);
+        }
+    return bad ? 2 : 0;
+}
+
+/*
  * Draft mask rows [DF, dispatch_dflash2_mask_rows_f32 and its test
  * gpu_mask_rows_preserve_anchors]: hidden is [lanes*rows][width] f32; in each
  * lane, row 0 (the anchor) is kept and rows 1..rows-1 become the widened bf16

@@ -193,3 +193,55 @@ def test_counters_are_clamped():
     rk2, _ = oracle.commit_kv(c.new_k, c.new_v, np.array([3, 3], np.uint32),
                               np.array([2, 2], np.uint32), c.ring_k, c.ring_v, g)
     np.testing.assert_array_equal(rk1, rk2)
+
+
+# ---------------------------------------------------------------------------
+# Ring-direct verify attention (the keys visited in ring-slot order)
+# ---------------------------------------------------------------------------
+def _chain(c, lens=None, pos=None):
+    g = c.geom
+    lens = c.cache_lengths if lens is None else lens
+    pos = c.write_positions if pos is None else pos
+    pq, pk, pv = oracle.pack_attention(c.ring_k, c.ring_v, c.cur_q, c.cur_k, c.cur_v, lens, pos, g)
+    mask = oracle.fill_mask(lens, g)
+    return oracle.verify_attention(pq, pk, pv, mask, g, c.scale)
+
+
+def test_ring_direct_equals_pack_mask_verify_chain():
+    """Same keys, values and visibility as the packed layout, visited in slot order;
+    covers write positions that wrap, empty and full histories and clamped counters."""
+    for seed, (R, W) in enumerate([(3, 11), (5, 12), (2, 40), (16, 37)]):
+        c = workloads.ring(lanes=4, rows=R, window=W, q_heads=4, kv_heads=2, head_dim=128,
+                           seed=20 + seed)
+        lens = np.array([0, W - 1, W, 5 * W + 3][: 4], np.uint32)
+        pos = np.array([W - 1, 0, W * 3 + 1, 2], np.uint32)
+        for ln, ps in [(c.cache_lengths, c.write_positions), (lens, pos)]:
+            got = oracle.verify_ring_attention(c.ring_k, c.ring_v, c.cur_q, c.cur_k, c.cur_v,
+                                               ln, ps, c.geom, c.scale)
+            np.testing.assert_allclose(got, _chain(c, ln, ps), rtol=1e-12, atol=1e-13)
+
+
+def test_ring_direct_is_invariant_under_slot_rotation():
+    """Rotating the ring contents by t slots together with the write position leaves
+    every history index, hence the result, unchanged."""
+    c = workloads.ring(lanes=2, rows=4, window=23, q_heads=4, kv_heads=1, head_dim=128, seed=31)
+    base = oracle.verify_ring_attention(c.ring_k, c.ring_v, c.cur_q, c.cur_k, c.cur_v,
+                                        c.cache_lengths, c.write_positions, c.geom, c.scale)
+    for t in (1, 7, 22):
+        rk = np.roll(c.ring_k, t, axis=2)
+        rv = np.roll(c.ring_v, t, axis=2)
+        pos = ((c.write_positions.astype(np.int64) + t) % 23).astype(np.uint32)
+        got = oracle.verify_ring_attention(rk, rv, c.cur_q, c.cur_k, c.cur_v, c.cache_lengths,
+                                           pos, c.geom, c.scale)
+        np.testing.assert_allclose(got, base, rtol=1e-12, atol=1e-13)
+
+
+def test_ring_direct_with_empty_history_is_attention_over_current_rows():
+    c = workloads.ring(lanes=1, rows=6, window=10, q_heads=4, kv_heads=2, head_dim=128, seed=33)
+    got = oracle.verify_ring_attention(c.ring_k, c.ring_v, c.cur_q, c.cur_k, c.cur_v,
+                                       np.array([0], np.uint32), np.array([3], np.uint32),
+                                       c.geom, c.scale)
+    ref = oracle.attention(workloads.bf16_bits(c.cur_q[0]), workloads.bf16_bits(c.cur_k[0]),
+                           workloads.bf16_bits(c.cur_v[0]), kv_dtype="bf16", q_dtype="bf16",
+                           scale=c.scale)
+    np.testing.assert_allclose(got[0], ref, rtol=1e-12, atol=1e-13)
