@@ -82,6 +82,8 @@ def library() -> ctypes.CDLL:
             "gqa_fill_mask": (i32, [vp, sz, vp, sz, rp, vp, vp]),
             "gqa_attn_verify_workspace_size": (sz, [rp]),
             "gqa_attn_verify": (i32, [vp, sz] * 5 + [rp, f32, vp, sz, vp, vp]),
+            "gqa_attn_verify_ring_workspace_size": (sz, [rp]),
+            "gqa_attn_verify_ring": (i32, [vp, sz] * 8 + [rp, f32, vp, sz, vp, vp]),
             "gqa_commit_kv": (i32, [vp, sz] * 6 + [rp, vp, vp]),
             "gqa_set_mask_rows": (i32, [vp, sz, vp, sz, ctypes.c_uint32, ctypes.c_uint32,
                                         ctypes.c_uint32, vp]),
@@ -103,7 +105,8 @@ def exported_symbols() -> list[str]:
             "gqa_attn_paged_decode_workspace_size", "gqa_attn_paged_decode",
             "gqa_attn_paged_decode_noalloc",
             "gqa_ring_params_valid", "gqa_pack_attention", "gqa_fill_mask",
-            "gqa_attn_verify_workspace_size", "gqa_attn_verify", "gqa_commit_kv",
+            "gqa_attn_verify_workspace_size", "gqa_attn_verify",
+            "gqa_attn_verify_ring_workspace_size", "gqa_attn_verify_ring", "gqa_commit_kv",
             "gqa_set_mask_rows"]
 
 
@@ -359,6 +362,33 @@ def gqa_attn_verify(packed_q, packed_k, packed_v, mask, params, scale: float, ou
         args += list(_exact(name, t, dt))
     _check(library().gqa_attn_verify(*args, ctypes.byref(p), float(scale), _ptr(workspace),
                                      _nbytes(workspace), _ptr(status), _stream(stream)))
+    return out
+
+
+def gqa_attn_verify_ring_workspace_size(params) -> int:
+    return int(library().gqa_attn_verify_ring_workspace_size(ctypes.byref(_ring(params))))
+
+
+def gqa_attn_verify_ring(ring_k, ring_v, cur_q, cur_k, cur_v, cache_lengths, write_positions,
+                         params, scale: float, out=None, workspace=None, status=None,
+                         stream=None) -> torch.Tensor:
+    """Fused verify attention read straight from the ring (no packed copy, no mask
+    tensor): O f32 [lanes, rows, q_heads, head_dim]."""
+    p = _ring(params)
+    if out is None:
+        out = torch.empty((p.lanes, p.rows, p.q_heads, p.head_dim), dtype=torch.float32,
+                          device=cur_q.device)
+    if workspace is None:
+        n = gqa_attn_verify_ring_workspace_size(p)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=cur_q.device)
+    args = []
+    for name, t, dt in (("ring_k", ring_k, torch.bfloat16), ("ring_v", ring_v, torch.bfloat16),
+                        ("cur_q", cur_q, torch.float32), ("cur_k", cur_k, torch.float32),
+                        ("cur_v", cur_v, torch.float32), ("cache_lengths", cache_lengths, torch.int32),
+                        ("write_positions", write_positions, torch.int32), ("out", out, torch.float32)):
+        args += list(_exact(name, t, dt))
+    _check(library().gqa_attn_verify_ring(*args, ctypes.byref(p), float(scale), _ptr(workspace),
+                                          _nbytes(workspace), _ptr(status), _stream(stream)))
     return out
 
 

@@ -482,6 +482,83 @@ int gqa_attn_verify(const uint16_t *packed_q, size_t packed_q_bytes, const uint1
     return ok();
 }
 
+size_t gqa_attn_verify_ring_workspace_size(const gqa_ring_params *p) {
+    if (!gqa_ring_params_valid(p)) return 0;
+    return gqa::verify_ring_workspace_bytes(*p);
+}
+
+int gqa_attn_verify_ring(const uint16_t *ring_k, size_t ring_k_bytes, const uint16_t *ring_v,
+                         size_t ring_v_bytes, const float *cur_q, size_t cur_q_bytes,
+                         const float *cur_k, size_t cur_k_bytes, const float *cur_v,
+                         size_t cur_v_bytes, const uint32_t *cache_lengths,
+                         size_t cache_lengths_bytes, const uint32_t *write_positions,
+                         size_t write_positions_bytes, float *o, size_t o_bytes,
+                         const gqa_ring_params *p, float scale, void *workspace,
+                         size_t workspace_bytes, int32_t *status, gqa_stream_t stream) {
+    RING_CHECK(p);
+    if (!std::isfinite(scale)) return fail("verify_ring: scale must be finite");
+    const uint64_t b = p->lanes, h = p->q_heads, hk = p->kv_heads, d = p->head_dim, r = p->rows,
+                   w = p->window;
+    const uint64_t ring[] = {b, hk, w, d}, cq[] = {b, r, h, d}, ck[] = {b, r, hk, d}, lanes[] = {b},
+                   od[] = {b, r, h, d};
+    int rc;
+    if ((rc = require_exact("ring keys", ring_k, ring_k_bytes, ring, 4, 2))) return rc;
+    if ((rc = require_exact("ring values", ring_v, ring_v_bytes, ring, 4, 2))) return rc;
+    if ((rc = require_exact("current queries", cur_q, cur_q_bytes, cq, 4, 4))) return rc;
+    if ((rc = require_exact("current keys", cur_k, cur_k_bytes, ck, 4, 4))) return rc;
+    if ((rc = require_exact("current values", cur_v, cur_v_bytes, ck, 4, 4))) return rc;
+    if ((rc = require_exact("cache lengths", cache_lengths, cache_lengths_bytes, lanes, 1, 4)))
+        return rc;
+    if ((rc = require_exact("write positions", write_positions, write_positions_bytes, lanes, 1, 4)))
+        return rc;
+    if ((rc = require_exact("output", o, o_bytes, od, 4, 4))) return rc;
+    if (!aligned(ring_k, 16) || !aligned(ring_v, 16) || !aligned(cur_q, 16) || !aligned(cur_k, 16) ||
+        !aligned(cur_v, 16))
+        return fail("verify_ring: rings and current rows must be 16-byte aligned");
+    const size_t ws_need = gqa::verify_ring_workspace_bytes(*p);
+    if (ws_need && (rc = need("workspace", workspace, workspace_bytes, ws_need))) return rc;
+    if (ws_need && !aligned(workspace, 256)) return fail("verify_ring: workspace must be 256-byte aligned");
+
+    gqa::AttnProblem a{};
+    a.q = cur_q;  // [b][r][h][d] f32, rounded to bf16 in the kernel
+    a.q_is_f32 = true;
+    a.q_row_stride = h * d;
+    a.q_head_stride = d;
+    a.q_lane_stride = r * h * d;
+    a.k = ring_k;
+    a.v = ring_v;
+    a.kv_dtype = GQA_DTYPE_BF16;
+    a.k_row_stride = d;
+    a.k_head_stride = w * d;
+    a.v_row_stride = d;
+    a.v_head_stride = w * d;
+    a.kv_lane_stride = hk * w * d;
+    a.kv_rows = (int)w;
+    a.mask = nullptr;
+    a.mask_is_bf16 = true;
+    a.o = o;
+    a.o_row_stride = h * d;
+    a.o_head_stride = d;
+    a.o_lane_stride = r * h * d;
+    a.lanes = (int)b;
+    a.rows = (int)r;
+    a.n_heads = (int)h;
+    a.n_kv_heads = (int)hk;
+    a.head_dim = (int)d;
+    a.n_keys = 0;
+    a.scale = scale;
+    a.status = status;
+    a.ring = true;
+    a.ring_w = (int)w;
+    a.cur_k = cur_k;
+    a.cur_v = cur_v;
+    a.ring_len = cache_lengths;
+    a.ring_wp = write_positions;
+    cudaError_t e = gqa::launch_attention(a, workspace, cs(stream));
+    if (e != cudaSuccess) return cuda_fail("verify_ring launch", e);
+    return ok();
+}
+
 int gqa_commit_kv(const float *new_k, size_t new_k_bytes, const float *new_v,
                   size_t new_v_bytes, const uint32_t *commit_counts, size_t commit_counts_bytes,
                   const uint32_t *write_positions, size_t write_positions_bytes,

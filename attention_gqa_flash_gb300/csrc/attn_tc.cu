@@ -130,7 +130,39 @@ struct AttnArgs {
     float *ws_o;      // split partials [unit][BM][DO]
     float *ws_lse;    // [unit][BM]
     int32_t *status;
+    // ring-direct verify: key tile 0 holds the lane's current rows (converted from
+    // f32 in shared memory, padded with zero rows), key tile t >= 1 holds ring slots
+    // [128 (t-1), 128 t); visibility comes from the lane's cache length and write
+    // position instead of a mask
+    int ring, ring_w, ring_r;
+    const float *cur_k, *cur_v;           // [lanes][ring_r][n_kv_heads][head_dim]
+    const uint32_t *ring_len, *ring_wp;   // [lanes]
 };
+
+// number of slots of [a, b) inside the circular range of `len` slots that starts at
+// `start` in a ring of w slots
+__device__ __forceinline__ int circ_overlap(int a, int b, int start, int len, int w) {
+    if (len <= 0) return 0;
+    auto lin = [](int a0, int b0, int a1, int b1) { return max(0, min(b0, b1) - max(a0, a1)); };
+    if (start + len <= w) return lin(a, b, start, start + len);
+    return lin(a, b, start, w) + lin(a, b, 0, start + len - w);
+}
+
+// Ring-direct verify: code of key tile t (0 skip, 1 every key visible to every
+// row, 2 mixed) for a lane with history length L (clamped to the window) and
+// write position wp (mod the window).  History index j = (wp - 1 - slot) mod w
+// is visible to draft row r when j < L and r + j + 1 < w: the slots seen by row 0
+// are the L' = min(L, w - 1) newest, those seen by every row the min(L, w - rows)
+// newest, each a circular range ending at slot wp - 1.
+__device__ __forceinline__ int ring_tile_code(const AttnArgs &a, int t, int L, int wp) {
+    if (t == 0) return 2;  // current rows, then padding
+    const int w = a.ring_w, s0 = (t - 1) * BN, s1 = min(s0 + BN, w);
+    const int l_any = min(L, w - 1), l_all = max(0, min(L, w - a.ring_r));
+    const int any = circ_overlap(s0, s1, ((wp - l_any) % w + w) % w, l_any, w);
+    if (any == 0) return 0;
+    const int all = circ_overlap(s0, s1, ((wp - l_all) % w + w) % w, l_all, w);
+    return all == BN ? 1 : 2;
+}
 
 struct Tile {
     int lane, kh, ht, rt;
@@ -340,7 +372,7 @@ __device__ __forceinline__ int slot_unit(int k, int slot, int slots, int units) 
 // (cta_group::2).  Each CTA loads only half of every K tile (64 of its keys) and
 // half of every V tile (half of the output columns), so the K/V bytes an SM takes
 // in per tile are halved; the even CTA issues all MMAs.
-template <int D, class KV, bool PAIR>
+template <int D, class KV, bool PAIR, bool RING = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq,
@@ -351,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kBf16 = KV::kind == GQA_DTYPE_BF16;
     constexpr int kQStages = D / 64;  // an f32 Q tile crosses the ring 64 columns per stage
     static_assert(!PAIR || D >= 256, "CTA pairs stage Q in shared memory (head_dim >= 256)");
+    static_assert(!(PAIR && RING), "ring-direct verify runs unpaired");
     // ring stages per K and per V tile (PAIR: one stage holds this CTA's 64 keys x
     // 256 columns of K, or its 128 keys x 128 output columns of V)
     constexpr int KST = PAIR ? D / 256 : KSUB;
@@ -467,11 +500,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the list buffer of unit k - 2 must have been read by every role
                 if (k >= 2) ok = __all_sync(0xffffffffu, wt.wait(list_free(b), ((k - 2) >> 1) & 1));
                 if (!ok) break;
+                // ring-direct verify: the lane's history length and write position
+                int ring_l = 0, ring_p = 0;
+                if constexpr (RING) {
+                    const uint32_t rl = a.ring_len[un.t.lane], rp = a.ring_wp[un.t.lane];
+                    // out-of-range counters are clamped, as by the pack and mask kernels
+                    if (lane == 0 && (rl > (uint32_t)a.ring_w || rp >= (uint32_t)a.ring_w))
+                        raise_flag(a.status, GQA_FLAG_RING_CLAMPED);
+                    ring_l = (int)min(rl, (uint32_t)a.ring_w);
+                    ring_p = (int)(rp % (uint32_t)a.ring_w);
+                }
                 // visible key tiles in order: (j - jb) | 0x8000 when the mask applies
                 int n = 0;
                 for (int base = un.jb; base < un.je; base += 32) {
                     const int j = base + lane;
-                    const int code = j < un.je ? tile_code(a, un.cg, j) : 0;
+                    const int code =
+                        j < un.je ? (RING ? ring_tile_code(a, j, ring_l, ring_p) : tile_code(a, un.cg, j)) : 0;
                     const unsigned vis = __ballot_sync(0xffffffffu, code != 0);
                     if (code)
                         list[n + __popc(vis & ((1u << lane) - 1u))] =
@@ -482,11 +526,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(list_full(b));
                 auto tile_at = [&](int v) { return un.jb + (list[v] & 0x7fff); };
-                if (lane == 0) {
-                    // f32 Q tile first (consumed by the softmax warps): [128 rows][32 f32]
-                    // boxes, completing on this CTA's own barrier
-                    for (int qs = 0; qs < (n > 0 ? q_pos : 0) && ok; ++qs) {
-                        if (!(ok = wt.wait(empty(stage), (round & 1) ^ 1))) break;
+                // Every lane walks the ring positions; lane 0 waits for a free slot and
+                // issues the TMA loads, and the whole warp fills the current-rows tile of a
+                // ring-direct verify.
+                auto slot_free = [&]() -> bool {
+                    bool w = true;
+                    if (lane == 0) w = wt.wait(empty(stage), (round & 1) ^ 1);
+                    return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+                };
+                // f32 Q tile first (consumed by the softmax warps): [128 rows][32 f32]
+                // boxes, completing on this CTA's own barrier
+                for (int qs = 0; qs < (n > 0 ? q_pos : 0) && ok; ++qs) {
+                    if (!(ok = slot_free())) break;
+                    if (lane == 0) {
                         const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
                         tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
 #pragma unroll
@@ -494,29 +546,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc::tma_load_3d(dst + bx * 16384, &tmq, full(stage), qs * 64 + bx * 32,
                                             a.q_rows_dim1 ? un.q_row0 : un.q_head0,
                                             a.q_rows_dim1 ? un.q_head0 : un.q_row0);
-                        next();
                     }
-                    // one stage of K or V: two boxes of [BN rows][64 columns] from column d0
-                    auto load = [&](int j, bool is_v, int d0) -> bool {
-                        if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
-                        const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
+                    next();
+                }
+                // the current rows of a ring-direct verify as one key tile: rows < ring_r
+                // from f32 (rounded to bf16), the rest zero; two [128 rows][64 columns]
+                // boxes from column d0, 128-byte swizzle
+                auto fill_current = [&](uint8_t *dst, bool is_v, int d0) {
+                    const float *src = (is_v ? a.cur_v : a.cur_k) +
+                                       ((int64_t)un.t.lane * a.ring_r * a.n_kv_heads + un.t.kh) * D + d0;
+                    for (int q = lane; q < BN * 16; q += 32) {
+                        const int row = q >> 4, c = (q >> 3) & 1, ch = q & 7;
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (row < a.ring_r) {
+                            const float *p = src + (int64_t)row * a.n_kv_heads * D + c * 64 + ch * 8;
+                            const float4 x0 = ld_nc_f4(p), x1 = ld_nc_f4(p + 4);
+                            v = make_uint4(pack2(KV{}, x0.x, x0.y), pack2(KV{}, x0.z, x0.w),
+                                           pack2(KV{}, x1.x, x1.y), pack2(KV{}, x1.z, x1.w));
+                        }
+                        *reinterpret_cast<uint4 *>(dst + c * 16384 + sw128(row, ch)) = v;
+                    }
+                };
+                // one stage of K or V: two boxes of [BN rows][64 columns] from column d0
+                auto load = [&](int j, bool is_v, int d0) -> bool {
+                    if (!slot_free()) return false;
+                    const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
+                    if (RING && j == 0) {
+                        fill_current(smem + L::kStages + stage * kStageBytes, is_v, d0);
+                        tc::fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(full(stage));
+                    } else if (lane == 0) {
                         tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
                         const int rows_dim1 = is_v ? a.v_rows_dim1 : a.k_rows_dim1;
-                        const int c1 = rows_dim1 ? j * BN : un.head_idx;
-                        const int c2 = rows_dim1 ? un.head_idx : j * BN;
+                        const int kr = (RING ? j - 1 : j) * BN;
+                        const int c1 = rows_dim1 ? kr : un.head_idx;
+                        const int c2 = rows_dim1 ? un.head_idx : kr;
 #pragma unroll
                         for (int c = 0; c < 2; ++c)
                             tc::tma_load_3d(dst + c * (BN * 128), is_v ? (const void *)&tmv : (const void *)&tmk,
                                             full(stage), d0 + c * 64, c1, c2);
-                        next();
-                        return true;
-                    };
-                    // PAIR: one stage of this CTA's half of a tile, counted on the even CTA's
-                    // full barrier (which expects both halves): K = keys [64 rank, +64) of
-                    // the tile, columns [d0, d0 + 256); V = all 128 keys, output columns
-                    // [d_off + 128 rank, +128)
-                    auto load_half = [&](int j, bool is_v, int d0) -> bool {
-                        if (!wt.wait(empty(stage), (round & 1) ^ 1)) return false;
+                    }
+                    next();
+                    return true;
+                };
+                // PAIR: one stage of this CTA's half of a tile, counted on the even CTA's
+                // full barrier (which expects both halves): K = keys [64 rank, +64) of the
+                // tile, columns [d0, d0 + 256); V = all 128 keys, output columns
+                // [d_off + 128 rank, +128)
+                auto load_half = [&](int j, bool is_v, int d0) -> bool {
+                    if (!slot_free()) return false;
+                    if (lane == 0) {
                         const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
                         if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), 2 * kStageBytes);
                         const uint32_t fb = tc::mapa_shared(full(stage), 0);
@@ -535,27 +615,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int c = 0; c < 4; ++c)
                                 tc::tma_load_3d_pair(dst + c * (BN / 2 * 128), &tmk, fb, d0 + c * 64, c1, c2);
                         }
-                        next();
-                        return true;
-                    };
-                    // the MMA issuer consumes K of tile v+1 before V of tile v: K0, K1, V0, K2, V1, ...
-                    if constexpr (PAIR) {
-                        for (int ks = 0; ks < KST && ok && n > 0; ++ks) ok = load_half(tile_at(0), false, ks * 256);
-                        for (int v = 0; ok && v < n; ++v) {
-                            for (int ks = 0; ks < KST && ok && v + 1 < n; ++ks)
-                                ok = load_half(tile_at(v + 1), false, ks * 256);
-                            if (ok) ok = load_half(tile_at(v), true, 0);
-                        }
-                    } else {
-                        for (int ks = 0; ks < KSUB && ok && n > 0; ++ks) ok = load(tile_at(0), false, ks * 128);
-                        for (int v = 0; ok && v < n; ++v) {
-                            for (int ks = 0; ks < KSUB && ok && v + 1 < n; ++ks)
-                                ok = load(tile_at(v + 1), false, ks * 128);
-                            for (int vs = 0; vs < VSUB && ok; ++vs) ok = load(tile_at(v), true, un.d_off + vs * 128);
-                        }
+                    }
+                    next();
+                    return true;
+                };
+                // the MMA issuer consumes K of tile v+1 before V of tile v: K0, K1, V0, K2, V1, ...
+                if constexpr (PAIR) {
+                    for (int ks = 0; ks < KST && ok && n > 0; ++ks) ok = load_half(tile_at(0), false, ks * 256);
+                    for (int v = 0; ok && v < n; ++v) {
+                        for (int ks = 0; ks < KST && ok && v + 1 < n; ++ks)
+                            ok = load_half(tile_at(v + 1), false, ks * 256);
+                        if (ok) ok = load_half(tile_at(v), true, 0);
+                    }
+                } else {
+                    for (int ks = 0; ks < KSUB && ok && n > 0; ++ks) ok = load(tile_at(0), false, ks * 128);
+                    for (int v = 0; ok && v < n; ++v) {
+                        for (int ks = 0; ks < KSUB && ok && v + 1 < n; ++ks)
+                            ok = load(tile_at(v + 1), false, ks * 128);
+                        for (int vs = 0; vs < VSUB && ok; ++vs) ok = load(tile_at(v), true, un.d_off + vs * 128);
                     }
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
             }
         } else if (warp == kMmaWarp) {
             // ------------------------------------------------------------ MMA issuer
@@ -818,34 +897,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     put_q(cb, w);
                 }
             } else {
-                // f32 Q without TMA: each thread reads its half of its own row
-#pragma unroll 1
+                // f32 Q without TMA: each thread reads its half of its own row, every load
+                // in flight at once, then converts and stores the blocks
+                float4 x[D / 64][8];
+#pragma unroll
+                for (int cb = 0; cb < D / 64; ++cb)
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        x[cb][v] = valid ? ld_nc_f4(static_cast<const float *>(a.q) + un.t.lane * a.q_lane +
+                                                    (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64 +
+                                                    h * 32 + v * 4)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
                 for (int cb = 0; cb < D / 64; ++cb) {
                     uint32_t w[16];
-                    if (valid && a.q_f32) {
-                        const float *src = static_cast<const float *>(a.q) + un.t.lane * a.q_lane +
-                                           (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64 + h * 32;
 #pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            const float4 x = ld_nc_f4(src + v * 4);
-                            w[2 * v] = pack2(KV{}, x.x, x.y);
-                            w[2 * v + 1] = pack2(KV{}, x.z, x.w);
-                        }
-                    } else if (valid) {
-                        const uint16_t *src = static_cast<const uint16_t *>(a.q) + un.t.lane * a.q_lane +
-                                              (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64 +
-                                              h * 32;
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const uint4 x = ld_nc_v4(src + v * 8);
-                            w[4 * v] = x.x;
-                            w[4 * v + 1] = x.y;
-                            w[4 * v + 2] = x.z;
-                            w[4 * v + 3] = x.w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int v = 0; v < 16; ++v) w[v] = 0u;
+                    for (int v = 0; v < 8; ++v) {
+                        w[2 * v] = pack2(KV{}, x[cb][v].x, x[cb][v].y);
+                        w[2 * v + 1] = pack2(KV{}, x[cb][v].z, x[cb][v].w);
                     }
                     put_q(cb, w);
                 }
@@ -882,6 +951,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                (int64_t)row * a.m_row + h * 64
                                          : nullptr;
             const bool m_vec = valid && (reinterpret_cast<uintptr_t>(mrow) & 15) == 0;
+            // ring-direct verify: ring slot s is visible to this draft row when its history
+            // index (wp - 1 - s) mod w is below min(L, w - 1 - row)
+            int ring_p = 0, ring_lim = 0;
+            if constexpr (RING) {
+                const int rl = (int)min(a.ring_len[cur.t.lane], (uint32_t)a.ring_w);
+                ring_p = (int)(a.ring_wp[cur.t.lane] % (uint32_t)a.ring_w);
+                ring_lim = min(rl, a.ring_w - 1 - row);
+            }
             float m_ref = kNegInf, l = 0.f;
             int n_done = 0;  // tiles whose P this thread has handed to the MMA issuer
             // ---- key tiles: this thread owns columns [h*64, h*64 + 64) of every tile.
@@ -918,6 +995,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // no mask: s stays unscaled; the scale is applied inside the exponent
                         // argument below, and the row maximum is taken on the raw scores
                         sc = scale_log2;
+                    } else if constexpr (RING) {
+                        if (j == 0) {
+                            // the current rows, then padding
+#pragma unroll
+                            for (int c = 0; c < 64; ++c)
+                                s[c] = (h * 64 + c < a.ring_r) ? s[c] * scale_log2 : kNegInf;
+                        } else {
+                            const int s0 = (j - 1) * BN + h * 64;  // ring slot of s[0]
+#pragma unroll
+                            for (int c = 0; c < 64; ++c) {
+                                int jj = ring_p - 1 - (s0 + c);
+                                jj += jj < 0 ? a.ring_w : 0;
+                                s[c] = (s0 + c < a.ring_w && jj < ring_lim) ? s[c] * scale_log2 : kNegInf;
+                            }
+                        }
                     } else {
                         const int c0 = j * BN + h * 64;  // key index of s[0]
                         const uint16_t *mt = mrow + j * BN;
@@ -1354,10 +1446,10 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
     return r == CUDA_SUCCESS;
 }
 
-template <int D, class KV, bool PAIR>
+template <int D, class KV, bool PAIR, bool RING = false>
 cudaError_t run_attn(const AttnArgs &a, const CUtensorMap *maps, int units, int tiles,
                      cudaStream_t stream) {
-    auto kern = attn_kernel<D, KV, PAIR>;
+    auto kern = attn_kernel<D, KV, PAIR, RING>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1426,9 +1518,18 @@ size_t verify_workspace_bytes(const gqa_ring_params &p) {
                                 (int)p.head_dim, (int)p.packed_len, false));
 }
 
+// key space of a ring-direct verify: one tile of current rows, then the ring slots
+int ring_keys(int window) { return BN + window; }
+
+size_t verify_ring_workspace_bytes(const gqa_ring_params &p) {
+    return plan_bytes(make_plan((int)p.lanes, (int)p.rows, (int)p.q_heads, (int)p.kv_heads,
+                                (int)p.head_dim, ring_keys((int)p.window), false));
+}
+
 cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t stream) {
-    const bool shared = p.mask_head_stride == 0;
-    const Plan pl = make_plan(p.lanes, p.rows, p.n_heads, p.n_kv_heads, p.head_dim, p.n_keys, shared);
+    const bool shared = !p.ring && p.mask_head_stride == 0;
+    const int n_keys = p.ring ? ring_keys(p.ring_w) : p.n_keys;
+    const Plan pl = make_plan(p.lanes, p.rows, p.n_heads, p.n_kv_heads, p.head_dim, n_keys, shared);
     AttnArgs a{};
     a.q = p.q;
     a.q_f32 = p.q_is_f32 ? 1 : 0;
@@ -1450,7 +1551,14 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     a.n_heads = p.n_heads;
     a.n_kv_heads = p.n_kv_heads;
     a.group = p.n_heads / p.n_kv_heads;
-    a.n_keys = p.n_keys;
+    a.n_keys = n_keys;
+    a.ring = p.ring ? 1 : 0;
+    a.ring_w = p.ring_w;
+    a.ring_r = p.rows;
+    a.cur_k = p.cur_k;
+    a.cur_v = p.cur_v;
+    a.ring_len = p.ring_len;
+    a.ring_wp = p.ring_wp;
     a.rows_per_head = pl.rows_per_head;
     a.heads_per_tile = pl.heads_per_tile;
     a.row_tiles = pl.row_tiles;
@@ -1498,9 +1606,12 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
         a.o_rows_dim1 = rows_first(p.n_heads, p.o_row_stride, p.o_head_stride) ? 1 : 0;
     }
 
-    classify_kernel<<<dim3(pl.code_groups, pl.code_cols), BM, 0, stream>>>(a, const_cast<uint8_t *>(a.codes));
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    // ring-direct verify classifies its tiles from the history length and write position
+    if (!p.ring) {
+        classify_kernel<<<dim3(pl.code_groups, pl.code_cols), BM, 0, stream>>>(a, const_cast<uint8_t *>(a.codes));
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     // persistent launch: one CTA (or CTA pair) per SM (or SM pair) at most; each runs
     // the units of its slot back to back
     const int units = pl.tiles * pl.d_parts * pl.splits;  // query tiles x output halves x key splits
@@ -1508,6 +1619,13 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     if (sms <= 0) sms = 148;
     const int ctas = pl.pair ? 2 * std::min(units / 2, sms / 2) : std::min(units, sms);
     const bool bf = a.kv_bf16;
+    if (p.ring) {
+        // ring-direct verify: bf16 rings, head_dim 128 or 256, unpaired
+        if (!bf || pl.pair) return cudaErrorInvalidValue;
+        if (p.head_dim == 128) return run_attn<128, BF16, false, true>(a, maps, ctas, pl.tiles, stream);
+        if (p.head_dim == 256) return run_attn<256, BF16, false, true>(a, maps, ctas, pl.tiles, stream);
+        return cudaErrorInvalidValue;
+    }
     switch (p.head_dim) {
         case 128:
             return bf ? run_attn<128, BF16, false>(a, maps, ctas, pl.tiles, stream)

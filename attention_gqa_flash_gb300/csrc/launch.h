@@ -48,9 +48,15 @@ struct AttnProblem {
     int lanes, rows, n_heads, n_kv_heads, head_dim, n_keys;
     float scale;
     int32_t *status;
+    // ring-direct verify (k, v are the rings; no mask): key tile 0 = the current rows
+    bool ring;
+    int ring_w;
+    const float *cur_k, *cur_v;
+    const uint32_t *ring_len, *ring_wp;
 };
 size_t prefill_workspace_bytes(int rows, int n_heads, int n_kv_heads, int head_dim, int kv_pad);
 size_t verify_workspace_bytes(const gqa_ring_params &p);
+size_t verify_ring_workspace_bytes(const gqa_ring_params &p);
 cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t stream);
 void set_attention_pairs(int mode);
 cudaError_t launch_bounded_wait_selftest(int32_t *status, int timeout_ms, cudaStream_t stream);

@@ -266,6 +266,33 @@ int gqa_attn_verify(const uint16_t *packed_q, size_t packed_q_bytes, const uint1
                     const gqa_ring_params *p, float scale, void *workspace,
                     size_t workspace_bytes, int32_t *status, gqa_stream_t stream);
 
+size_t gqa_attn_verify_ring_workspace_size(const gqa_ring_params *p);
+
+/*
+ * Fused ring-direct verify attention (mlx-native 0.21.1 dflash2_attention_pack.rs:
+ * the pack and mask dispatchers and the verify attention taken together).  The
+ * same result as gqa_pack_attention -> gqa_fill_mask -> gqa_attn_verify, read
+ * straight from the ring: the keys of draft row r of lane b are the r current
+ * rows (bf16 of cur_k / cur_v, all visible) and every ring slot s whose
+ * history index j = (write_position - 1 - s) mod w satisfies
+ * j < min(cache_length, w) and r + j + 1 < w; the query is bf16(cur_q).  No
+ * packed copy and no mask tensor is made; the counters are read on the device.
+ *   ring_k, ring_v   bf16 [b][hk][w][d]
+ *   cur_q            f32  [b][r][h][d];  cur_k, cur_v f32 [b][r][hk][d]
+ *   cache_lengths, write_positions  u32 [b] (device)
+ *   o                f32  [b][r][h][d]
+ * Every buffer contiguous with the exact size, rings and current rows 16-byte
+ * aligned; workspace as gqa_attn_verify_ring_workspace_size (256-byte aligned).
+ */
+int gqa_attn_verify_ring(const uint16_t *ring_k, size_t ring_k_bytes, const uint16_t *ring_v,
+                         size_t ring_v_bytes, const float *cur_q, size_t cur_q_bytes,
+                         const float *cur_k, size_t cur_k_bytes, const float *cur_v,
+                         size_t cur_v_bytes, const uint32_t *cache_lengths,
+                         size_t cache_lengths_bytes, const uint32_t *write_positions,
+                         size_t write_positions_bytes, float *o, size_t o_bytes,
+                         const gqa_ring_params *p, float scale, void *workspace,
+                         size_t workspace_bytes, int32_t *status, gqa_stream_t stream);
+
 /*
  * Commit accepted rows: for i < min(commit_counts[b], max_commit),
  * ring slot (write_positions[b] + i) mod w of lane b receives bf16(new row i)
