@@ -284,6 +284,14 @@ def setup_verify(torch, g, c):
         for f in ops.values():
             f()
 
+    fused_out = torch.empty((B, R, H, D), dtype=torch.float32, device="cuda")
+    fws = torch.empty(max(1, g.gqa_attn_verify_ring_workspace_size(c.geom)), dtype=torch.uint8,
+                      device="cuda")
+    fused = {
+        "attn": lambda: g.gqa_attn_verify_ring(rk, rv, cq, ck, cv, lens, pos, c.geom, c.scale,
+                                               out=fused_out, workspace=fws),
+        "commit": ops["commit"],
+    }
     hist = int(sum(min(int(x), W - 1) for x in c.cache_lengths))
     n_commit = int(sum(min(int(x), MC) for x in c.commit_counts))
     nb = lambda t: t.numel() * t.element_size()
@@ -293,7 +301,11 @@ def setup_verify(torch, g, c):
         "attn": nb(pq) + nb(pk) + nb(pv) + nb(mask) + nb(out),
         "commit": n_commit * HK * D * (4 + 2) * 2,
     }
-    return step, ops, {"bytes": by, "launches": 1 + 1 + 2 + 1}
+    # fused: the visible history once, the current rows, O
+    fby = {"attn": hist * HK * D * 2 * 2 + nb(cq) + nb(ck) + nb(cv) + nb(out),
+           "commit": by["commit"]}
+    return step, ops, {"bytes": by, "launches": 1 + 1 + 2 + 1, "fused": fused,
+                       "fused_bytes": fby, "fused_launches": 1 + 1 + 1}
 
 
 # ---------------------------------------------------------------------------
@@ -512,8 +524,27 @@ def main() -> None:
                                  "unit": "GB/s", "ms_per_step": t, "bytes_per_step": total,
                                  "peak": hbm_peak, "frac": total / (t * 1e-3) / 1e9 / hbm_peak,
                                  "kernels": kernels}
+        # the same verify step with the fused ring-direct attention (no pack, no mask)
+        fops, fby = iv["fused"], iv["fused_bytes"]
+
+        def fstep():
+            for f in fops.values():
+                f()
+        ms = tm.steps(fstep, max(5, args.steps // 2), args.warmup)
+        t = tm.max_over_ranks(sum(ms) / len(ms))
+        ftotal = sum(fby.values())
+        fkernels = {}
+        for name, f in fops.items():
+            k = tm.kernel_ms(g, f, 5)
+            fkernels[name] = {"bytes": fby[name], "kernel_ms": k,
+                              "achieved_gbs": fby[name] / (k * 1e-3) / 1e9,
+                              "frac": fby[name] / (k * 1e-3) / 1e9 / hbm_peak}
+        paths["verify_fused"] = {"workload": vc.name, "value": world * ftotal / (t * 1e-3) / 1e9,
+                                 "unit": "GB/s", "ms_per_step": t, "bytes_per_step": ftotal,
+                                 "peak": hbm_peak, "frac": ftotal / (t * 1e-3) / 1e9 / hbm_peak,
+                                 "kernels": fkernels}
         line["paths"] = paths
-        line["gpu_launches"] += (2 + 2 + iv["launches"]) * max(5, args.steps // 2)
+        line["gpu_launches"] += (2 + 2 + iv["launches"] + iv["fused_launches"]) * max(5, args.steps // 2)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(head)
