@@ -64,6 +64,14 @@ def _load():
                 getattr(lib, name).restype = i32
             lib.orc_pack_attention.argtypes = [vp] * 11
             lib.orc_fill_mask.argtypes = [vp, vp, vp]
+            lib.orc_f32_to_f16.restype = ctypes.c_uint16
+            lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
+            lib.orc_paged_append.restype = i32
+            lib.orc_paged_append.argtypes = [vp, vp, vp, vp, vp, i64, vp, vp, i32, i64, i64, i64,
+                                             i32, i32, i32, i32, i64, vp]
+            lib.orc_paged_prefill.restype = i32
+            lib.orc_paged_prefill.argtypes = [vp, vp, vp, i32, i64, i64, i64, vp, i64, vp, vp,
+                                              i32, i32, i32, i32, i32, i64, dbl, vp]
             lib.orc_verify_ring_attention.restype = i32
             lib.orc_verify_ring_attention.argtypes = [vp] * 8 + [dbl, vp]
             lib.orc_commit_kv.argtypes = [vp] * 7
@@ -289,6 +297,54 @@ def verify_ring_attention(ring_k, ring_v, cur_q, cur_k, cur_v, cache_lengths, wr
                                            _ptr(out))
     if rc != 0:
         raise ValueError("invalid ring geometry" if rc == 1 else "out of memory")
+    return out
+
+
+def f32_to_f16(x) -> int:
+    """IEEE binary16 bits of float32 x, round to nearest even (the oracle's own rounding)."""
+    return int(_load().orc_f32_to_f16(float(np.float32(x))))
+
+
+def paged_append(k_new, v_new, token_offsets, position_start, page_table, k_pool, v_pool, *,
+                 kv_dtype: str, page_stride: int, token_stride: int, head_stride: int,
+                 page_size: int):
+    """Returns (k_pool', v_pool', skipped): copies of the pools (float16, or uint16 bf16
+    bits; the result has the input's dtype) with every new token's K / V row rounded
+    into its page slot."""
+    kn, vn = _c(k_new, np.float32), _c(v_new, np.float32)
+    offs, ps, pt = _c(token_offsets, np.int32), _c(position_start, np.int32), _c(page_table, np.int32)
+    in_dtype = np.asarray(k_pool).dtype
+    kp = np.array(np.ascontiguousarray(_bits16(np.asarray(k_pool))), copy=True)
+    vp_ = np.array(np.ascontiguousarray(_bits16(np.asarray(v_pool))), copy=True)
+    S = offs.size - 1
+    T, HK, D = kn.shape
+    num_pages = kp.size // page_stride
+    skipped = np.zeros(1, np.int64)
+    rc = _load().orc_paged_append(_ptr(kn), _ptr(vn), _ptr(offs), _ptr(ps), _ptr(pt),
+                                  pt.shape[1], _ptr(kp), _ptr(vp_), _DTYPES[kv_dtype],
+                                  page_stride, token_stride, head_stride, S, HK, D, page_size,
+                                  num_pages, _ptr(skipped))
+    if rc != 0:
+        raise ValueError("invalid paged append arguments")
+    return kp.view(in_dtype), vp_.view(in_dtype), int(skipped[0])
+
+
+def paged_prefill(q, k_pool, v_pool, page_table, token_offsets, position_start, *,
+                  kv_dtype: str, page_stride: int, token_stride: int, head_stride: int,
+                  n_kv_heads: int, page_size: int, scale: float) -> np.ndarray:
+    """Chunked prefill over pages: float64 [tokens, n_heads, head_dim]."""
+    qq = _c(q, np.float32)
+    T, H, D = qq.shape
+    kp = np.ascontiguousarray(_bits16(np.asarray(k_pool)))
+    vp_ = np.ascontiguousarray(_bits16(np.asarray(v_pool)))
+    pt, offs, ps = _c(page_table, np.int32), _c(token_offsets, np.int32), _c(position_start, np.int32)
+    out = np.zeros((T, H, D), np.float64)
+    rc = _load().orc_paged_prefill(_ptr(qq), _ptr(kp), _ptr(vp_), _DTYPES[kv_dtype], page_stride,
+                                   token_stride, head_stride, _ptr(pt), pt.shape[1], _ptr(offs),
+                                   _ptr(ps), offs.size - 1, H, n_kv_heads, D, page_size,
+                                   kp.size // page_stride, float(scale), _ptr(out))
+    if rc != 0:
+        raise ValueError("invalid paged prefill arguments")
     return out
 
 

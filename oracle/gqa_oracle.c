@@ -85,6 +85,47 @@ uint16_t orc_f32_to_bf16(float x)
     return (uint16_t)keep;
 }
 
+/* float32 -> IEEE 754 binary16, round to nearest, ties to even, from the
+ * format's definition: 1 sign, 5 exponent (bias 15), 10 fraction bits;
+ * subnormals below 2^-14, overflow to infinity, NaN kept quiet. */
+uint16_t orc_f32_to_f16(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    const uint32_t sign = (u >> 16) & 0x8000u;
+    const uint32_t mag = u & 0x7fffffffu;
+    if (mag > 0x7f800000u)
+        return (uint16_t)(sign | 0x7e00u);
+    if (mag == 0x7f800000u)
+        return (uint16_t)(sign | 0x7c00u);
+    const int e = (int)(mag >> 23) - 127;           /* unbiased exponent */
+    uint32_t m = (mag & 0x7fffffu) | (mag ? 0x800000u : 0u);  /* 24-bit significand */
+    if (mag == 0)
+        return (uint16_t)sign;
+    /* value = m * 2^(e - 23); the f16 unit in the last place is 2^(max(e, -14) - 10) */
+    const int shift = (e < -14 ? -14 : e) - 10 - (e - 23);     /* bits dropped from m */
+    uint32_t q;
+    if (shift >= 32) {
+        q = 0;
+    } else {
+        q = m >> shift;
+        const uint32_t rem = m & ((1u << shift) - 1u), half = 1u << (shift - 1);
+        if (rem > half || (rem == half && (q & 1u)))
+            q += 1;
+    }
+    /* q counts units of 2^(max(e,-14) - 10); rebuild the bit pattern */
+    int be = (e < -14 ? -14 : e);
+    if (q >= 0x800u) {          /* rounding carried into the next binade */
+        q >>= 1;
+        be += 1;
+    }
+    if (q < 0x400u)             /* subnormal (be == -14) */
+        return (uint16_t)(sign | q);
+    if (be > 15)
+        return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | ((uint32_t)(be + 15) << 10) | (q & 0x3ffu));
+}
+
 static double load_q(const void *q, int q_dtype, int64_t idx)
 {
     if (q_dtype == ORC_F32)
@@ -415,6 +456,124 @@ int orc_commit_kv(const float *new_k, const float *new_v, const uint32_t *commit
         }
     }
     return 0;
+}
+
+/*
+ * Page append [PA, paged_state_regions and validate_signature; the prepare
+ * step writes each new token's K and V into its page before attention]: token
+ * i of the batch belongs to the sequence s with token_offsets[s] <= i <
+ * token_offsets[s+1] and sits at position p = position_start[s] + (i -
+ * token_offsets[s]); its K row (kv head g, element e) is rounded to nearest
+ * even into the pool type and stored at
+ *     pool[page*page_stride + (p % page_size)*token_stride + g*head_stride + e],
+ * page = page_table[s*max_pages_per_seq + p / page_size].  A token whose page
+ * entry lies outside the table or the pool is not written; the count of such
+ * tokens is returned in *skipped.
+ */
+int orc_paged_append(const float *k_new, const float *v_new, const int32_t *token_offsets,
+                     const int32_t *position_start, const int32_t *page_table,
+                     int64_t max_pages_per_seq, uint16_t *k_pool, uint16_t *v_pool, int kv_dtype,
+                     int64_t page_stride, int64_t token_stride, int64_t head_stride, int num_seqs,
+                     int n_kv_heads, int head_dim, int page_size, int64_t num_pages,
+                     int64_t *skipped)
+{
+    if (num_seqs <= 0 || n_kv_heads <= 0 || head_dim <= 0 || page_size <= 0 ||
+        !(kv_dtype == ORC_F16 || kv_dtype == ORC_BF16))
+        return 1;
+    int64_t skip = 0;
+    for (int s = 0; s < num_seqs; ++s)
+        for (int64_t i = token_offsets[s]; i < token_offsets[s + 1]; ++i) {
+            const int64_t p = (int64_t)position_start[s] + (i - token_offsets[s]);
+            const int64_t slot_page = p / page_size;
+            if (p < 0 || slot_page >= max_pages_per_seq) {
+                ++skip;
+                continue;
+            }
+            const int32_t page = page_table[(int64_t)s * max_pages_per_seq + slot_page];
+            if (page < 0 || page >= num_pages) {
+                ++skip;
+                continue;
+            }
+            for (int g = 0; g < n_kv_heads; ++g)
+                for (int e = 0; e < head_dim; ++e) {
+                    const int64_t dst = page * page_stride + (p % page_size) * token_stride +
+                                        g * head_stride + e;
+                    const int64_t src = (i * n_kv_heads + g) * head_dim + e;
+                    k_pool[dst] = kv_dtype == ORC_F16 ? orc_f32_to_f16(k_new[src])
+                                                      : orc_f32_to_bf16(k_new[src]);
+                    v_pool[dst] = kv_dtype == ORC_F16 ? orc_f32_to_f16(v_new[src])
+                                                      : orc_f32_to_bf16(v_new[src]);
+                }
+        }
+    *skipped = skip;
+    return 0;
+}
+
+/*
+ * Paged multi-token (chunked) prefill [PA, the causal attention of `tokens`
+ * new queries at position_start over the paged state]: query token i of
+ * sequence s (position p as for the append above) and query head h attend to
+ * the keys at positions 0..p of their sequence, gathered from the pages as in
+ * paged decode: out[i][h] = sum_t softmax_t(scale q.k_t) v_t.  q f32
+ * [tokens][n_heads][head_dim] (widened exactly); out double, same layout.
+ */
+int orc_paged_prefill(const float *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                      int kv_dtype, int64_t page_stride, int64_t token_stride,
+                      int64_t head_stride, const int32_t *page_table, int64_t max_pages_per_seq,
+                      const int32_t *token_offsets, const int32_t *position_start, int num_seqs,
+                      int n_heads, int n_kv_heads, int head_dim, int page_size,
+                      int64_t num_pages, double scale, double *out)
+{
+    if (num_seqs <= 0 || n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0 ||
+        head_dim <= 0 || page_size <= 0)
+        return 1;
+    const int group = n_heads / n_kv_heads;
+    const int64_t total = token_offsets[num_seqs];
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+    for (int64_t i = 0; i < total; ++i)
+        for (int h = 0; h < n_heads; ++h) {
+            int s = 0;
+            while (s + 1 < num_seqs && token_offsets[s + 1] <= i)
+                ++s;
+            const int64_t p = (int64_t)position_start[s] + (i - token_offsets[s]);
+            const int64_t n = p + 1;
+            if (p < 0 || (n + page_size - 1) / page_size > max_pages_per_seq) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            const int kh = h / group;
+            const uint16_t **kr = (const uint16_t **)malloc(sizeof(void *) * (size_t)n);
+            const uint16_t **vr = (const uint16_t **)malloc(sizeof(void *) * (size_t)n);
+            double *sc = (double *)malloc(sizeof(double) * (size_t)n);
+            double *qrow = (double *)malloc(sizeof(double) * (size_t)head_dim);
+            int ok = kr && vr && sc && qrow;
+            for (int64_t t = 0; ok && t < n; ++t) {
+                const int32_t page = page_table[(int64_t)s * max_pages_per_seq + t / page_size];
+                if (page < 0 || page >= num_pages) {
+                    ok = 0;
+                    break;
+                }
+                const int64_t off = page * page_stride + (t % page_size) * token_stride + kh * head_stride;
+                kr[t] = k_pool + off;
+                vr[t] = v_pool + off;
+            }
+            if (!ok) {
+#pragma omp atomic write
+                bad = 1;
+            } else {
+                for (int e = 0; e < head_dim; ++e)
+                    qrow[e] = (double)q[(i * n_heads + h) * head_dim + e];
+                attention_row(qrow, head_dim, kr, vr, kv_dtype, (int)n, NULL, scale, sc,
+                              out + (i * n_heads + h) * head_dim);
+            }
+            free(kr);
+            free(vr);
+            free(sc);
+            free(qrow);
+        }
+    return bad ? 2 : 0;
 }
 
 /*

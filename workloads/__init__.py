@@ -236,6 +236,91 @@ def paged_decode(*, num_seqs: int = 64, ctx_lo: int = 512, ctx_hi: int = 16384,
 
 
 # ---------------------------------------------------------------------------
+# paged chunked prefill and page append
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass
+class PagedChunkCase:
+    name: str
+    num_seqs: int
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    page_size: int
+    num_pages: int
+    max_pages_per_seq: int
+    scale: float
+    kv_dtype: str
+    q: np.ndarray               # f32 [tokens, n_heads, head_dim]
+    k_new: np.ndarray           # f32 [tokens, n_kv_heads, head_dim]: the new tokens' K / V
+    v_new: np.ndarray
+    k_pool: np.ndarray          # [num_pages, page_size, n_kv_heads, head_dim]: the prefix
+    v_pool: np.ndarray          #   written, the new tokens' slots and unused pages NaN
+    page_table: np.ndarray      # int32 [num_seqs, max_pages_per_seq], -1 where unused
+    token_offsets: np.ndarray   # int32 [num_seqs + 1]
+    position_start: np.ndarray  # int32 [num_seqs]
+
+    @property
+    def tokens(self) -> int:
+        return int(self.token_offsets[-1])
+
+    def flops(self) -> float:
+        """4 h d per (query, visible key): query j of sequence s sees position_start + j + 1 keys."""
+        n = 0
+        for s in range(self.num_seqs):
+            t = int(self.token_offsets[s + 1] - self.token_offsets[s])
+            n += t * int(self.position_start[s]) + t * (t + 1) // 2
+        return 4.0 * self.n_heads * self.head_dim * n
+
+
+def paged_chunk(*, num_seqs: int = 4, tokens_lo: int = 1, tokens_hi: int = 64,
+                prefix_lo: int = 0, prefix_hi: int = 300, num_pages: int = 256,
+                page_size: int = 16, n_heads: int = 8, n_kv_heads: int = 2, head_dim: int = 128,
+                kv_dtype: str = "f16", scale: float | None = None, seed: int = 0,
+                name: str | None = None) -> PagedChunkCase:
+    """tokens ~ U{tokens_lo..tokens_hi}, position_start ~ U{prefix_lo..prefix_hi} per
+    sequence; pages taken in order from a random permutation of the pool; the prefix's K/V
+    ~ N(0,1) in the pool, the new tokens' K/V ~ N(0,1) f32 (to be appended) and their slots,
+    the unused pages and page tails NaN; Q ~ N(0,1) f32."""
+    rng = np.random.default_rng(seed)
+    toks = rng.integers(tokens_lo, tokens_hi, size=num_seqs, endpoint=True).astype(np.int32)
+    ps = rng.integers(prefix_lo, prefix_hi, size=num_seqs, endpoint=True).astype(np.int32)
+    ctx = (ps + toks).astype(np.int64)
+    need = -(-ctx // page_size)
+    max_pages = int(need.max())
+    if need.sum() > num_pages:
+        raise ValueError("pool too small")
+    perm = rng.permutation(num_pages).astype(np.int32)
+    table = np.full((num_seqs, max_pages), -1, np.int32)
+    pos = 0
+    for s in range(num_seqs):
+        table[s, :need[s]] = perm[pos:pos + need[s]]
+        pos += int(need[s])
+    draw = _normal_f16 if kv_dtype == "f16" else _normal_bf16
+    shape = (num_pages, page_size, n_kv_heads, head_dim)
+    k_pool, v_pool = draw(rng, shape), draw(rng, shape)
+    nan = np.float16(np.nan) if kv_dtype == "f16" else np.uint16(0x7fc0)
+    written = np.zeros((num_pages, page_size), bool)
+    for s in range(num_seqs):
+        t = np.arange(int(ps[s]))
+        written[table[s, t // page_size], t % page_size] = True
+    k_pool[~written] = nan
+    v_pool[~written] = nan
+    offs = np.concatenate([[0], np.cumsum(toks)]).astype(np.int32)
+    T = int(offs[-1])
+    q = _normal_f32(rng, (T, n_heads, head_dim))
+    k_new = _normal_f32(rng, (T, n_kv_heads, head_dim))
+    v_new = _normal_f32(rng, (T, n_kv_heads, head_dim))
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+    if name is None:
+        name = (f"paged_chunk_{num_seqs}seq_tok{tokens_lo}-{tokens_hi}_pre{prefix_lo}-{prefix_hi}"
+                f"_h{n_heads}_hk{n_kv_heads}_d{head_dim}")
+    return PagedChunkCase(name, num_seqs, n_heads, n_kv_heads, head_dim, page_size, num_pages,
+                          max_pages, float(scale), kv_dtype, q, k_new, v_new, k_pool, v_pool,
+                          table, offs, ps)
+
+
+# ---------------------------------------------------------------------------
 # DFlash2 ring KV (speculative verify)
 # ---------------------------------------------------------------------------
 @dataclasses.dataclass
