@@ -77,6 +77,12 @@ def library() -> ctypes.CDLL:
             "gqa_attn_paged_decode_noalloc": (i32, [vp, sz, vp, vp, sz, i32, i64, i64, i64, vp, sz,
                                                     i32, vp, sz, vp, sz, i32, i32, i32, i32, i32,
                                                     i32, f32, vp, vp]),
+            "gqa_paged_append": (i32, [vp, vp, sz, vp, sz, vp, sz, vp, sz, i32, vp, vp, sz, i32,
+                                       i64, i64, i64, i32, i32, i32, i32, i32, i32, vp, vp]),
+            "gqa_attn_paged_prefill_workspace_size": (sz, [i32] * 7),
+            "gqa_attn_paged_prefill": (i32, [vp, sz, vp, vp, sz, i32, i64, i64, i64, vp, sz, i32,
+                                             vp, sz, vp, sz, vp, sz, i32, i32, i32, i32, i32, i32,
+                                             i32, i32, f32, vp, sz, vp, vp]),
             "gqa_ring_params_valid": (i32, [rp]),
             "gqa_pack_attention": (i32, [vp, sz] * 10 + [rp, vp, vp]),
             "gqa_fill_mask": (i32, [vp, sz, vp, sz, rp, vp, vp]),
@@ -104,6 +110,7 @@ def exported_symbols() -> list[str]:
             "gqa_attn_prefill_workspace_size", "gqa_attn_prefill",
             "gqa_attn_paged_decode_workspace_size", "gqa_attn_paged_decode",
             "gqa_attn_paged_decode_noalloc",
+            "gqa_paged_append", "gqa_attn_paged_prefill_workspace_size", "gqa_attn_paged_prefill",
             "gqa_ring_params_valid", "gqa_pack_attention", "gqa_fill_mask",
             "gqa_attn_verify_workspace_size", "gqa_attn_verify",
             "gqa_attn_verify_ring_workspace_size", "gqa_attn_verify_ring", "gqa_commit_kv",
@@ -272,6 +279,95 @@ def gqa_attn_paged_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch
         _ptr(context_lens), _nbytes(context_lens), _ptr(out), _nbytes(out),
         num_seqs, n_heads, n_kv, d, page_size, num_pages, float(scale),
         _ptr(workspace), _nbytes(workspace), _ptr(status), _stream(stream)))
+    return out
+
+
+def _pool(k_pages: torch.Tensor, v_pages: torch.Tensor, head_dim: int):
+    _cuda("k_pages", k_pages, tuple(_KV_DTYPES))
+    _cuda("v_pages", v_pages, (k_pages.dtype,))
+    num_pages, page_size, n_kv, d2 = k_pages.shape
+    if v_pages.shape != k_pages.shape or v_pages.stride() != k_pages.stride() or d2 != head_dim:
+        raise ValueError("K and V pools must share shape and strides")
+    if k_pages.stride(3) != 1:
+        raise ValueError("pool head_dim must be contiguous")
+    return num_pages, page_size, n_kv
+
+
+def _seq_arrays(token_offsets, position_start, page_table):
+    for name, t in (("token_offsets", token_offsets), ("position_start", position_start),
+                    ("page_table", page_table)):
+        _cuda(name, t, (torch.int32,))
+        _contig(name, t)
+    num_seqs = position_start.shape[0]
+    if token_offsets.shape != (num_seqs + 1,) or page_table.shape[0] != num_seqs:
+        raise ValueError("token_offsets [num_seqs + 1], position_start [num_seqs], "
+                         "page_table [num_seqs, max_pages]")
+    return num_seqs
+
+
+def gqa_paged_append(k_new: torch.Tensor, v_new: torch.Tensor, token_offsets: torch.Tensor,
+                     position_start: torch.Tensor, page_table: torch.Tensor,
+                     k_pages: torch.Tensor, v_pages: torch.Tensor,
+                     status: torch.Tensor | None = None, stream=None) -> None:
+    """k_new / v_new f32 [total_tokens, n_kv_heads, head_dim] rounded into their page
+    slots of k_pages / v_pages (f16/bf16 [num_pages, page_size, n_kv_heads, head_dim]);
+    token_offsets int32 [num_seqs + 1], position_start int32 [num_seqs], page_table
+    int32 [num_seqs, max_pages_per_seq]."""
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _cuda(name, t, (torch.float32,))
+        _contig(name, t)
+    if v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must have the same shape")
+    total, n_kv, d = k_new.shape
+    num_pages, page_size, n_kv2 = _pool(k_pages, v_pages, d)
+    if n_kv2 != n_kv:
+        raise ValueError("k_new and the pools disagree on n_kv_heads")
+    num_seqs = _seq_arrays(token_offsets, position_start, page_table)
+    _check(library().gqa_paged_append(
+        _ptr(k_new), _ptr(v_new), min(_nbytes(k_new), _nbytes(v_new)),
+        _ptr(token_offsets), _nbytes(token_offsets), _ptr(position_start), _nbytes(position_start),
+        _ptr(page_table), _nbytes(page_table), page_table.shape[1],
+        _ptr(k_pages), _ptr(v_pages), min(_nbytes(k_pages), _nbytes(v_pages)),
+        _KV_DTYPES[k_pages.dtype], k_pages.stride(0), k_pages.stride(1), k_pages.stride(2),
+        num_seqs, total, n_kv, d, page_size, num_pages, _ptr(status), _stream(stream)))
+
+
+def gqa_attn_paged_prefill_workspace_size(num_seqs: int, max_tokens: int, n_heads: int,
+                                          n_kv_heads: int, head_dim: int, max_pages_per_seq: int,
+                                          page_size: int) -> int:
+    return int(library().gqa_attn_paged_prefill_workspace_size(
+        num_seqs, max_tokens, n_heads, n_kv_heads, head_dim, max_pages_per_seq, page_size))
+
+
+def gqa_attn_paged_prefill(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                           page_table: torch.Tensor, token_offsets: torch.Tensor,
+                           position_start: torch.Tensor, max_tokens: int, scale: float,
+                           out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                           status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Chunked prefill over pages: q f32 [total_tokens, n_heads, head_dim]; the pools,
+    page_table, token_offsets and position_start as for gqa_paged_append; max_tokens
+    bounds every sequence's token count.  Returns o f32 like q."""
+    _cuda("q", q, (torch.float32,))
+    _contig("q", q)
+    total, n_heads, d = q.shape
+    num_pages, page_size, n_kv = _pool(k_pages, v_pages, d)
+    num_seqs = _seq_arrays(token_offsets, position_start, page_table)
+    max_pages = page_table.shape[1]
+    if out is None:
+        out = torch.empty((total, n_heads, d), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = gqa_attn_paged_prefill_workspace_size(num_seqs, max_tokens, n_heads, n_kv, d,
+                                                  max_pages, page_size)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    _check(library().gqa_attn_paged_prefill(
+        _ptr(q), _nbytes(q), _ptr(k_pages), _ptr(v_pages),
+        min(_nbytes(k_pages), _nbytes(v_pages)), _KV_DTYPES[k_pages.dtype],
+        k_pages.stride(0), k_pages.stride(1), k_pages.stride(2),
+        _ptr(page_table), _nbytes(page_table), max_pages,
+        _ptr(token_offsets), _nbytes(token_offsets), _ptr(position_start), _nbytes(position_start),
+        _ptr(out), _nbytes(out), num_seqs, total, max_tokens, n_heads, n_kv, d, page_size,
+        num_pages, float(scale), _ptr(workspace), _nbytes(workspace), _ptr(status),
+        _stream(stream)))
     return out
 
 

@@ -344,6 +344,147 @@ int gqa_attn_paged_decode_noalloc(const float *q, size_t q_bytes, const void *k_
 }
 
 // ---------------------------------------------------------------------------
+// Page append and chunked prefill over pages
+// ---------------------------------------------------------------------------
+namespace {
+
+// Checks shared by the two entry points that address the pool through
+// token_offsets / position_start / page_table (`what` names the caller).
+int check_pool(const char *what, const void *k_pages, const void *v_pages, size_t pool_bytes,
+               int kv_dtype, int64_t page_stride, int64_t token_stride, int64_t head_stride,
+               const int32_t *page_table, size_t page_table_bytes, int max_pages_per_seq,
+               const int32_t *token_offsets, size_t token_offsets_bytes,
+               const int32_t *position_start, size_t position_start_bytes, int num_seqs,
+               int n_kv_heads, int head_dim, int page_size, int num_pages) {
+    if (num_seqs <= 0 || n_kv_heads <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 ||
+        page_size <= 0)
+        return fail("%s: empty shape", what);
+    if (kv_dtype != GQA_DTYPE_F16 && kv_dtype != GQA_DTYPE_BF16)
+        return fail("%s: kv_dtype must be GQA_DTYPE_F16 or GQA_DTYPE_BF16", what);
+    if (page_stride <= 0 || token_stride <= 0 || head_stride <= 0 || page_stride % 8 ||
+        token_stride % 8 || head_stride % 8)
+        return fail("%s: pool strides must be positive multiples of 8", what);
+    if ((int64_t)max_pages_per_seq * page_size > INT32_MAX)
+        return fail("%s: max_pages_per_seq * page_size exceeds int32", what);
+    if (!aligned(k_pages, 16) || !aligned(v_pages, 16))
+        return fail("%s: pools must be 16-byte aligned", what);
+    __int128 last = (__int128)(num_pages - 1) * page_stride + (__int128)(page_size - 1) * token_stride +
+                    (__int128)(n_kv_heads - 1) * head_stride + head_dim;
+    if (last * 2 > (__int128)UINT64_MAX) return fail("%s: pool extent overflows", what);
+    int rc;
+    if ((rc = need("k_pages", k_pages, pool_bytes, (uint64_t)(last * 2)))) return rc;
+    if ((rc = need("v_pages", v_pages, pool_bytes, (uint64_t)(last * 2)))) return rc;
+    if ((rc = need("page_table", page_table, page_table_bytes,
+                   (uint64_t)num_seqs * max_pages_per_seq * 4)))
+        return rc;
+    if ((rc = need("token_offsets", token_offsets, token_offsets_bytes, ((uint64_t)num_seqs + 1) * 4)))
+        return rc;
+    if ((rc = need("position_start", position_start, position_start_bytes, (uint64_t)num_seqs * 4)))
+        return rc;
+    return GQA_OK;
+}
+
+}  // namespace
+
+int gqa_paged_append(const float *k_new, const float *v_new, size_t new_bytes,
+                     const int32_t *token_offsets, size_t token_offsets_bytes,
+                     const int32_t *position_start, size_t position_start_bytes,
+                     const int32_t *page_table, size_t page_table_bytes, int max_pages_per_seq,
+                     void *k_pages, void *v_pages, size_t pool_bytes, int kv_dtype,
+                     int64_t page_stride, int64_t token_stride, int64_t head_stride, int num_seqs,
+                     int total_tokens, int n_kv_heads, int head_dim, int page_size, int num_pages,
+                     int32_t *status, gqa_stream_t stream) {
+    int rc;
+    if (head_dim <= 0 || head_dim % 8 || head_dim > 4096)
+        return fail("paged append: head_dim %d must be a positive multiple of 8 (at most 4096)",
+                    head_dim);
+    if (total_tokens < 0) return fail("paged append: total_tokens is negative");
+    if ((rc = check_pool("paged append", k_pages, v_pages, pool_bytes, kv_dtype, page_stride,
+                         token_stride, head_stride, page_table, page_table_bytes, max_pages_per_seq,
+                         token_offsets, token_offsets_bytes, position_start, position_start_bytes,
+                         num_seqs, n_kv_heads, head_dim, page_size, num_pages)))
+        return rc;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16))
+        return fail("paged append: k_new and v_new must be 16-byte aligned");
+    const uint64_t rows = (uint64_t)total_tokens * n_kv_heads * head_dim * 4;
+    if (total_tokens > 0) {
+        if ((rc = need("k_new", k_new, new_bytes, rows))) return rc;
+        if ((rc = need("v_new", v_new, new_bytes, rows))) return rc;
+    }
+    gqa::PagedAppendProblem p{k_new,       v_new,        token_offsets, position_start,
+                              page_table,  max_pages_per_seq, k_pages, v_pages,
+                              kv_dtype,    page_stride,  token_stride,  head_stride,
+                              num_seqs,    total_tokens, n_kv_heads,    head_dim,
+                              page_size,   num_pages,    status};
+    const cudaError_t e = gqa::launch_paged_append(p, cs(stream));
+    if (e != cudaSuccess) return cuda_fail("paged append launch", e);
+    return ok();
+}
+
+size_t gqa_attn_paged_prefill_workspace_size(int num_seqs, int max_tokens, int n_heads,
+                                             int n_kv_heads, int head_dim, int max_pages_per_seq,
+                                             int page_size) {
+    if (num_seqs <= 0 || max_tokens <= 0 || n_heads <= 0 || n_kv_heads <= 0 ||
+        n_heads % n_kv_heads || !(head_dim == 128 || head_dim == 256) || max_pages_per_seq <= 0 ||
+        page_size <= 0 || (int64_t)max_pages_per_seq * page_size > INT32_MAX)
+        return 0;
+    return gqa::paged_prefill_workspace_bytes(num_seqs, max_tokens, n_heads, n_kv_heads, head_dim,
+                                              max_pages_per_seq, page_size);
+}
+
+int gqa_attn_paged_prefill(const float *q, size_t q_bytes, const void *k_pages,
+                           const void *v_pages, size_t pool_bytes, int kv_dtype,
+                           int64_t page_stride, int64_t token_stride, int64_t head_stride,
+                           const int32_t *page_table, size_t page_table_bytes,
+                           int max_pages_per_seq, const int32_t *token_offsets,
+                           size_t token_offsets_bytes, const int32_t *position_start,
+                           size_t position_start_bytes, float *o, size_t o_bytes, int num_seqs,
+                           int total_tokens, int max_tokens, int n_heads, int n_kv_heads,
+                           int head_dim, int page_size, int num_pages, float scale,
+                           void *workspace, size_t workspace_bytes, int32_t *status,
+                           gqa_stream_t stream) {
+    int rc;
+    if (n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0)
+        return fail("paged prefill: n_heads %d is not a positive multiple of n_kv_heads %d", n_heads,
+                    n_kv_heads);
+    if (head_dim != 128 && head_dim != 256)
+        return fail("paged prefill: unsupported head_dim %d (128 or 256)", head_dim);
+    if (page_size % 8)
+        return fail("paged prefill: page_size %d must be a multiple of 8", page_size);
+    if (total_tokens < 0 || max_tokens <= 0)
+        return fail("paged prefill: total_tokens must be >= 0 and max_tokens > 0");
+    if ((int64_t)total_tokens * n_heads > INT32_MAX)
+        return fail("paged prefill: total_tokens * n_heads exceeds int32");
+    if ((rc = check_pool("paged prefill", k_pages, v_pages, pool_bytes, kv_dtype, page_stride,
+                         token_stride, head_stride, page_table, page_table_bytes, max_pages_per_seq,
+                         token_offsets, token_offsets_bytes, position_start, position_start_bytes,
+                         num_seqs, n_kv_heads, head_dim, page_size, num_pages)))
+        return rc;
+    if (!aligned(q, 16) || !aligned(o, 16)) return fail("paged prefill: q and o must be 16-byte aligned");
+    if (!std::isfinite(scale)) return fail("paged prefill: scale must be finite");
+    const uint64_t qo = (uint64_t)total_tokens * n_heads * head_dim * 4;
+    if (total_tokens > 0) {
+        if ((rc = need("q", q, q_bytes, qo))) return rc;
+        if ((rc = need("o", o, o_bytes, qo))) return rc;
+    }
+    const size_t ws_need = gqa::paged_prefill_workspace_bytes(num_seqs, max_tokens, n_heads, n_kv_heads,
+                                                              head_dim, max_pages_per_seq, page_size);
+    if (ws_need > 0) {
+        if ((rc = need("workspace", workspace, workspace_bytes, ws_need))) return rc;
+        if (!aligned(workspace, 256)) return fail("paged prefill: workspace must be 256-byte aligned");
+    }
+    gqa::PagedPrefillProblem p{q,           o,           k_pages,          v_pages,
+                               kv_dtype,    page_stride, token_stride,     head_stride,
+                               page_table,  max_pages_per_seq, token_offsets, position_start,
+                               num_seqs,    total_tokens, max_tokens,      n_heads,
+                               n_kv_heads,  head_dim,    page_size,        num_pages,
+                               scale,       status};
+    const cudaError_t e = gqa::launch_paged_prefill(p, workspace, cs(stream));
+    if (e != cudaSuccess) return cuda_fail("paged prefill launch", e);
+    return ok();
+}
+
+// ---------------------------------------------------------------------------
 // DFlash2 ring KV
 // ---------------------------------------------------------------------------
 int gqa_ring_params_valid(const gqa_ring_params *p) {

@@ -30,6 +30,12 @@
 // half of the output, both recomputing S.
 // Few tiles (verify) are split along the keys; partial results carry a
 // log2-sum-exp and are merged by a combine kernel.
+// Three ways of finding the visible keys, one kernel instance each: an
+// additive mask tensor (prefill, verify), a ring read directly (fused
+// verify), and pages (chunked prefill: ferrum-kernels 0.8.3
+// causal_attention.rs, CausalAttentionParams position_start / tokens -- query
+// token i of a sequence sits at position position_start + i and sees keys
+// 0..position_start + i of its own sequence, gathered from its pages).
 // Every mbarrier wait is bounded (2 s); on expiry the CTA raises
 // GQA_FLAG_TIMEOUT, unwinds, frees its TMEM and exits.
 #include <cuda.h>
@@ -38,6 +44,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <numeric>
 
 #include "common.cuh"
 #include "launch.h"
@@ -68,6 +75,10 @@ constexpr int kMaxListTiles = 128;
 // shared memory left for the Q tile and the ring after barriers, the row-max
 // exchange and the two tile lists (the dynamic shared memory base is 1024-aligned)
 constexpr int kSmemBudget = 232448 - 256 - 2048 - 2 * 2 * kMaxListTiles;
+// how a kernel instance finds the visible keys
+constexpr int kMaskMode = 0;   // additive mask tensor, tiles classified by a pre-pass
+constexpr int kRingMode = 1;   // ring-direct verify
+constexpr int kPagedMode = 2;  // chunked prefill over pages, causal by position
 
 // Per head_dim: KSUB stages per K tile, VSUB per V tile (DO output columns),
 // Q in TMEM only at head_dim 128 (at 256 and 512, O and two S buffers fill
@@ -137,7 +148,47 @@ struct AttnArgs {
     int ring, ring_w, ring_r;
     const float *cur_k, *cur_v;           // [lanes][ring_r][n_kv_heads][head_dim]
     const uint32_t *ring_len, *ring_wp;   // [lanes]
+    // chunked prefill over pages: a unit's lane is a sequence s whose tokens are
+    // rows tok_off[s] .. tok_off[s+1]-1 of Q and O (at most `rows` of them), query
+    // token i at position pos_start[s] + i; key t of the sequence is slot
+    // t % page_size of page page_table[s][t / page_size], K/V by 4-D tensor maps
+    // {head_dim, kv heads, page_size, num_pages} in boxes of pg_box slots
+    const int32_t *tok_off, *pos_start, *page_table;
+    const uint16_t *v_pool;
+    int64_t pool_page, pool_token, pool_head;  // element strides
+    int total_tokens, max_pages, page_size, num_pages, pg_box;
+    int pg_dim[3];  // logical coordinate (0 kv head, 1 slot, 2 page) of map dimensions 1..3
 };
+
+// A sequence's tokens and start position as read from the device counters,
+// clamped so that every access stays in bounds: rows [t0, t0 + ntok) of Q and O,
+// positions ps .. ps + ntok - 1, keys below ps + ntok <= max_pages * page_size.
+struct SeqSpan {
+    int t0, ntok, ps;
+};
+__device__ __forceinline__ SeqSpan seq_span(const AttnArgs &a, int s, bool flag) {
+    const int cap = a.max_pages * a.page_size;
+    const int o0 = a.tok_off[s], o1 = a.tok_off[s + 1], ps = a.pos_start[s];
+    SeqSpan q;
+    q.t0 = min(max(o0, 0), a.total_tokens);
+    const int t1 = min(max(o1, q.t0), a.total_tokens);
+    q.ps = min(max(ps, 0), cap);
+    q.ntok = min(min(t1 - q.t0, a.rows), cap - q.ps);
+    if (flag && (q.t0 != o0 || t1 != o1 || q.ps != ps || q.ntok != o1 - o0))
+        raise_flag(a.status, GQA_FLAG_CONTEXT_CLAMPED);
+    return q;
+}
+
+// physical page of key t of sequence s (t below the sequence's context),
+// clamped into the pool
+__device__ __forceinline__ int page_of(const AttnArgs &a, int s, int t) {
+    int page = a.page_table[(int64_t)s * a.max_pages + t / a.page_size];
+    if (page < 0 || page >= a.num_pages) {
+        raise_flag(a.status, GQA_FLAG_PAGE_CLAMPED);
+        page = page < 0 ? 0 : a.num_pages - 1;
+    }
+    return page;
+}
 
 // number of slots of [a, b) inside the circular range of `len` slots that starts at
 // `start` in a ring of w slots
@@ -325,6 +376,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int c16) {
 struct Unit {
     Tile t;
     int tile_id, dpart, split, cg, jb, je, d_off, head_idx, q_head0, q_row0;
+    int t0, ntok, ps;  // chunked prefill: the sequence's span (else 0, rows, 0)
 };
 
 // Unit u of the heavy-first order (row tiles from the last, which see the most
@@ -348,7 +400,29 @@ __device__ __forceinline__ Unit unit_of(const AttnArgs &a, int u, bool pair, uin
     n.head_idx = n.t.lane * a.n_kv_heads + n.t.kh;
     n.q_head0 = n.t.kh * a.group + n.t.ht * a.heads_per_tile;
     n.q_row0 = n.t.rt * a.rows_per_head;
+    n.t0 = 0;
+    n.ntok = a.rows;
+    n.ps = 0;
     return n;
+}
+
+__device__ __forceinline__ void set_span(const AttnArgs &a, Unit &n, bool flag) {
+    const SeqSpan q = seq_span(a, n.t.lane, flag);
+    n.t0 = q.t0;
+    n.ntok = q.ntok;
+    n.ps = q.ps;
+}
+
+// Chunked prefill: code of key tile j for a unit (0 skip, 1 visible to every
+// row, 2 mixed).  The unit's rows are tokens r0 .. r0 + rows_per_head - 1 of its
+// sequence (those below ntok carry a query), at positions ps + row.
+__device__ __forceinline__ int paged_tile_code(const AttnArgs &a, const Unit &n, int j) {
+    const int r0 = n.q_row0;
+    if (r0 >= n.ntok) return 0;
+    const int p0 = n.ps + r0, p1 = n.ps + min(r0 + a.rows_per_head, n.ntok) - 1;
+    const int k0 = j * BN;
+    if (k0 > p1) return 0;
+    return k0 + BN - 1 <= p0 ? 1 : 2;
 }
 
 // The k-th unit of work slot `slot` of `slots` (a slot is a CTA, or a CTA pair):
@@ -372,7 +446,7 @@ __device__ __forceinline__ int slot_unit(int k, int slot, int slots, int units) 
 // (cta_group::2).  Each CTA loads only half of every K tile (64 of its keys) and
 // half of every V tile (half of the output columns), so the K/V bytes an SM takes
 // in per tile are halved; the even CTA issues all MMAs.
-template <int D, class KV, bool PAIR, bool RING = false>
+template <int D, class KV, bool PAIR, int MODE = kMaskMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq,
@@ -383,7 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool kBf16 = KV::kind == GQA_DTYPE_BF16;
     constexpr int kQStages = D / 64;  // an f32 Q tile crosses the ring 64 columns per stage
     static_assert(!PAIR || D >= 256, "CTA pairs stage Q in shared memory (head_dim >= 256)");
-    static_assert(!(PAIR && RING), "ring-direct verify runs unpaired");
+    constexpr bool RING = MODE == kRingMode, PAGED = MODE == kPagedMode;
+    static_assert(!(PAIR && MODE != kMaskMode), "ring-direct verify and chunked prefill run unpaired");
     // ring stages per K and per V tile (PAIR: one stage holds this CTA's 64 keys x
     // 256 columns of K, or its 128 keys x 128 output columns of V)
     constexpr int KST = PAIR ? D / 256 : KSUB;
@@ -494,7 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; ok; ++k) {
                 const int uid = slot_unit(k, slot, slots, units);
                 if (uid < 0) break;
-                const Unit un = unit_of(a, uid, PAIR, rank, DO);
+                Unit un = unit_of(a, uid, PAIR, rank, DO);
+                if constexpr (PAGED) set_span(a, un, lane == 0);
                 const int b = k & 1;
                 uint16_t *list = lists + b * kMaxListTiles;
                 // the list buffer of unit k - 2 must have been read by every role
@@ -514,8 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int n = 0;
                 for (int base = un.jb; base < un.je; base += 32) {
                     const int j = base + lane;
-                    const int code =
-                        j < un.je ? (RING ? ring_tile_code(a, j, ring_l, ring_p) : tile_code(a, un.cg, j)) : 0;
+                    const int code = j >= un.je ? 0
+                                     : RING  ? ring_tile_code(a, j, ring_l, ring_p)
+                                     : PAGED ? paged_tile_code(a, un, j)
+                                             : tile_code(a, un.cg, j);
                     const unsigned vis = __ballot_sync(0xffffffffu, code != 0);
                     if (code)
                         list[n + __popc(vis & ((1u << lane) - 1u))] =
@@ -544,8 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int bx = 0; bx < 2; ++bx)
                             tc::tma_load_3d(dst + bx * 16384, &tmq, full(stage), qs * 64 + bx * 32,
-                                            a.q_rows_dim1 ? un.q_row0 : un.q_head0,
-                                            a.q_rows_dim1 ? un.q_head0 : un.q_row0);
+                                            a.q_rows_dim1 ? un.t0 + un.q_row0 : un.q_head0,
+                                            a.q_rows_dim1 ? un.q_head0 : un.t0 + un.q_row0);
                     }
                     next();
                 }
@@ -567,11 +645,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4 *>(dst + c * 16384 + sw128(row, ch)) = v;
                     }
                 };
+                // chunked prefill: one stage of K or V of key tile j over the sequence's
+                // pages, as BN / pg_box boxes of [pg_box slots][64 columns] (pg_box divides
+                // the page size, so no box straddles two pages), each lane issuing one.
+                // Keys at or past the context end ctx are never visible: their K rows
+                // are left as they are (their scores are replaced by -inf), their V rows
+                // are zeroed, so that the zero probabilities meet finite values; the V
+                // box holding the context end is copied row by row.
+                auto fill_paged = [&](uint32_t dst, bool is_v, int j, int d0) {
+                    const int ctx = un.ps + un.ntok;
+                    const int kb = j * BN, key0 = kb + lane * a.pg_box;
+                    const bool tma = lane * a.pg_box < BN && key0 < ctx && (!is_v || key0 + a.pg_box <= ctx);
+                    int page = 0;
+                    if (tma) page = page_of(a, un.t.lane, key0);
+                    if (is_v && kb + BN > ctx) {
+                        uint8_t *img = smem + (dst - sbase);
+                        const int m0 = max((ctx / a.pg_box) * a.pg_box - kb, 0);  // first row not by TMA
+                        for (int q = m0 * 16 + lane; q < BN * 16; q += 32) {
+                            const int row = q >> 4, c = (q >> 3) & 1, ch = q & 7;
+                            const int key = kb + row;
+                            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                            if (key < ctx)
+                                v = ld_nc_v4(a.v_pool + (int64_t)page_of(a, un.t.lane, key) * a.pool_page +
+                                             (int64_t)(key % a.page_size) * a.pool_token +
+                                             (int64_t)un.t.kh * a.pool_head + d0 + c * 64 + ch * 8);
+                            *reinterpret_cast<uint4 *>(img + c * (BN * 128) + sw128(row, ch)) = v;
+                        }
+                        tc::fence_async_smem();
+                    }
+                    const int boxes = __popc(__ballot_sync(0xffffffffu, tma));
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (boxes)
+                            tc::mbar_arrive_expect_tx(full(stage), (uint32_t)boxes * a.pg_box * 256u);
+                        else
+                            tc::mbar_arrive(full(stage));
+                    }
+                    __syncwarp();
+                    if (tma) {
+                        const int slot_in_page = key0 % a.page_size;
+                        auto crd = [&](int w) { return w == 0 ? un.t.kh : (w == 1 ? slot_in_page : page); };
+                        const int c1 = crd(a.pg_dim[0]), c2 = crd(a.pg_dim[1]), c3 = crd(a.pg_dim[2]);
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            tc::tma_load_4d(dst + c * (BN * 128) + lane * a.pg_box * 128,
+                                            is_v ? (const void *)&tmv : (const void *)&tmk, full(stage),
+                                            d0 + c * 64, c1, c2, c3);
+                    }
+                };
                 // one stage of K or V: two boxes of [BN rows][64 columns] from column d0
                 auto load = [&](int j, bool is_v, int d0) -> bool {
                     if (!slot_free()) return false;
                     const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
-                    if (RING && j == 0) {
+                    if (PAGED) {
+                        fill_paged(dst, is_v, j, d0);
+                    } else if (RING && j == 0) {
                         fill_current(smem + L::kStages + stage * kStageBytes, is_v, d0);
                         tc::fence_async_smem();
                         __syncwarp();
@@ -836,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // f32 stages are kept (not released) to stage the previous unit's O.
         auto convert_q = [&](const Unit &un, int qpos, bool hold) {
             int head = 0, row = 0;
-            const bool valid = row_of(a, un.t, r, head, row);
+            const bool valid = row_of(a, un.t, r, head, row) && row < un.ntok;
             auto put_q = [&](int cb, const uint32_t(&w)[16]) {
                 if constexpr (C::QTM) {
                     tc::tmem_st16(tm_q + cb * 32 + h * 16 + lane_base, w);
@@ -881,8 +1009,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
                         x[cb][v] = valid ? ld_nc_v4(static_cast<const uint16_t *>(a.q) + un.t.lane * a.q_lane +
-                                                    (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64 +
-                                                    h * 32 + v * 8)
+                                                    (int64_t)head * a.q_head + (int64_t)(un.t0 + row) * a.q_row +
+                                                    cb * 64 + h * 32 + v * 8)
                                          : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int cb = 0; cb < D / 64; ++cb) {
@@ -905,8 +1033,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
                         x[cb][v] = valid ? ld_nc_f4(static_cast<const float *>(a.q) + un.t.lane * a.q_lane +
-                                                    (int64_t)head * a.q_head + (int64_t)row * a.q_row + cb * 64 +
-                                                    h * 32 + v * 4)
+                                                    (int64_t)head * a.q_head + (int64_t)(un.t0 + row) * a.q_row +
+                                                    cb * 64 + h * 32 + v * 4)
                                          : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int cb = 0; cb < D / 64; ++cb) {
@@ -938,6 +1066,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int cur_n = 0, cur_pos = 0;  // visible tiles and first ring position of unit k
         if (uid >= 0) {
             cur = unit_of(a, uid, PAIR, rank, DO);
+            if constexpr (PAGED) set_span(a, cur, false);
             ok = __all_sync(0xffffffffu, wt.wait(list_full(0), 0));
             cur_n = ok ? n_vis_smem[0] : 0;
             if (ok && cur_n > 0) convert_q(cur, 0, false);
@@ -946,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (uid >= 0 && ok) {
             const uint16_t *list = lists + (k & 1) * kMaxListTiles;
             int head = 0, row = 0;
-            const bool valid = row_of(a, cur.t, r, head, row);
+            const bool valid = row_of(a, cur.t, r, head, row) && row < cur.ntok;
             const uint16_t *mrow = valid ? a.mask + cur.t.lane * a.m_lane + (int64_t)head * a.m_head +
                                                (int64_t)row * a.m_row + h * 64
                                          : nullptr;
@@ -995,6 +1124,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // no mask: s stays unscaled; the scale is applied inside the exponent
                         // argument below, and the row maximum is taken on the raw scores
                         sc = scale_log2;
+                    } else if constexpr (PAGED) {
+                        // keys up to this query's position are visible
+                        const int lim = cur.ps + row - (j * BN + h * 64);  // last visible s[c]
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) s[c] = c <= lim ? s[c] * scale_log2 : kNegInf;
                     } else if constexpr (RING) {
                         if (j == 0) {
                             // the current rows, then padding
@@ -1148,11 +1282,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 512 (its 8 Q stages cycle through a 3-stage ring and cannot be held): in
             // the Q tile area (128 KiB), before the next unit's Q is converted.
             constexpr bool kHoldQ = kQStages <= NS;
-            const bool stage_o = a.o_tma && cur_n > 0;
+            // (chunked prefill: only tiles whose rows all belong to the sequence)
+            const bool stage_o = a.o_tma && cur_n > 0 && (!PAGED || cur.q_row0 + BM <= cur.ntok);
             int o_slot0 = 0;       // first ring position of the staging area
             bool hold_q = false;   // staging in the next unit's Q slots
             if (nuid >= 0 && ok) {
                 nxt = unit_of(a, nuid, PAIR, rank, DO);
+                if constexpr (PAGED) set_span(a, nxt, false);
                 ok = __all_sync(0xffffffffu, wt.wait(list_full((k + 1) & 1), ((k + 1) >> 1) & 1));
                 nxt_n = ok ? n_vis_smem[(k + 1) & 1] : 0;
                 if constexpr (kHoldQ) {
@@ -1224,8 +1360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::named_bar(6 + h, kSoftmaxThreads / 2);
                     if (issuer && !*abort_flag)
                         tc::tma_store_3d(&tmo, smem_u32(stg), cur.d_off + box * 32,
-                                         a.o_rows_dim1 ? cur.q_row0 : cur.q_head0,
-                                         a.o_rows_dim1 ? cur.q_head0 : cur.q_row0);
+                                         a.o_rows_dim1 ? cur.t0 + cur.q_row0 : cur.q_head0,
+                                         a.o_rows_dim1 ? cur.q_head0 : cur.t0 + cur.q_row0);
                 }
                 if (issuer) {
                     tc::bulk_commit();
@@ -1235,7 +1371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float *dst;
                 if (a.splits == 1) {
                     dst = valid ? a.o + cur.t.lane * a.o_lane + (int64_t)head * a.o_head +
-                                      (int64_t)row * a.o_row + cur.d_off + h * (DO / 2)
+                                      (int64_t)(cur.t0 + row) * a.o_row + cur.d_off + h * (DO / 2)
                                 : nullptr;
                 } else {
                     const int64_t unit = ((int64_t)cur.tile_id * a.d_parts + cur.dpart) * a.splits + cur.split;
@@ -1305,6 +1441,12 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a, int
     const Tile t = tile_of(a, tile_id);
     int head, row;
     if (!row_of(a, t, r, head, row)) return;
+    if (a.tok_off) {
+        // chunked prefill: tile rows past the sequence's tokens carry no query
+        const SeqSpan q = seq_span(a, t.lane, false);
+        if (row >= q.ntok) return;
+        row += q.t0;
+    }
     const int64_t u0 = ((int64_t)tile_id * a.d_parts + dpart) * a.splits;
     float M = kNegInf;
     for (int s = 0; s < a.splits; ++s) M = fmaxf(M, a.ws_lse[(u0 + s) * BM + r]);
@@ -1446,10 +1588,45 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
     return r == CUDA_SUCCESS;
 }
 
-template <int D, class KV, bool PAIR, bool RING = false>
+// A 4-D tiled map over a page pool: head_dim x (kv heads, page slots, pages) with
+// element strides (hs, ts, ps), the three outer dimensions ordered by increasing
+// stride; box = 64 columns x box_rows slots of one head and one page, 128-byte
+// swizzle, so that its shared-memory image is [box_rows][64 columns] whatever the
+// order.  dim_of[i] receives the logical coordinate (0 head, 1 slot, 2 page) of
+// map dimension i + 1.
+bool make_paged_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int d, int hk,
+                    int page_size, int num_pages, int64_t hs, int64_t ts, int64_t ps, int box_rows,
+                    int dim_of[3]) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    struct Dim {
+        int64_t size, stride;
+        int which;
+    } v[3] = {{hk, hs, 0}, {page_size, ts, 1}, {num_pages, ps, 2}};
+    // a dimension of one element is never stepped along: give it a harmless stride
+    for (auto &x : v)
+        if (x.size == 1) x.stride = std::max<int64_t>(x.stride, 8);
+    std::stable_sort(v, v + 3, [](const Dim &x, const Dim &y) { return x.stride < y.stride; });
+    cuuint64_t dims[4] = {(cuuint64_t)d, 0, 0, 0};
+    cuuint64_t strides[3];
+    cuuint32_t box[4] = {64, 1, 1, 1};
+    for (int i = 0; i < 3; ++i) {
+        dims[i + 1] = (cuuint64_t)v[i].size;
+        strides[i] = (cuuint64_t)v[i].stride * 2;
+        if (v[i].which == 1) box[i + 1] = (cuuint32_t)box_rows;
+        dim_of[i] = v[i].which;
+    }
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, dt, 4, const_cast<void *>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, class KV, bool PAIR, int MODE = kMaskMode>
 cudaError_t run_attn(const AttnArgs &a, const CUtensorMap *maps, int units, int tiles,
                      cudaStream_t stream) {
-    auto kern = attn_kernel<D, KV, PAIR, RING>;
+    auto kern = attn_kernel<D, KV, PAIR, MODE>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1524,6 +1701,110 @@ int ring_keys(int window) { return BN + window; }
 size_t verify_ring_workspace_bytes(const gqa_ring_params &p) {
     return plan_bytes(make_plan((int)p.lanes, (int)p.rows, (int)p.q_heads, (int)p.kv_heads,
                                 (int)p.head_dim, ring_keys((int)p.window), false));
+}
+
+// Chunked prefill: sequences are the lanes, max_tokens their rows, the key space
+// max_pages_per_seq * page_size; no mask classification, never paired.
+static Plan paged_plan(int num_seqs, int max_tokens, int n_heads, int n_kv_heads, int head_dim,
+                       int max_pages_per_seq, int page_size) {
+    Plan pl = make_plan(num_seqs, max_tokens, n_heads, n_kv_heads, head_dim,
+                        max_pages_per_seq * page_size, false);
+    pl.codes_bytes = 0;
+    return pl;
+}
+
+size_t paged_prefill_workspace_bytes(int num_seqs, int max_tokens, int n_heads, int n_kv_heads,
+                                     int head_dim, int max_pages_per_seq, int page_size) {
+    return plan_bytes(paged_plan(num_seqs, max_tokens, n_heads, n_kv_heads, head_dim,
+                                 max_pages_per_seq, page_size));
+}
+
+cudaError_t launch_paged_prefill(const PagedPrefillProblem &p, void *workspace, cudaStream_t stream) {
+    if (p.total_tokens == 0) return cudaSuccess;
+    const Plan pl = paged_plan(p.num_seqs, p.max_tokens, p.n_heads, p.n_kv_heads, p.head_dim,
+                               p.max_pages_per_seq, p.page_size);
+    AttnArgs a{};
+    const int64_t row = (int64_t)p.n_heads * p.head_dim;
+    a.q = p.q;
+    a.q_f32 = 1;
+    a.q_row = row;
+    a.q_head = p.head_dim;
+    a.kv_bf16 = p.kv_dtype == GQA_DTYPE_BF16;
+    a.o = p.o;
+    a.o_row = row;
+    a.o_head = p.head_dim;
+    a.lanes = p.num_seqs;
+    a.rows = p.max_tokens;
+    a.n_heads = p.n_heads;
+    a.n_kv_heads = p.n_kv_heads;
+    a.group = p.n_heads / p.n_kv_heads;
+    a.n_keys = p.max_pages_per_seq * p.page_size;
+    a.rows_per_head = pl.rows_per_head;
+    a.heads_per_tile = pl.heads_per_tile;
+    a.row_tiles = pl.row_tiles;
+    a.head_tiles = pl.head_tiles;
+    a.tiles_total = pl.tiles;
+    a.n_blk = pl.n_blk;
+    a.splits = pl.splits;
+    a.blk_per_split = pl.bps;
+    a.d_parts = pl.d_parts;
+    a.scale_log2 = p.scale * kLog2e;
+    char *ws = static_cast<char *>(workspace);
+    a.ws_o = pl.splits > 1 ? reinterpret_cast<float *>(ws) : nullptr;
+    a.ws_lse = pl.splits > 1 ? reinterpret_cast<float *>(ws + pl.part_o_bytes) : nullptr;
+    a.status = p.status;
+    a.tok_off = p.token_offsets;
+    a.pos_start = p.position_start;
+    a.page_table = p.page_table;
+    a.v_pool = static_cast<const uint16_t *>(p.v_pool);
+    a.pool_page = p.page_stride;
+    a.pool_token = p.token_stride;
+    a.pool_head = p.head_stride;
+    a.total_tokens = p.total_tokens;
+    a.max_pages = p.max_pages_per_seq;
+    a.page_size = p.page_size;
+    a.num_pages = p.num_pages;
+    a.pg_box = std::gcd(p.page_size, BN);  // >= 8: the page size is a multiple of 8
+
+    CUtensorMap maps[4];
+    memset(maps, 0, sizeof maps);
+    const CUtensorMapDataType kvt =
+        a.kv_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    int dim_k[3], dim_v[3];
+    if (!make_paged_map(&maps[0], p.k_pool, kvt, p.head_dim, p.n_kv_heads, p.page_size, p.num_pages,
+                        p.head_stride, p.token_stride, p.page_stride, a.pg_box, dim_k) ||
+        !make_paged_map(&maps[1], p.v_pool, kvt, p.head_dim, p.n_kv_heads, p.page_size, p.num_pages,
+                        p.head_stride, p.token_stride, p.page_stride, a.pg_box, dim_v))
+        return cudaErrorInvalidValue;
+    for (int i = 0; i < 3; ++i) a.pg_dim[i] = dim_k[i];
+    // f32 Q in by TMA and O out by TMA for one head's 128-token tiles
+    if (pl.heads_per_tile == 1 && pl.rows_per_head == BM &&
+        make_map(&maps[2], p.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.head_dim, p.total_tokens,
+                 p.n_heads, row, p.head_dim, 32, BM)) {
+        a.q_tma = 1;
+        a.q_rows_dim1 = rows_first(p.n_heads, row, p.head_dim) ? 1 : 0;
+        if (pl.splits == 1 &&
+            make_map(&maps[3], p.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.head_dim, p.total_tokens,
+                     p.n_heads, row, p.head_dim, 32, BM)) {
+            a.o_tma = 1;
+            a.o_rows_dim1 = a.q_rows_dim1;
+        }
+    }
+    const int units = pl.tiles * pl.d_parts * pl.splits;
+    int sms = sm_count();
+    if (sms <= 0) sms = 148;
+    const int ctas = std::min(units, sms);
+    const bool bf = a.kv_bf16;
+    switch (p.head_dim) {
+        case 128:
+            return bf ? run_attn<128, BF16, false, kPagedMode>(a, maps, ctas, pl.tiles, stream)
+                      : run_attn<128, F16, false, kPagedMode>(a, maps, ctas, pl.tiles, stream);
+        case 256:
+            return bf ? run_attn<256, BF16, false, kPagedMode>(a, maps, ctas, pl.tiles, stream)
+                      : run_attn<256, F16, false, kPagedMode>(a, maps, ctas, pl.tiles, stream);
+        default:
+            return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t stream) {
@@ -1622,8 +1903,8 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     if (p.ring) {
         // ring-direct verify: bf16 rings, head_dim 128 or 256, unpaired
         if (!bf || pl.pair) return cudaErrorInvalidValue;
-        if (p.head_dim == 128) return run_attn<128, BF16, false, true>(a, maps, ctas, pl.tiles, stream);
-        if (p.head_dim == 256) return run_attn<256, BF16, false, true>(a, maps, ctas, pl.tiles, stream);
+        if (p.head_dim == 128) return run_attn<128, BF16, false, kRingMode>(a, maps, ctas, pl.tiles, stream);
+        if (p.head_dim == 256) return run_attn<256, BF16, false, kRingMode>(a, maps, ctas, pl.tiles, stream);
         return cudaErrorInvalidValue;
     }
     switch (p.head_dim) {

@@ -58,6 +58,37 @@ size_t prefill_workspace_bytes(int rows, int n_heads, int n_kv_heads, int head_d
 size_t verify_workspace_bytes(const gqa_ring_params &p);
 size_t verify_ring_workspace_bytes(const gqa_ring_params &p);
 cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t stream);
+
+// append.cu -- page append (new tokens' K/V rows into their page slots)
+struct PagedAppendProblem {
+    const float *k_new, *v_new;  // [total_tokens][n_kv_heads][head_dim]
+    const int32_t *token_offsets, *position_start, *page_table;
+    int max_pages_per_seq;
+    void *k_pool, *v_pool;
+    int kv_dtype;
+    int64_t page_stride, token_stride, head_stride;
+    int num_seqs, total_tokens, n_kv_heads, head_dim, page_size, num_pages;
+    int32_t *status;
+};
+cudaError_t launch_paged_append(const PagedAppendProblem &p, cudaStream_t stream);
+
+// attn_tc.cu -- chunked prefill over pages (tcgen05 attention, keys gathered from pages)
+struct PagedPrefillProblem {
+    const float *q;  // [total_tokens][n_heads][head_dim]
+    float *o;        // same layout
+    const void *k_pool, *v_pool;
+    int kv_dtype;
+    int64_t page_stride, token_stride, head_stride;
+    const int32_t *page_table;
+    int max_pages_per_seq;
+    const int32_t *token_offsets, *position_start;
+    int num_seqs, total_tokens, max_tokens, n_heads, n_kv_heads, head_dim, page_size, num_pages;
+    float scale;
+    int32_t *status;
+};
+size_t paged_prefill_workspace_bytes(int num_seqs, int max_tokens, int n_heads, int n_kv_heads,
+                                     int head_dim, int max_pages_per_seq, int page_size);
+cudaError_t launch_paged_prefill(const PagedPrefillProblem &p, void *workspace, cudaStream_t stream);
 void set_attention_pairs(int mode);
 cudaError_t launch_bounded_wait_selftest(int32_t *status, int timeout_ms, cudaStream_t stream);
 

@@ -308,6 +308,34 @@ def setup_verify(torch, g, c):
                        "fused_bytes": fby, "fused_launches": 1 + 1 + 1}
 
 
+def setup_chunk(torch, g, c):
+    """Chunked prefill over pages: append the new tokens' K/V into their pages, then
+    attend (each new token over its sequence's cached prefix and the new tokens up to
+    itself)."""
+    q, kn, vn = _dev(torch, c.q), _dev(torch, c.k_new), _dev(torch, c.v_new)
+    kp, vp = _dev(torch, c.k_pool), _dev(torch, c.v_pool)
+    pt, off, ps = _dev(torch, c.page_table), _dev(torch, c.token_offsets), _dev(torch, c.position_start)
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    max_tok = int(np.diff(c.token_offsets).max())
+    ws = torch.empty(max(1, g.gqa_attn_paged_prefill_workspace_size(
+        c.num_seqs, max_tok, c.n_heads, c.n_kv_heads, c.head_dim, c.max_pages_per_seq,
+        c.page_size)), dtype=torch.uint8, device="cuda")
+    ops = {
+        "append": lambda: g.gqa_paged_append(kn, vn, off, ps, pt, kp, vp),
+        "attn": lambda: g.gqa_attn_paged_prefill(q, kp, vp, pt, off, ps, max_tok, c.scale,
+                                                 out=out, workspace=ws),
+    }
+
+    def step():
+        for f in ops.values():
+            f()
+
+    nb = lambda t: t.numel() * t.element_size()
+    # append: f32 rows in, 16-bit rows out, for K and V
+    append_bytes = nb(kn) + nb(vn) + (nb(kn) + nb(vn)) // 2
+    return step, ops, {"flops": c.flops(), "append_bytes": append_bytes, "launches": 2}
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing (baseline and reference arm)
 # ---------------------------------------------------------------------------
@@ -376,6 +404,7 @@ CAPTURE_CASES = {
     "prefill_d512": lambda w: w.prefill_d512_prefix(seed=0),
     "decode_16seq": lambda w: w.paged_decode(num_seqs=16, num_pages=16384, seed=0),
     "verify": lambda w: w.verify_full(seed=0),
+    "paged_chunk": lambda w: w.paged_chunk_full(seed=0),
 }
 
 
@@ -390,6 +419,8 @@ def run_capture(name: str, reps: int) -> None:
         step = setup_prefill(torch, g, c)[0]
     elif name.startswith("decode"):
         step = setup_decode(torch, g, c)[0]
+    elif name == "paged_chunk":
+        step = setup_chunk(torch, g, c)[0]
     else:
         step = setup_verify(torch, g, c)[0]
     for _ in range(max(1, reps)):
@@ -543,8 +574,30 @@ def main() -> None:
                                  "unit": "GB/s", "ms_per_step": t, "bytes_per_step": ftotal,
                                  "peak": hbm_peak, "frac": ftotal / (t * 1e-3) / 1e9 / hbm_peak,
                                  "kernels": fkernels}
+        del sv, ops, fops, fstep, vc
+        torch.cuda.empty_cache()
+        # chunked prefill over pages: page append + attention
+        cc = workloads.paged_chunk_full(seed=0)
+        sc, cops, ic = setup_chunk(torch, g, cc)
+        ms = tm.steps(sc, max(5, args.steps // 2), args.warmup)
+        t = tm.max_over_ranks(sum(ms) / len(ms))
+        ka = tm.kernel_ms(g, cops["append"], 5)
+        kt = tm.kernel_ms(g, cops["attn"], 5)
+        paths["paged_chunk_prefill"] = {
+            "workload": cc.name, "value": world * ic["flops"] / (t * 1e-3) / 1e12,
+            "unit": "TFLOP/s", "ms_per_step": t, "flops_per_step": ic["flops"],
+            "roofline": {"bound": "tensor", "kernel": "attn_kernel<256,f16,paged>",
+                         "achieved": ic["flops"] / (kt * 1e-3) / 1e12, "peak": tensor_peak,
+                         "unit": "TFLOP/s", "frac": ic["flops"] / (kt * 1e-3) / 1e12 / tensor_peak,
+                         "kernel_ms": kt},
+            "append": {"kernel": "page_append_kernel<f16>", "bytes": ic["append_bytes"],
+                       "kernel_ms": ka, "achieved_gbs": ic["append_bytes"] / (ka * 1e-3) / 1e9,
+                       "frac": ic["append_bytes"] / (ka * 1e-3) / 1e9 / hbm_peak}}
+        del sc, cops, cc
+        torch.cuda.empty_cache()
         line["paths"] = paths
-        line["gpu_launches"] += (2 + 2 + iv["launches"] + iv["fused_launches"]) * max(5, args.steps // 2)
+        line["gpu_launches"] += ((2 + 2 + iv["launches"] + iv["fused_launches"] + ic["launches"])
+                                 * max(5, args.steps // 2))
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(head)

@@ -206,6 +206,78 @@ int gqa_attn_paged_decode_noalloc(const float *q, size_t q_bytes, const void *k_
                                   gqa_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Page append and chunked prefill over pages (ferrum-kernels 0.8.3          */
+/* causal_attention.rs: CausalAttentionParams position_start / tokens,       */
+/* dispatch_prepare writing K/V into the paged state, dispatch_attention).    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * A batch of new tokens from num_seqs sequences.  Token i of the batch (rows of
+ * the [total_tokens][...] arrays) belongs to the sequence s with
+ *     token_offsets[s] <= i < token_offsets[s+1]
+ * and sits at position p = position_start[s] + (i - token_offsets[s]) of that
+ * sequence; position p is slot p % page_size of physical page
+ *     page_table[s*max_pages_per_seq + p/page_size]
+ * and its K (V) element (kv head g, e) lives at
+ *     pool[page*page_stride + slot*token_stride + g*head_stride + e].
+ * token_offsets int32 [num_seqs+1] (non-decreasing, token_offsets[0] = 0,
+ * token_offsets[num_seqs] <= total_tokens), position_start int32 [num_seqs] and
+ * page_table int32 [num_seqs][max_pages_per_seq] are device arrays; out-of-range
+ * values are clamped or skipped and flagged (never read or written out of
+ * bounds).  Pools: kv_dtype, pool_bytes each, 16-byte aligned, strides positive
+ * multiples of 8 elements.
+ */
+
+/*
+ * Page append: k_new / v_new f32 [total_tokens][n_kv_heads][head_dim]
+ * (16-byte aligned, new_bytes each) are rounded to nearest even into kv_dtype
+ * and written into every token's slot; no other slot changes.  A token whose
+ * position falls outside its page table row, or whose page id is outside
+ * [0, num_pages), is not written (GQA_FLAG_PAGE_CLAMPED); inconsistent
+ * token_offsets raise GQA_FLAG_CONTEXT_CLAMPED.  head_dim a positive multiple
+ * of 8.  Tokens of one call must not share a slot (the order of such writes
+ * is undefined).
+ */
+int gqa_paged_append(const float *k_new, const float *v_new, size_t new_bytes,
+                     const int32_t *token_offsets, size_t token_offsets_bytes,
+                     const int32_t *position_start, size_t position_start_bytes,
+                     const int32_t *page_table, size_t page_table_bytes, int max_pages_per_seq,
+                     void *k_pages, void *v_pages, size_t pool_bytes, int kv_dtype,
+                     int64_t page_stride, int64_t token_stride, int64_t head_stride, int num_seqs,
+                     int total_tokens, int n_kv_heads, int head_dim, int page_size, int num_pages,
+                     int32_t *status, gqa_stream_t stream);
+
+size_t gqa_attn_paged_prefill_workspace_size(int num_seqs, int max_tokens, int n_heads,
+                                             int n_kv_heads, int head_dim, int max_pages_per_seq,
+                                             int page_size);
+
+/*
+ * Chunked (multi-token) prefill over pages: query token i of sequence s, at
+ * position p, attends to the keys at positions 0..p of its own sequence (the
+ * earlier context and the batch's tokens up to itself, which must already be
+ * in the pages, e.g. by gqa_paged_append):
+ *     o[i][h] = softmax_t(scale * q[i][h] . k_t) v_t,  t = 0..p,
+ * KV head h / (n_heads / n_kv_heads).  q, o f32 [total_tokens][n_heads][head_dim]
+ * contiguous, 16-byte aligned.  head_dim 128 or 256; page_size a multiple of 8.
+ * max_tokens bounds every sequence's token count (rows beyond it are not
+ * computed and raise GQA_FLAG_CONTEXT_CLAMPED), as does
+ * position_start[s] + tokens <= max_pages_per_seq * page_size.  Rows of o
+ * that belong to no sequence are not written.  Out-of-range page ids inside a
+ * sequence's context are clamped into the pool (GQA_FLAG_PAGE_CLAMPED).
+ */
+int gqa_attn_paged_prefill(const float *q, size_t q_bytes, const void *k_pages,
+                           const void *v_pages, size_t pool_bytes, int kv_dtype,
+                           int64_t page_stride, int64_t token_stride, int64_t head_stride,
+                           const int32_t *page_table, size_t page_table_bytes,
+                           int max_pages_per_seq, const int32_t *token_offsets,
+                           size_t token_offsets_bytes, const int32_t *position_start,
+                           size_t position_start_bytes, float *o, size_t o_bytes, int num_seqs,
+                           int total_tokens, int max_tokens, int n_heads, int n_kv_heads,
+                           int head_dim, int page_size, int num_pages, float scale,
+                           void *workspace, size_t workspace_bytes, int32_t *status,
+                           gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* DFlash2 ring KV (mlx-native 0.21.1 dflash2_attention_pack.rs).           */
 /* ------------------------------------------------------------------------ */
 

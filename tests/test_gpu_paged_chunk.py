@@ -1,0 +1,165 @@
+"""GPU parity of page append (bit-exact against the oracle's rounding into the
+pages) and of chunked prefill over pages (max |err| <= 1e-2, mean <= 1e-3 against
+the float64 oracle), through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import attention_gqa_flash_gb300 as g
+    g.library()
+    return g
+
+
+def _pool_dev(pool, kv, head_major=False):
+    """The pool on the device as [num_pages, page_size, hk, d]; head_major stores it
+    as [num_pages, hk, page_size, d] and hands the library a permuted view."""
+    import torch
+    from gpu_helpers import dev
+    t = dev(pool, "bf16") if kv == "bf16" else dev(pool)
+    if head_major:
+        t = t.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+    return t
+
+
+def _strides(c):
+    hk, d = c.n_kv_heads, c.head_dim
+    return dict(page_stride=c.page_size * hk * d, token_stride=hk * d, head_stride=d,
+                page_size=c.page_size)
+
+
+def _append_gpu(g, c, head_major=False, table=None):
+    import torch
+    from gpu_helpers import dev, new_status
+    kp, vp = _pool_dev(c.k_pool, c.kv_dtype, head_major), _pool_dev(c.v_pool, c.kv_dtype, head_major)
+    st = new_status()
+    g.gqa_paged_append(dev(c.k_new), dev(c.v_new), dev(c.token_offsets), dev(c.position_start),
+                       dev(c.page_table if table is None else table), kp, vp, status=st)
+    torch.cuda.synchronize()
+    return kp, vp, int(st.item())
+
+
+def _bits(t):
+    from gpu_helpers import host_bits
+    return host_bits(t.contiguous())
+
+
+@pytest.mark.parametrize("kv", ["f16", "bf16"])
+@pytest.mark.parametrize("head_major", [False, True])
+def test_append_is_bit_exact(lib, kv, head_major):
+    c = workloads.paged_chunk(num_seqs=6, tokens_hi=70, prefix_hi=200, head_dim=128, kv_dtype=kv,
+                              seed=11)
+    kp, vp, st = _append_gpu(lib, c, head_major)
+    assert st == 0
+    rk, rv, skipped = oracle.paged_append(c.k_new, c.v_new, c.token_offsets, c.position_start,
+                                          c.page_table, c.k_pool, c.v_pool, kv_dtype=kv,
+                                          **_strides(c))
+    assert skipped == 0
+    np.testing.assert_array_equal(_bits(kp), rk.view(np.uint16))
+    np.testing.assert_array_equal(_bits(vp), rv.view(np.uint16))
+
+
+def test_append_skips_tokens_without_a_page(lib):
+    c = workloads.paged_chunk(num_seqs=3, tokens_lo=20, tokens_hi=40, prefix_hi=60, head_dim=64,
+                              seed=12)
+    table = c.page_table.copy()
+    s, last = 1, int(c.position_start[1] + c.token_offsets[2] - c.token_offsets[1] - 1)
+    table[s, last // c.page_size] = -1             # no page for the last token(s) of sequence 1
+    table[2, 0] = c.num_pages + 5                  # a page id outside the pool
+    kp, vp, st = _append_gpu(lib, c, table=table)
+    rk, rv, skipped = oracle.paged_append(c.k_new, c.v_new, c.token_offsets, c.position_start,
+                                          table, c.k_pool, c.v_pool, kv_dtype="f16", **_strides(c))
+    assert skipped > 0 and st == 1   # GQA_FLAG_PAGE_CLAMPED
+    np.testing.assert_array_equal(_bits(kp), rk.view(np.uint16))
+    np.testing.assert_array_equal(_bits(vp), rv.view(np.uint16))
+
+
+CASES = [
+    # num_seqs, tokens, prefix, h, hk, d, page_size, kv, head_major
+    (3, (1, 40), (0, 70), 8, 2, 128, 16, "f16", False),       # short chunks: heads packed per tile
+    (2, (100, 300), (0, 500), 4, 2, 256, 16, "bf16", False),  # 128-token tiles, ragged tails
+    (4, (1, 8), (200, 3000), 8, 8, 128, 16, "f16", False),    # decode-like: split along the keys
+    (3, (50, 200), (0, 400), 4, 1, 128, 24, "f16", True),     # 24-slot pages, head-major pool
+    (2, (129, 260), (0, 300), 2, 2, 256, 256, "bf16", False), # pages longer than a key tile
+    (2, (128, 128), (0, 0), 4, 2, 128, 32, "f16", False),     # no prefix, one whole tile
+]
+
+
+@pytest.mark.parametrize("n,tok,pre,h,hk,d,ps,kv,head_major", CASES)
+def test_chunked_prefill_matches_oracle(lib, n, tok, pre, h, hk, d, ps, kv, head_major):
+    import torch
+    from gpu_helpers import assert_attention_close, dev, new_status
+    need = n * (-(-(pre[1] + tok[1]) // ps))
+    c = workloads.paged_chunk(num_seqs=n, tokens_lo=tok[0], tokens_hi=tok[1], prefix_lo=pre[0],
+                              prefix_hi=pre[1], num_pages=need + 7, page_size=ps, n_heads=h,
+                              n_kv_heads=hk, head_dim=d, kv_dtype=kv, seed=n * 7 + d + ps)
+    kp, vp, st = _append_gpu(lib, c, head_major)
+    assert st == 0
+    max_tokens = int(np.diff(c.token_offsets).max())
+    status = new_status()
+    out = lib.gqa_attn_paged_prefill(dev(c.q), kp, vp, dev(c.page_table), dev(c.token_offsets),
+                                     dev(c.position_start), max_tokens, c.scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rk, rv, _ = oracle.paged_append(c.k_new, c.v_new, c.token_offsets, c.position_start,
+                                    c.page_table, c.k_pool, c.v_pool, kv_dtype=kv, **_strides(c))
+    ref = oracle.paged_prefill(c.q, rk, rv, c.page_table, c.token_offsets, c.position_start,
+                               kv_dtype=kv, n_kv_heads=hk, scale=c.scale, **_strides(c))
+    assert_attention_close(out.cpu().numpy(), ref, f"chunked prefill {c.name}")
+
+
+def test_chunked_prefill_leaves_rows_of_no_sequence_alone(lib):
+    """Rows past token_offsets[num_seqs] belong to no sequence and are not written."""
+    import torch
+    from gpu_helpers import dev, new_status
+    c = workloads.paged_chunk(num_seqs=2, tokens_lo=30, tokens_hi=60, prefix_hi=100, head_dim=128,
+                              seed=21)
+    kp, vp, _ = _append_gpu(lib, c)
+    T = c.tokens
+    q = np.concatenate([c.q, np.ones((5,) + c.q.shape[1:], np.float32)])
+    out = torch.full((T + 5,) + c.q.shape[1:], 7.0, dtype=torch.float32, device="cuda")
+    st = new_status()
+    lib.gqa_attn_paged_prefill(dev(q), kp, vp, dev(c.page_table), dev(c.token_offsets),
+                               dev(c.position_start), 64, c.scale, out=out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.all(out[T:] == 7.0)
+
+
+def test_chunked_prefill_full_size_sampled(lib):
+    """8 sequences x 512 new tokens over cached prefixes of up to 7680 tokens, 16/4
+    heads, head_dim 256, 16-slot f16 pages: every output must be finite, and sampled
+    query tokens match the oracle (a single query at position p over the pages is
+    the decode definition with context p + 1)."""
+    import torch
+    from gpu_helpers import assert_attention_close, dev, new_status
+    c = workloads.paged_chunk_full(seed=0)
+    kp, vp, st = _append_gpu(lib, c)
+    assert st == 0
+    status = new_status()
+    out = lib.gqa_attn_paged_prefill(dev(c.q), kp, vp, dev(c.page_table), dev(c.token_offsets),
+                                     dev(c.position_start), 512, c.scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    rng = np.random.default_rng(5)
+    sel = np.sort(rng.choice(c.tokens, 48, replace=False))
+    seq = np.searchsorted(c.token_offsets, sel, side="right") - 1
+    pos = c.position_start[seq] + (sel - c.token_offsets[seq])
+    rk, rv, _ = oracle.paged_append(c.k_new, c.v_new, c.token_offsets, c.position_start,
+                                    c.page_table, c.k_pool, c.v_pool, kv_dtype="f16", **_strides(c))
+    np.testing.assert_array_equal(_bits(kp), rk.view(np.uint16))
+    np.testing.assert_array_equal(_bits(vp), rv.view(np.uint16))
+    ref = oracle.paged_decode(c.q[sel], rk, rv, kv_dtype="f16", page_table=c.page_table[seq],
+                              context_lens=(pos + 1).astype(np.int32), scale=c.scale)
+    assert_attention_close(got[sel], ref, "chunked prefill full size (sampled)")

@@ -320,6 +320,16 @@ def paged_chunk(*, num_seqs: int = 4, tokens_lo: int = 1, tokens_hi: int = 64,
                           table, offs, ps)
 
 
+def paged_chunk_full(seed: int = 0) -> PagedChunkCase:
+    """Chunked prefill shaped like the paged causal-attention pages' model geometry:
+    16 query heads over 4 KV heads of head_dim 256, so one token's K and V take
+    4096 bytes of f16 and a 64 KiB page holds 16 tokens; 8 sequences of 512 new
+    tokens each after a cached prefix of U{0..7680} tokens."""
+    return paged_chunk(num_seqs=8, tokens_lo=512, tokens_hi=512, prefix_lo=0, prefix_hi=7680,
+                       num_pages=4608, page_size=16, n_heads=16, n_kv_heads=4, head_dim=256,
+                       kv_dtype="f16", seed=seed, name="paged_chunk_8seq_512tok_pre0-7680_h16_hk4_d256")
+
+
 # ---------------------------------------------------------------------------
 # DFlash2 ring KV (speculative verify)
 # ---------------------------------------------------------------------------
