@@ -109,7 +109,8 @@ struct Layout {
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kNumVis = kAbort + 4;     // visible tiles of the unit in each list buffer
-    static constexpr int kXchg = kNumVis + 8;      // row-max exchange: [2 tiles][2 halves][128] f32
+    static constexpr int kUid = kNumVis + 8;       // the unit in each list buffer (-1: queue ended)
+    static constexpr int kXchg = kUid + 8;         // row-max exchange: [2 tiles][2 halves][128] f32
     static constexpr int kList = kXchg + 2 * 2 * BM * 4;  // two lists of visible key tiles (uint16)
     static constexpr int kEnd = kList + 2 * 2 * kMaxListTiles;
     static constexpr int kBytes = kEnd;
@@ -158,6 +159,11 @@ struct AttnArgs {
     int64_t pool_page, pool_token, pool_head;  // element strides
     int total_tokens, max_pages, page_size, num_pages, pg_box;
     int pg_dim[3];  // logical coordinate (0 kv head, 1 slot, 2 page) of map dimensions 1..3
+    // dynamic unit queue (unpaired): units in decreasing cost order; each CTA takes
+    // the next one from the counter when it starts a unit.  Null: the static
+    // snake assignment.
+    const int *sched_perm;
+    int *sched_counter;
 };
 
 // A sequence's tokens and start position as read from the device counters,
@@ -425,6 +431,58 @@ __device__ __forceinline__ int paged_tile_code(const AttnArgs &a, const Unit &n,
     return k0 + BN - 1 <= p0 ? 1 : 2;
 }
 
+// Chunked prefill: visible key tiles of unit u, plus one for the unit's own
+// overhead when it has any (the scheduling cost), capped at kCostBins - 1.
+constexpr int kCostBins = 1024;
+__device__ __forceinline__ int paged_unit_cost(const AttnArgs &a, int u) {
+    Unit un = unit_of(a, u, false, 0, 0);
+    set_span(a, un, false);
+    if (un.q_row0 >= un.ntok) return 0;
+    const int p1 = un.ps + min(un.q_row0 + a.rows_per_head, un.ntok) - 1;
+    const int n = max(0, min(un.je, p1 / BN + 1) - un.jb);
+    return min(n + (n > 0 ? 1 : 0), kCostBins - 1);
+}
+
+// One CTA of 1024 threads: counting sort of the units by decreasing cost into
+// sched_perm, and the queue counter reset for the attention launch that follows.
+__global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int units) {
+    __shared__ int bins[kCostBins];
+    __shared__ int wsum[32];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    bins[t] = 0;
+    __syncthreads();
+    for (int u = t; u < units; u += 1024) atomicAdd(&bins[paged_unit_cost(a, u)], 1);
+    __syncthreads();
+    // thread t takes cost c = kCostBins - 1 - t; start[c] = units costing more than c
+    const int c = kCostBins - 1 - t;
+    const int v = bins[c];
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        wsum[lane] = w;
+    }
+    __syncthreads();
+    const int start = x - v + (warp > 0 ? wsum[warp - 1] : 0);
+    __syncthreads();
+    bins[c] = start;
+    __syncthreads();
+    int *perm = const_cast<int *>(a.sched_perm);
+    for (int u = t; u < units; u += 1024) perm[atomicAdd(&bins[paged_unit_cost(a, u)], 1)] = u;
+    if (t == 0) *a.sched_counter = 0;
+}
+
 // The k-th unit of work slot `slot` of `slots` (a slot is a CTA, or a CTA pair):
 // slots take the heavy-first units in snake order (0..S-1, then S-1..0, ...), so
 // that each slot's total work is close to the mean; -1 when the slot is done.
@@ -480,6 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlot);
     volatile int *n_vis_smem = reinterpret_cast<volatile int *>(smem + L::kNumVis);
+    volatile int *uid_smem = reinterpret_cast<volatile int *>(smem + L::kUid);
     float *xchg = reinterpret_cast<float *>(smem + L::kXchg);
     uint16_t *lists = reinterpret_cast<uint16_t *>(smem + L::kList);
     const Waiter wt{abort_flag, a.status, kWaitLimitNs};
@@ -567,15 +626,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const int uid = slot_unit(k, slot, slots, units);
-                if (uid < 0) break;
-                Unit un = unit_of(a, uid, PAIR, rank, DO);
-                if constexpr (PAGED) set_span(a, un, lane == 0);
+                int uid;
+                if (a.sched_perm) {
+                    int idx = 0;
+                    if (lane == 0) idx = atomicAdd(a.sched_counter, 1);
+                    idx = __shfl_sync(0xffffffffu, idx, 0);
+                    uid = idx < units ? a.sched_perm[idx] : -1;
+                } else {
+                    uid = slot_unit(k, slot, slots, units);
+                    if (uid < 0) break;
+                }
                 const int b = k & 1;
                 uint16_t *list = lists + b * kMaxListTiles;
                 // the list buffer of unit k - 2 must have been read by every role
                 if (k >= 2) ok = __all_sync(0xffffffffu, wt.wait(list_free(b), ((k - 2) >> 1) & 1));
                 if (!ok) break;
+                if (uid < 0) {
+                    // the queue is empty: tell the other roles, then stop
+                    if (lane == 0) {
+                        uid_smem[b] = -1;
+                        n_vis_smem[b] = 0;
+                        tc::mbar_arrive(list_full(b));
+                    }
+                    break;
+                }
+                Unit un = unit_of(a, uid, PAIR, rank, DO);
+                if constexpr (PAGED) set_span(a, un, lane == 0);
                 // ring-direct verify: the lane's history length and write position
                 int ring_l = 0, ring_p = 0;
                 if constexpr (RING) {
@@ -600,7 +676,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (uint16_t)((j - un.jb) | (code == 2 ? 0x8000 : 0));
                     n += __popc(vis);
                 }
-                if (lane == 0) n_vis_smem[b] = n;
+                if (lane == 0) {
+                    n_vis_smem[b] = n;
+                    uid_smem[b] = uid;
+                }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(list_full(b));
                 auto tile_at = [&](int v) { return un.jb + (list[v] & 0x7fff); };
@@ -827,9 +906,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int g = 0;        // global index of the unit's first tile
                 int with_o = 0;   // units so far that produced O (one o_free phase each)
                 for (int k = 0; ok; ++k) {
-                    if (slot_unit(k, slot, slots, units) < 0) break;
+                    if (!a.sched_perm && slot_unit(k, slot, slots, units) < 0) break;
                     const int b = k & 1;
                     if (!(ok = wt.wait(list_full(b), (k >> 1) & 1))) break;
+                    if (uid_smem[b] < 0) break;  // the unit queue has ended
                     const int n = n_vis_smem[b];
                     tc::mbar_arrive(list_free(b));
                     if (n == 0) continue;  // no visible key: no loads, no Q, no O
@@ -1061,15 +1141,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 
         int k = 0;
-        int uid = slot_unit(0, slot, slots, units);
+        int uid = -1;
         Unit cur{};
         int cur_n = 0, cur_pos = 0;  // visible tiles and first ring position of unit k
-        if (uid >= 0) {
-            cur = unit_of(a, uid, PAIR, rank, DO);
-            if constexpr (PAGED) set_span(a, cur, false);
+        if (a.sched_perm || slot_unit(0, slot, slots, units) >= 0) {
             ok = __all_sync(0xffffffffu, wt.wait(list_full(0), 0));
-            cur_n = ok ? n_vis_smem[0] : 0;
-            if (ok && cur_n > 0) convert_q(cur, 0, false);
+            uid = ok ? uid_smem[0] : -1;
+            if (uid >= 0) {
+                cur = unit_of(a, uid, PAIR, rank, DO);
+                if constexpr (PAGED) set_span(a, cur, false);
+                cur_n = n_vis_smem[0];
+                if (cur_n > 0) convert_q(cur, 0, false);
+            }
         }
         int g = 0;  // global index of the current unit's first tile
         while (uid >= 0 && ok) {
@@ -1271,7 +1354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- the next unit's Q is converted before this unit's epilogue, so that its
             // first Q.K^T products overlap the epilogue (all of unit k's S are complete:
             // nothing reads the Q staging area any more)
-            const int nuid = slot_unit(k + 1, slot, slots, units);
+            int nuid = -1;
             Unit nxt{};
             int nxt_n = 0;
             const int nxt_pos = cur_pos + (cur_n > 0 ? unit_positions(cur_n) : 0);
@@ -1286,11 +1369,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool stage_o = a.o_tma && cur_n > 0 && (!PAGED || cur.q_row0 + BM <= cur.ntok);
             int o_slot0 = 0;       // first ring position of the staging area
             bool hold_q = false;   // staging in the next unit's Q slots
-            if (nuid >= 0 && ok) {
+            if (ok && (a.sched_perm || slot_unit(k + 1, slot, slots, units) >= 0)) {
+                ok = __all_sync(0xffffffffu, wt.wait(list_full((k + 1) & 1), ((k + 1) >> 1) & 1));
+                nuid = ok ? uid_smem[(k + 1) & 1] : -1;
+            }
+            if (nuid >= 0) {
                 nxt = unit_of(a, nuid, PAIR, rank, DO);
                 if constexpr (PAGED) set_span(a, nxt, false);
-                ok = __all_sync(0xffffffffu, wt.wait(list_full((k + 1) & 1), ((k + 1) >> 1) & 1));
-                nxt_n = ok ? n_vis_smem[(k + 1) & 1] : 0;
+                nxt_n = n_vis_smem[(k + 1) & 1];
                 if constexpr (kHoldQ) {
                     hold_q = stage_o && nxt_n > 0;
                     if (ok && nxt_n > 0) convert_q(nxt, nxt_pos, hold_q);
@@ -1484,6 +1570,7 @@ struct Plan {
     int n_blk, code_cols, code_groups, splits, bps;
     bool shared_mask, pair;
     size_t codes_bytes, part_o_bytes, part_lse_bytes;
+    size_t sched_bytes;  // dynamic unit queue: counter (256 bytes) + order
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -1545,7 +1632,9 @@ Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, i
     return p;
 }
 
-size_t plan_bytes(const Plan &p) { return p.codes_bytes + p.part_o_bytes + p.part_lse_bytes; }
+size_t plan_bytes(const Plan &p) {
+    return p.codes_bytes + p.part_o_bytes + p.part_lse_bytes + p.sched_bytes;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1710,6 +1799,8 @@ static Plan paged_plan(int num_seqs, int max_tokens, int n_heads, int n_kv_heads
     Plan pl = make_plan(num_seqs, max_tokens, n_heads, n_kv_heads, head_dim,
                         max_pages_per_seq * page_size, false);
     pl.codes_bytes = 0;
+    // units differ in cost with each sequence's prefix: a cost-ordered dynamic queue
+    pl.sched_bytes = 256 + align256((size_t)pl.tiles * pl.d_parts * pl.splits * 4);
     return pl;
 }
 
@@ -1752,6 +1843,9 @@ cudaError_t launch_paged_prefill(const PagedPrefillProblem &p, void *workspace, 
     char *ws = static_cast<char *>(workspace);
     a.ws_o = pl.splits > 1 ? reinterpret_cast<float *>(ws) : nullptr;
     a.ws_lse = pl.splits > 1 ? reinterpret_cast<float *>(ws + pl.part_o_bytes) : nullptr;
+    char *sched = ws + pl.part_o_bytes + pl.part_lse_bytes;
+    a.sched_counter = reinterpret_cast<int *>(sched);
+    a.sched_perm = reinterpret_cast<const int *>(sched + 256);
     a.status = p.status;
     a.tok_off = p.token_offsets;
     a.pos_start = p.position_start;
@@ -1794,6 +1888,9 @@ cudaError_t launch_paged_prefill(const PagedPrefillProblem &p, void *workspace, 
     int sms = sm_count();
     if (sms <= 0) sms = 148;
     const int ctas = std::min(units, sms);
+    order_units_kernel<<<1, 1024, 0, stream>>>(a, units);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     const bool bf = a.kv_bf16;
     switch (p.head_dim) {
         case 128:

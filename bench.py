@@ -333,7 +333,8 @@ def setup_chunk(torch, g, c):
     nb = lambda t: t.numel() * t.element_size()
     # append: f32 rows in, 16-bit rows out, for K and V
     append_bytes = nb(kn) + nb(vn) + (nb(kn) + nb(vn)) // 2
-    return step, ops, {"flops": c.flops(), "append_bytes": append_bytes, "launches": 2}
+    # append, unit ordering, attention
+    return step, ops, {"flops": c.flops(), "append_bytes": append_bytes, "launches": 3}
 
 
 # ---------------------------------------------------------------------------
