@@ -443,17 +443,46 @@ __device__ __forceinline__ int paged_unit_cost(const AttnArgs &a, int u) {
     return min(n + (n > 0 ? 1 : 0), kCostBins - 1);
 }
 
-// One CTA of 1024 threads: counting sort of the units by decreasing cost into
-// sched_perm, and the queue counter reset for the attention launch that follows.
+// Unit j of group g = (sequence, KV head) in the queue order: row tiles from the
+// last (the most keys), then head tiles, output halves and key splits.  This
+// inverts unit_of's (unpaired) numbering.
+__device__ __forceinline__ int unit_in_group(const AttnArgs &a, int g, int j) {
+    const int split = j % a.splits;
+    j /= a.splits;
+    const int dpart = j % a.d_parts;
+    j /= a.d_parts;
+    const int ht = j % a.head_tiles;
+    const int rt = a.row_tiles - 1 - j / a.head_tiles;
+    const int lane = g / a.n_kv_heads, kh = g - lane * a.n_kv_heads;
+    const int per_rt = a.lanes * a.n_kv_heads * a.head_tiles;
+    const int tile_id = ((rt * a.lanes + lane) * a.n_kv_heads + kh) * a.head_tiles + ht;
+    const int ut = (a.row_tiles - 1 - rt) * per_rt + tile_id % per_rt;
+    return (ut * a.d_parts + dpart) * a.splits + split;
+}
+
+// queue key of group g: its mean unit cost
+__device__ __forceinline__ int group_key(const AttnArgs &a, int g, int per_group) {
+    int c = 0;
+    for (int j = 0; j < per_group; ++j) c += paged_unit_cost(a, unit_in_group(a, g, j));
+    return min((c + per_group - 1) / per_group, kCostBins - 1);
+}
+
+// One CTA of 1024 threads: the queue order for a chunked prefill.  The units of
+// one (sequence, KV head) group read the same keys and values, so they are queued
+// together (and run at the same time, sharing those bytes through L2); groups go
+// in decreasing order of cost (counting sort), so that the dynamic queue ends
+// with the light ones.  Also resets the queue counter for the attention launch
+// that follows.
 __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int units) {
     __shared__ int bins[kCostBins];
     __shared__ int wsum[32];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int groups = a.lanes * a.n_kv_heads, per_group = units / groups;
     bins[t] = 0;
     __syncthreads();
-    for (int u = t; u < units; u += 1024) atomicAdd(&bins[paged_unit_cost(a, u)], 1);
+    for (int g = t; g < groups; g += 1024) atomicAdd(&bins[group_key(a, g, per_group)], 1);
     __syncthreads();
-    // thread t takes cost c = kCostBins - 1 - t; start[c] = units costing more than c
+    // thread t takes key c = kCostBins - 1 - t; start[c] = groups with a larger key
     const int c = kCostBins - 1 - t;
     const int v = bins[c];
     int x = v;
@@ -479,7 +508,10 @@ __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int
     bins[c] = start;
     __syncthreads();
     int *perm = const_cast<int *>(a.sched_perm);
-    for (int u = t; u < units; u += 1024) perm[atomicAdd(&bins[paged_unit_cost(a, u)], 1)] = u;
+    for (int g = t; g < groups; g += 1024) {
+        const int slot = atomicAdd(&bins[group_key(a, g, per_group)], 1);
+        for (int j = 0; j < per_group; ++j) perm[slot * per_group + j] = unit_in_group(a, g, j);
+    }
     if (t == 0) *a.sched_counter = 0;
 }
 
@@ -731,12 +763,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // are left as they are (their scores are replaced by -inf), their V rows
                 // are zeroed, so that the zero probabilities meet finite values; the V
                 // box holding the context end is copied row by row.
-                auto fill_paged = [&](uint32_t dst, bool is_v, int j, int d0) {
+                auto fill_paged = [&](uint32_t dst, bool is_v, int j, int d0, int page) {
                     const int ctx = un.ps + un.ntok;
                     const int kb = j * BN, key0 = kb + lane * a.pg_box;
                     const bool tma = lane * a.pg_box < BN && key0 < ctx && (!is_v || key0 + a.pg_box <= ctx);
-                    int page = 0;
-                    if (tma) page = page_of(a, un.t.lane, key0);
                     if (is_v && kb + BN > ctx) {
                         uint8_t *img = smem + (dst - sbase);
                         const int m0 = max((ctx / a.pg_box) * a.pg_box - kb, 0);  // first row not by TMA
@@ -772,12 +802,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             d0 + c * 64, c1, c2, c3);
                     }
                 };
+                // chunked prefill: the page of this lane's box of key tile j (its load is
+                // issued a tile ahead of the stages that use it, so that its latency is
+                // not on the producer's path)
+                auto box_page = [&](int j) -> int {
+                    const int key0 = j * BN + lane * a.pg_box;
+                    if (!PAGED || lane * a.pg_box >= BN || key0 >= un.ps + un.ntok) return 0;
+                    return ld_s32(a.page_table + (int64_t)un.t.lane * a.max_pages + key0 / a.page_size);
+                };
+                auto checked = [&](int page) {
+                    if (page < 0 || page >= a.num_pages) {
+                        raise_flag(a.status, GQA_FLAG_PAGE_CLAMPED);
+                        page = page < 0 ? 0 : a.num_pages - 1;
+                    }
+                    return page;
+                };
                 // one stage of K or V: two boxes of [BN rows][64 columns] from column d0
-                auto load = [&](int j, bool is_v, int d0) -> bool {
+                auto load = [&](int j, bool is_v, int d0, int page = 0) -> bool {
                     if (!slot_free()) return false;
                     const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
                     if (PAGED) {
-                        fill_paged(dst, is_v, j, d0);
+                        fill_paged(dst, is_v, j, d0, checked(page));
                     } else if (RING && j == 0) {
                         fill_current(smem + L::kStages + stage * kStageBytes, is_v, d0);
                         tc::fence_async_smem();
@@ -835,11 +880,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (ok) ok = load_half(tile_at(v), true, 0);
                     }
                 } else {
-                    for (int ks = 0; ks < KSUB && ok && n > 0; ++ks) ok = load(tile_at(0), false, ks * 128);
+                    // pages of tiles v and v + 1 (chunked prefill)
+                    int pg_v = n > 0 ? box_page(tile_at(0)) : 0;
+                    int pg_n = n > 1 ? box_page(tile_at(1)) : 0;
+                    for (int ks = 0; ks < KSUB && ok && n > 0; ++ks) ok = load(tile_at(0), false, ks * 128, pg_v);
                     for (int v = 0; ok && v < n; ++v) {
+                        const int pg_nn = v + 2 < n ? box_page(tile_at(v + 2)) : 0;
                         for (int ks = 0; ks < KSUB && ok && v + 1 < n; ++ks)
-                            ok = load(tile_at(v + 1), false, ks * 128);
-                        for (int vs = 0; vs < VSUB && ok; ++vs) ok = load(tile_at(v), true, un.d_off + vs * 128);
+                            ok = load(tile_at(v + 1), false, ks * 128, pg_n);
+                        for (int vs = 0; vs < VSUB && ok; ++vs) ok = load(tile_at(v), true, un.d_off + vs * 128, pg_v);
+                        pg_v = pg_n;
+                        pg_n = pg_nn;
                     }
                 }
             }

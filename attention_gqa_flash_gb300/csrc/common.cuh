@@ -65,6 +65,13 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
                  : "l"(p));
     return r;
 }
+// A 32-bit load issued where it stands in the program (the asm is volatile), so
+// that a value fetched ahead of its use keeps its latency off the critical path.
+__device__ __forceinline__ int ld_s32(const int32_t *p) {
+    int r;
+    asm volatile("ld.global.s32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
 __device__ __forceinline__ float4 ld_nc_f4(const float *p) {
     float4 r;
     asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
