@@ -434,6 +434,7 @@ __device__ __forceinline__ int paged_tile_code(const AttnArgs &a, const Unit &n,
 // Chunked prefill: visible key tiles of unit u, plus one for the unit's own
 // overhead when it has any (the scheduling cost), capped at kCostBins - 1.
 constexpr int kCostBins = 1024;
+constexpr int kMaxQueueGroups = 10240;  // (sequence, KV head) groups the ordering pass handles (40 KiB)
 __device__ __forceinline__ int paged_unit_cost(const AttnArgs &a, int u) {
     Unit un = unit_of(a, u, false, 0, 0);
     set_span(a, un, false);
@@ -460,27 +461,30 @@ __device__ __forceinline__ int unit_in_group(const AttnArgs &a, int g, int j) {
     return (ut * a.d_parts + dpart) * a.splits + split;
 }
 
-// queue key of group g: its mean unit cost
-__device__ __forceinline__ int group_key(const AttnArgs &a, int g, int per_group) {
-    int c = 0;
-    for (int j = 0; j < per_group; ++j) c += paged_unit_cost(a, unit_in_group(a, g, j));
-    return min((c + per_group - 1) / per_group, kCostBins - 1);
-}
-
 // One CTA of 1024 threads: the queue order for a chunked prefill.  The units of
 // one (sequence, KV head) group read the same keys and values, so they are queued
 // together (and run at the same time, sharing those bytes through L2); groups go
-// in decreasing order of cost (counting sort), so that the dynamic queue ends
-// with the light ones.  Also resets the queue counter for the attention launch
-// that follows.
+// in decreasing order of their mean unit cost (counting sort), so that the
+// dynamic queue ends with the light ones.  Also resets the queue counter for the
+// attention launch that follows.  Dynamic shared memory: one int per group.
 __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int units) {
     __shared__ int bins[kCostBins];
     __shared__ int wsum[32];
+    extern __shared__ int gval[];  // group cost, then the group's place in the queue
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int groups = a.lanes * a.n_kv_heads, per_group = units / groups;
     bins[t] = 0;
+    for (int g = t; g < groups; g += 1024) gval[g] = 0;
     __syncthreads();
-    for (int g = t; g < groups; g += 1024) atomicAdd(&bins[group_key(a, g, per_group)], 1);
+    for (int u = t; u < units; u += 1024) {
+        const Unit un = unit_of(a, u, false, 0, 0);
+        atomicAdd(&gval[un.t.lane * a.n_kv_heads + un.t.kh], paged_unit_cost(a, u));
+    }
+    __syncthreads();
+    for (int g = t; g < groups; g += 1024) {
+        gval[g] = min((gval[g] + per_group - 1) / per_group, kCostBins - 1);
+        atomicAdd(&bins[gval[g]], 1);
+    }
     __syncthreads();
     // thread t takes key c = kCostBins - 1 - t; start[c] = groups with a larger key
     const int c = kCostBins - 1 - t;
@@ -507,10 +511,12 @@ __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int
     __syncthreads();
     bins[c] = start;
     __syncthreads();
+    for (int g = t; g < groups; g += 1024) gval[g] = atomicAdd(&bins[gval[g]], 1);
+    __syncthreads();
     int *perm = const_cast<int *>(a.sched_perm);
-    for (int g = t; g < groups; g += 1024) {
-        const int slot = atomicAdd(&bins[group_key(a, g, per_group)], 1);
-        for (int j = 0; j < per_group; ++j) perm[slot * per_group + j] = unit_in_group(a, g, j);
+    for (int i = t; i < units; i += 1024) {
+        const int g = i / per_group, j = i - g * per_group;
+        perm[gval[g] * per_group + j] = unit_in_group(a, g, j);
     }
     if (t == 0) *a.sched_counter = 0;
 }
@@ -1939,9 +1945,15 @@ cudaError_t launch_paged_prefill(const PagedPrefillProblem &p, void *workspace, 
     int sms = sm_count();
     if (sms <= 0) sms = 148;
     const int ctas = std::min(units, sms);
-    order_units_kernel<<<1, 1024, 0, stream>>>(a, units);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    const int groups = p.num_seqs * p.n_kv_heads;
+    if (groups <= kMaxQueueGroups) {
+        order_units_kernel<<<1, 1024, groups * sizeof(int), stream>>>(a, units);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    } else {
+        a.sched_perm = nullptr;  // too many groups for one CTA's table: static snake order
+        a.sched_counter = nullptr;
+    }
     const bool bf = a.kv_bf16;
     switch (p.head_dim) {
         case 128:
