@@ -139,7 +139,7 @@ struct AttnArgs {
     const uint8_t *codes;  // [code groups][code_cols] per 64 keys: 0 skip, 1 no mask, 2 mixed
     int code_cols;
     int shared_mask;  // mask identical for all heads: code group = (lane, row tile)
-    float *ws_o;      // split partials [unit][BM][DO]
+    float *ws_o;      // split partials [unit][DO / 4][BM] float4 (a warp's rows are adjacent)
     float *ws_lse;    // [unit][BM]
     int32_t *status;
     // ring-direct verify: key tile 0 holds the lane's current rows (converted from
@@ -148,6 +148,11 @@ struct AttnArgs {
     // position instead of a mask
     int ring, ring_w, ring_r;
     const float *cur_k, *cur_v;           // [lanes][ring_r][n_kv_heads][head_dim]
+    // the current rows rounded to bf16 by the pre-pass, [K|V][lanes * n_kv_heads][ring_r]
+    // [head_dim]; key tile 0 loads them by TMA (rows ring_r..127 are out of the map's
+    // bounds and arrive as zeros)
+    uint16_t *cur16;
+    int head_dim;
     const uint32_t *ring_len, *ring_wp;   // [lanes]
     // chunked prefill over pages: a unit's lane is a sequence s whose tokens are
     // rows tok_off[s] .. tok_off[s+1]-1 of Q and O (at most `rows` of them), query
@@ -164,6 +169,17 @@ struct AttnArgs {
     // snake assignment.
     const int *sched_perm;
     int *sched_counter;
+    // key splits over the visible tiles (ring-direct verify): every split of a tile
+    // scans all key tiles and takes the split-th of `splits` equal shares of the
+    // visible ones, instead of a fixed range of tiles
+    int vis_split;
+    // ring-direct verify with splits over the visible tiles: the pre-pass gives lane l
+    // lane_splits[l] of the `splits` split slots, in proportion to its visible tiles
+    // (split_budget of them per KV head in all, about one unit per SM), queues only
+    // those units (queue_len of them) and numbers their partial results in queue
+    // order: part_slot[(tile * d_parts + dpart) * splits + split]
+    int *lane_splits, *queue_len, *part_slot;
+    int split_budget;
 };
 
 // A sequence's tokens and start position as read from the device counters,
@@ -401,8 +417,8 @@ __device__ __forceinline__ Unit unit_of(const AttnArgs &a, int u, bool pair, uin
     n.t = tile_of(a, n.tile_id);
     n.cg = code_group(a, n.t);
     n.d_off = n.dpart * d_out;
-    n.jb = n.split * a.blk_per_split;
-    n.je = min(a.n_blk, n.jb + a.blk_per_split);
+    n.jb = a.vis_split ? 0 : n.split * a.blk_per_split;
+    n.je = a.vis_split ? a.n_blk : min(a.n_blk, n.jb + a.blk_per_split);
     n.head_idx = n.t.lane * a.n_kv_heads + n.t.kh;
     n.q_head0 = n.t.kh * a.group + n.t.ht * a.heads_per_tile;
     n.q_row0 = n.t.rt * a.rows_per_head;
@@ -431,16 +447,28 @@ __device__ __forceinline__ int paged_tile_code(const AttnArgs &a, const Unit &n,
     return k0 + BN - 1 <= p0 ? 1 : 2;
 }
 
-// Chunked prefill: visible key tiles of unit u, plus one for the unit's own
-// overhead when it has any (the scheduling cost), capped at kCostBins - 1.
+// Key tiles unit u visits (chunked prefill, or ring-direct verify with splits
+// over the visible tiles), plus one for the unit's own overhead when it has any
+// (the scheduling cost), capped at kCostBins - 1.
 constexpr int kCostBins = 1024;
 constexpr int kMaxQueueGroups = 10240;  // (sequence, KV head) groups the ordering pass handles (40 KiB)
-__device__ __forceinline__ int paged_unit_cost(const AttnArgs &a, int u) {
+__device__ __forceinline__ int unit_cost(const AttnArgs &a, int u) {
     Unit un = unit_of(a, u, false, 0, 0);
-    set_span(a, un, false);
-    if (un.q_row0 >= un.ntok) return 0;
-    const int p1 = un.ps + min(un.q_row0 + a.rows_per_head, un.ntok) - 1;
-    const int n = max(0, min(un.je, p1 / BN + 1) - un.jb);
+    int n;
+    if (a.ring) {
+        const int L = (int)min(a.ring_len[un.t.lane], (uint32_t)a.ring_w);
+        const int wp = (int)(a.ring_wp[un.t.lane] % (uint32_t)a.ring_w);
+        int all = 0;
+        for (int j = 0; j < a.n_blk; ++j) all += ring_tile_code(a, j, L, wp) != 0;
+        const int S = a.lane_splits ? a.lane_splits[un.t.lane] : a.splits;
+        if (un.split >= S) return 0;
+        n = (int)((int64_t)(un.split + 1) * all / S) - (int)((int64_t)un.split * all / S);
+    } else {
+        set_span(a, un, false);
+        if (un.q_row0 >= un.ntok) return 0;
+        const int p1 = un.ps + min(un.q_row0 + a.rows_per_head, un.ntok) - 1;
+        n = max(0, min(un.je, p1 / BN + 1) - un.jb);
+    }
     return min(n + (n > 0 ? 1 : 0), kCostBins - 1);
 }
 
@@ -472,13 +500,108 @@ __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int
     __shared__ int wsum[32];
     extern __shared__ int gval[];  // group cost, then the group's place in the queue
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    if (blockIdx.x > 0) {
+        // ring-direct verify: the current K and V rows rounded to bf16 (8 per thread step)
+        const int cpr = a.head_dim / 8;
+        const int64_t per = (int64_t)a.lanes * a.ring_r * a.n_kv_heads * cpr;
+        for (int64_t i = (int64_t)(blockIdx.x - 1) * 1024 + t; i < 2 * per; i += (int64_t)(gridDim.x - 1) * 1024) {
+            const int which = (int)(i / per);
+            int64_t r = i - which * per;
+            const int ch = (int)(r % cpr);
+            r /= cpr;
+            const int g = (int)(r % a.n_kv_heads);
+            r /= a.n_kv_heads;
+            const int row = (int)(r % a.ring_r), ln = (int)(r / a.ring_r);
+            const float *src = (which ? a.cur_v : a.cur_k) +
+                               (((int64_t)ln * a.ring_r + row) * a.n_kv_heads + g) * a.head_dim + ch * 8;
+            const float4 x = ld_nc_f4(src), y = ld_nc_f4(src + 4);
+            uint16_t *dst = a.cur16 + (((which * (int64_t)a.lanes + ln) * a.n_kv_heads + g) * a.ring_r + row) *
+                                          a.head_dim + ch * 8;
+            st_v4(dst, make_uint4(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w), pack_bf16x2(y.x, y.y),
+                                  pack_bf16x2(y.z, y.w)));
+        }
+        return;
+    }
+    if (!a.sched_perm) return;
+    if (a.lane_splits) {
+        // ring-direct verify: split slots per lane in proportion to its visible tiles, then
+        // a counting sort of the units in use by decreasing cost
+        __shared__ int s_vis[64];
+        __shared__ int s_real;
+        if (t < a.lanes) {
+            const int L = (int)min(a.ring_len[t], (uint32_t)a.ring_w);
+            const int wp = (int)(a.ring_wp[t] % (uint32_t)a.ring_w);
+            int vis = 0;
+            for (int j = 0; j < a.n_blk; ++j) vis += ring_tile_code(a, j, L, wp) != 0;
+            s_vis[t] = vis;
+        }
+        bins[t] = 0;
+        if (t == 0) s_real = 0;
+        __syncthreads();
+        if (t == 0) {
+            int total = 0;
+            for (int l = 0; l < a.lanes; ++l) total += s_vis[l];
+            for (int l = 0; l < a.lanes; ++l) {
+                int S = (int)((int64_t)s_vis[l] * a.split_budget / max(total, 1));
+                S = min(max(S, 1), min(a.splits, max(s_vis[l], 1)));
+                a.lane_splits[l] = S;
+            }
+        }
+        __syncthreads();
+        for (int u = t; u < units; u += 1024) {
+            const int c = unit_cost(a, u);
+            if (c > 0) {
+                atomicAdd(&bins[c], 1);
+                atomicAdd(&s_real, 1);
+            }
+        }
+        __syncthreads();
+        const int c = kCostBins - 1 - t;
+        const int v = c > 0 ? bins[c] : 0;
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            wsum[lane] = w;
+        }
+        __syncthreads();
+        const int start = x - v + (warp > 0 ? wsum[warp - 1] : 0);
+        __syncthreads();
+        bins[c] = start;
+        __syncthreads();
+        int *perm = const_cast<int *>(a.sched_perm);
+        for (int u = t; u < units; u += 1024) {
+            const int cu = unit_cost(a, u);
+            if (cu == 0) continue;
+            const int pos = atomicAdd(&bins[cu], 1);
+            perm[pos] = u;
+            const Unit un = unit_of(a, u, false, 0, 0);
+            a.part_slot[((int64_t)un.tile_id * a.d_parts + un.dpart) * a.splits + un.split] = pos;
+        }
+        if (t == 0) {
+            *a.queue_len = s_real;
+            *a.sched_counter = 0;
+        }
+        return;
+    }
     const int groups = a.lanes * a.n_kv_heads, per_group = units / groups;
     bins[t] = 0;
     for (int g = t; g < groups; g += 1024) gval[g] = 0;
     __syncthreads();
     for (int u = t; u < units; u += 1024) {
         const Unit un = unit_of(a, u, false, 0, 0);
-        atomicAdd(&gval[un.t.lane * a.n_kv_heads + un.t.kh], paged_unit_cost(a, u));
+        atomicAdd(&gval[un.t.lane * a.n_kv_heads + un.t.kh], unit_cost(a, u));
     }
     __syncthreads();
     for (int g = t; g < groups; g += 1024) {
@@ -663,13 +786,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             bool ok = true;
+            const int qlen = a.queue_len ? *a.queue_len : units;
             for (int k = 0; ok; ++k) {
                 int uid;
                 if (a.sched_perm) {
                     int idx = 0;
                     if (lane == 0) idx = atomicAdd(a.sched_counter, 1);
                     idx = __shfl_sync(0xffffffffu, idx, 0);
-                    uid = idx < units ? a.sched_perm[idx] : -1;
+                    uid = idx < qlen ? a.sched_perm[idx] : -1;
                 } else {
                     uid = slot_unit(k, slot, slots, units);
                     if (uid < 0) break;
@@ -701,18 +825,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ring_p = (int)(rp % (uint32_t)a.ring_w);
                 }
                 // visible key tiles in order: (j - jb) | 0x8000 when the mask applies
-                int n = 0;
+                auto code_of = [&](int j) {
+                    return j >= un.je ? 0
+                           : RING     ? ring_tile_code(a, j, ring_l, ring_p)
+                           : PAGED    ? paged_tile_code(a, un, j)
+                                      : tile_code(a, un.cg, j);
+                };
+                // splits over the visible tiles: this unit keeps visible tiles [lo, hi)
+                int lo = 0, hi = 0x7fffffff;
+                if (a.vis_split) {
+                    int all = 0;
+                    for (int base = un.jb; base < un.je; base += 32)
+                        all += __popc(__ballot_sync(0xffffffffu, code_of(base + lane) != 0));
+                    const int S = a.lane_splits ? a.lane_splits[un.t.lane] : a.splits;
+                    lo = (int)((int64_t)un.split * all / S);
+                    hi = (int)((int64_t)(un.split + 1) * all / S);
+                }
+                int n = 0, seen = 0;
                 for (int base = un.jb; base < un.je; base += 32) {
                     const int j = base + lane;
-                    const int code = j >= un.je ? 0
-                                     : RING  ? ring_tile_code(a, j, ring_l, ring_p)
-                                     : PAGED ? paged_tile_code(a, un, j)
-                                             : tile_code(a, un.cg, j);
+                    const int code = code_of(j);
                     const unsigned vis = __ballot_sync(0xffffffffu, code != 0);
-                    if (code)
-                        list[n + __popc(vis & ((1u << lane) - 1u))] =
+                    const int idx = seen + __popc(vis & ((1u << lane) - 1u));
+                    const bool keep = code != 0 && idx >= lo && idx < hi;
+                    const unsigned kept = __ballot_sync(0xffffffffu, keep);
+                    if (keep)
+                        list[n + __popc(kept & ((1u << lane) - 1u))] =
                             (uint16_t)((j - un.jb) | (code == 2 ? 0x8000 : 0));
-                    n += __popc(vis);
+                    n += __popc(kept);
+                    seen += __popc(vis);
                 }
                 if (lane == 0) {
                     n_vis_smem[b] = n;
@@ -744,24 +885,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     next();
                 }
-                // the current rows of a ring-direct verify as one key tile: rows < ring_r
-                // from f32 (rounded to bf16), the rest zero; two [128 rows][64 columns]
-                // boxes from column d0, 128-byte swizzle
-                auto fill_current = [&](uint8_t *dst, bool is_v, int d0) {
-                    const float *src = (is_v ? a.cur_v : a.cur_k) +
-                                       ((int64_t)un.t.lane * a.ring_r * a.n_kv_heads + un.t.kh) * D + d0;
-                    for (int q = lane; q < BN * 16; q += 32) {
-                        const int row = q >> 4, c = (q >> 3) & 1, ch = q & 7;
-                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                        if (row < a.ring_r) {
-                            const float *p = src + (int64_t)row * a.n_kv_heads * D + c * 64 + ch * 8;
-                            const float4 x0 = ld_nc_f4(p), x1 = ld_nc_f4(p + 4);
-                            v = make_uint4(pack2(KV{}, x0.x, x0.y), pack2(KV{}, x0.z, x0.w),
-                                           pack2(KV{}, x1.x, x1.y), pack2(KV{}, x1.z, x1.w));
-                        }
-                        *reinterpret_cast<uint4 *>(dst + c * 16384 + sw128(row, ch)) = v;
-                    }
-                };
                 // chunked prefill: one stage of K or V of key tile j over the sequence's
                 // pages, as BN / pg_box boxes of [pg_box slots][64 columns] (pg_box divides
                 // the page size, so no box straddles two pages), each lane issuing one.
@@ -830,10 +953,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (PAGED) {
                         fill_paged(dst, is_v, j, d0, checked(page));
                     } else if (RING && j == 0) {
-                        fill_current(smem + L::kStages + stage * kStageBytes, is_v, d0);
-                        tc::fence_async_smem();
-                        __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(full(stage));
+                        // the current rows (bf16, padded with zero rows by the tensor map)
+                        if (lane == 0) {
+                            tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
+#pragma unroll
+                            for (int c = 0; c < 2; ++c)
+                                tc::tma_load_3d(dst + c * (BN * 128), is_v ? (const void *)&tmo : (const void *)&tmq,
+                                                full(stage), d0 + c * 64, 0, un.head_idx);
+                        }
                     } else if (lane == 0) {
                         tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
                         const int rows_dim1 = is_v ? a.v_rows_dim1 : a.k_rows_dim1;
@@ -1517,9 +1644,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       (int64_t)(cur.t0 + row) * a.o_row + cur.d_off + h * (DO / 2)
                                 : nullptr;
                 } else {
-                    const int64_t unit = ((int64_t)cur.tile_id * a.d_parts + cur.dpart) * a.splits + cur.split;
-                    dst = a.ws_o + (unit * BM + r) * DO + h * (DO / 2);
-                    if (h == 0) a.ws_lse[unit * BM + r] = l > 0.f ? m_ref + __log2f(l) : kNegInf;
+                    // partials column-chunk major: the 32 rows of a warp store 512
+                    // contiguous bytes per instruction
+                    int64_t unit = ((int64_t)cur.tile_id * a.d_parts + cur.dpart) * a.splits + cur.split;
+                    if (a.part_slot) unit = a.part_slot[unit];
+                    dst = nullptr;
+                    if (valid) {
+                        if (h == 0) a.ws_lse[unit * BM + r] = l > 0.f ? m_ref + __log2f(l) : kNegInf;
+                        float4 *base = reinterpret_cast<float4 *>(a.ws_o) + (unit * (DO / 4) + h * (DO / 8)) * BM + r;
+#pragma unroll
+                        for (int cb = 0; cb < NCB; ++cb)
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4) {
+                                asm volatile("" : "+r"(rr[cb][e]), "+r"(rr[cb][e + 1]), "+r"(rr[cb][e + 2]),
+                                             "+r"(rr[cb][e + 3]));
+                                base[(cb * 8 + e / 4) * BM] =
+                                    make_float4(__uint_as_float(rr[cb][e]) * inv, __uint_as_float(rr[cb][e + 1]) * inv,
+                                                __uint_as_float(rr[cb][e + 2]) * inv,
+                                                __uint_as_float(rr[cb][e + 3]) * inv);
+                            }
+                    }
                 }
                 if (dst) {
 #pragma unroll
@@ -1591,19 +1735,26 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a, int
         row += q.t0;
     }
     const int64_t u0 = ((int64_t)tile_id * a.d_parts + dpart) * a.splits;
+    // the splits in use and where their partials are
+    const int S = a.lane_splits ? a.lane_splits[t.lane] : a.splits;
+    auto slot = [&](int s) -> int64_t { return a.part_slot ? a.part_slot[u0 + s] : u0 + s; };
     float M = kNegInf;
-    for (int s = 0; s < a.splits; ++s) M = fmaxf(M, a.ws_lse[(u0 + s) * BM + r]);
+    for (int s = 0; s < S; ++s) M = fmaxf(M, a.ws_lse[slot(s) * BM + r]);
     float acc[DO / 32];
 #pragma unroll
     for (int k = 0; k < DO / 32; ++k) acc[k] = 0.f;
     float L = 0.f;
     if (M != kNegInf) {
-        for (int s = 0; s < a.splits; ++s) {
-            const float w = ex2(a.ws_lse[(u0 + s) * BM + r] - M);
+        for (int s = 0; s < S; ++s) {
+            const float w = ex2(a.ws_lse[slot(s) * BM + r] - M);
             L += w;
-            const float *src = a.ws_o + ((u0 + s) * BM + r) * DO;
+            // [unit][DO / 4][BM] float4: column c of row r at ((unit * DO/4 + c/4) * BM + r) * 4 + c % 4
+            const float *src = a.ws_o + (slot(s) * (DO / 4) * BM + r) * 4;
 #pragma unroll
-            for (int k = 0; k < DO / 32; ++k) acc[k] += w * src[lane + 32 * k];
+            for (int k = 0; k < DO / 32; ++k) {
+                const int c = lane + 32 * k;
+                acc[k] += w * src[(int64_t)(c >> 2) * BM * 4 + (c & 3)];
+            }
         }
     }
     float *out = a.o + t.lane * a.o_lane + (int64_t)head * a.o_head + (int64_t)row * a.o_row +
@@ -1625,9 +1776,12 @@ struct Plan {
     int bn, do_, d_parts;
     int rows_per_head, heads_per_tile, row_tiles, head_tiles, tiles;
     int n_blk, code_cols, code_groups, splits, bps;
-    bool shared_mask, pair;
+    bool shared_mask, pair, vis_split;
+    int split_budget;
+    size_t part_slots;  // split partial slots in the workspace
     size_t codes_bytes, part_o_bytes, part_lse_bytes;
     size_t sched_bytes;  // dynamic unit queue: counter (256 bytes) + order
+    size_t cur_bytes;    // ring-direct verify: the current rows in bf16
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -1646,7 +1800,8 @@ bool pairable(int rows, int n_heads, int n_kv_heads, int head_dim, bool shared_m
 }
 
 Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, int n_keys,
-               bool shared_mask) {
+               bool shared_mask, bool ring = false) {
+    const bool vis_split = ring;
     Plan p{};
     p.bn = BN;
     p.do_ = head_dim == 512 ? 256 : head_dim;
@@ -1670,27 +1825,51 @@ Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, i
     if (sms <= 0) sms = 148;
     if (p.pair) sms /= 2;
     p.splits = 1;
-    if (units < sms && p.n_blk > 1) {
+    // (the unit queue of the ordering pass is required: its group table and the lane
+    // split counts in the queue header bound the lanes and groups)
+    p.vis_split = vis_split && !p.pair && p.n_blk <= kMaxListTiles && lanes <= 60 &&
+                  lanes * n_kv_heads <= kMaxQueueGroups;
+    if (p.vis_split) {
+        // splits share out each tile's visible key tiles: at most sms / n_kv_heads per
+        // lane (the pre-pass hands them out in proportion to the lanes' visible tiles,
+        // about one unit per SM in all)
+        int s = sms / n_kv_heads;
+        p.split_budget = s < 1 ? 1 : s;
+        p.splits = p.split_budget > p.n_blk ? p.n_blk : p.split_budget;
+        p.bps = p.n_blk;
+    } else if (units < sms && p.n_blk > 1) {
         // one CTA per SM at most: a CTA past the SM count would run as a second wave and
         // double the time of the whole launch
         int s = sms / units;
         if (s > p.n_blk) s = p.n_blk;
         p.splits = s;
     }
-    p.bps = (p.n_blk + p.splits - 1) / p.splits;
-    if (p.bps > kMaxListTiles) p.bps = kMaxListTiles;  // a unit's tile list fits in shared memory
-    p.splits = (p.n_blk + p.bps - 1) / p.bps;
+    if (!p.vis_split) {
+        p.bps = (p.n_blk + p.splits - 1) / p.splits;
+        if (p.bps > kMaxListTiles) p.bps = kMaxListTiles;  // a unit's tile list fits in shared memory
+        p.splits = (p.n_blk + p.bps - 1) / p.bps;
+    }
     p.codes_bytes = align256((size_t)p.code_groups * p.code_cols);
     if (p.splits > 1) {
-        const size_t nunits = (size_t)p.tiles * p.d_parts * p.splits;
+        size_t nunits = (size_t)p.tiles * p.d_parts * p.splits;
+        // splits over the visible tiles: at most split_budget + 1 per (lane, KV head) group
+        // are in use, fewer than the split slots
+        if (p.vis_split) {
+            const size_t used = (size_t)lanes * n_kv_heads * (p.split_budget + 1) * p.d_parts;
+            if (used < nunits) nunits = used;
+        }
+        p.part_slots = nunits;
         p.part_o_bytes = align256(nunits * BM * p.do_ * 4);
         p.part_lse_bytes = align256(nunits * BM * 4);
     }
+    if (p.vis_split)  // counter, queue length, lane split counts; order; partial slots
+        p.sched_bytes = 256 + 2 * align256((size_t)p.tiles * p.d_parts * p.splits * 4);
+    if (ring) p.cur_bytes = align256((size_t)2 * lanes * n_kv_heads * rows * head_dim * 2);
     return p;
 }
 
 size_t plan_bytes(const Plan &p) {
-    return p.codes_bytes + p.part_o_bytes + p.part_lse_bytes + p.sched_bytes;
+    return p.codes_bytes + p.part_o_bytes + p.part_lse_bytes + p.sched_bytes + p.cur_bytes;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1846,7 +2025,7 @@ int ring_keys(int window) { return BN + window; }
 
 size_t verify_ring_workspace_bytes(const gqa_ring_params &p) {
     return plan_bytes(make_plan((int)p.lanes, (int)p.rows, (int)p.q_heads, (int)p.kv_heads,
-                                (int)p.head_dim, ring_keys((int)p.window), false));
+                                (int)p.head_dim, ring_keys((int)p.window), false, true));
 }
 
 // Chunked prefill: sequences are the lanes, max_tokens their rows, the key space
@@ -1970,7 +2149,7 @@ cudaError_t launch_paged_prefill(const PagedPrefillProblem &p, void *workspace, 
 cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t stream) {
     const bool shared = !p.ring && p.mask_head_stride == 0;
     const int n_keys = p.ring ? ring_keys(p.ring_w) : p.n_keys;
-    const Plan pl = make_plan(p.lanes, p.rows, p.n_heads, p.n_kv_heads, p.head_dim, n_keys, shared);
+    const Plan pl = make_plan(p.lanes, p.rows, p.n_heads, p.n_kv_heads, p.head_dim, n_keys, shared, p.ring);
     AttnArgs a{};
     a.q = p.q;
     a.q_f32 = p.q_is_f32 ? 1 : 0;
@@ -2016,6 +2195,23 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     a.codes = reinterpret_cast<uint8_t *>(ws);
     a.ws_o = pl.splits > 1 ? reinterpret_cast<float *>(ws + pl.codes_bytes) : nullptr;
     a.ws_lse = pl.splits > 1 ? reinterpret_cast<float *>(ws + pl.codes_bytes + pl.part_o_bytes) : nullptr;
+    a.vis_split = pl.vis_split ? 1 : 0;
+    if (pl.sched_bytes) {
+        char *sched = ws + pl.codes_bytes + pl.part_o_bytes + pl.part_lse_bytes;
+        a.sched_counter = reinterpret_cast<int *>(sched);
+        a.sched_perm = reinterpret_cast<const int *>(sched + 256);
+        if (pl.vis_split) {
+            a.queue_len = reinterpret_cast<int *>(sched + 4);
+            a.lane_splits = reinterpret_cast<int *>(sched + 8);
+            a.part_slot = reinterpret_cast<int *>(sched + 256 +
+                                                  align256((size_t)pl.tiles * pl.d_parts * pl.splits * 4));
+            a.split_budget = pl.split_budget;
+        }
+    }
+    a.head_dim = p.head_dim;
+    if (p.ring)
+        a.cur16 = reinterpret_cast<uint16_t *>(ws + pl.codes_bytes + pl.part_o_bytes + pl.part_lse_bytes +
+                                               pl.sched_bytes);
     a.status = p.status;
 
     // K, V (and, for single-head 128-row prefill tiles, f32 Q and O) tensor maps
@@ -2063,6 +2259,25 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     if (p.ring) {
         // ring-direct verify: bf16 rings, head_dim 128 or 256, unpaired
         if (!bf || pl.pair) return cudaErrorInvalidValue;
+        const int groups = p.lanes * p.n_kv_heads;
+        if (groups > kMaxQueueGroups) {
+            a.sched_perm = nullptr;
+            a.sched_counter = nullptr;
+        }
+        // key tile 0: the current rows in bf16, [lanes * kv heads][rows][head_dim], read in
+        // boxes of 128 rows (the rows past `rows` are out of bounds: zeros)
+        const int kvh = p.lanes * p.n_kv_heads;
+        const size_t half = (size_t)kvh * p.rows * p.head_dim;
+        if (!make_map(&maps[2], a.cur16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.head_dim, p.rows, kvh,
+                      p.head_dim, (int64_t)p.rows * p.head_dim, 64, BM) ||
+            !make_map(&maps[3], a.cur16 + half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.head_dim, p.rows,
+                      kvh, p.head_dim, (int64_t)p.rows * p.head_dim, 64, BM))
+            return cudaErrorInvalidValue;
+        const int64_t chunks = (int64_t)2 * half / 8;
+        const int conv = (int)std::min<int64_t>(64, (chunks + 1023) / 1024);
+        order_units_kernel<<<1 + conv, 1024, (a.sched_perm ? groups : 1) * sizeof(int), stream>>>(a, units);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
         if (p.head_dim == 128) return run_attn<128, BF16, false, kRingMode>(a, maps, ctas, pl.tiles, stream);
         if (p.head_dim == 256) return run_attn<256, BF16, false, kRingMode>(a, maps, ctas, pl.tiles, stream);
         return cudaErrorInvalidValue;
