@@ -108,7 +108,14 @@ cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
 
 void timing_mark(bool before, cudaStream_t stream) {
     if (!g_timing) return;
-    cudaEventRecord(before ? g_ev_start : g_ev_stop, stream);
+    cudaEvent_t ev = before ? g_ev_start : g_ev_stop;
+    // under stream capture the record becomes an event node of the graph, so that
+    // every replay records the kernel's time
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (stream && cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
+    else
+        cudaEventRecord(ev, stream);
     if (!before) g_timing_recorded = true;
 }
 

@@ -879,9 +879,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
 #pragma unroll
                         for (int bx = 0; bx < 2; ++bx)
-                            tc::tma_load_3d(dst + bx * 16384, &tmq, full(stage), qs * 64 + bx * 32,
-                                            a.q_rows_dim1 ? un.t0 + un.q_row0 : un.q_head0,
-                                            a.q_rows_dim1 ? un.q_head0 : un.t0 + un.q_row0);
+                            if constexpr (RING)  // {d, rows, heads, lanes}: 128 / rows heads x rows
+                                tc::tma_load_4d(dst + bx * 16384, &tmq, full(stage), qs * 64 + bx * 32, 0,
+                                                un.q_head0, un.t.lane);
+                            else
+                                tc::tma_load_3d(dst + bx * 16384, &tmq, full(stage), qs * 64 + bx * 32,
+                                                a.q_rows_dim1 ? un.t0 + un.q_row0 : un.q_head0,
+                                                a.q_rows_dim1 ? un.q_head0 : un.t0 + un.q_row0);
                     }
                     next();
                 }
@@ -953,13 +957,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (PAGED) {
                         fill_paged(dst, is_v, j, d0, checked(page));
                     } else if (RING && j == 0) {
-                        // the current rows (bf16, padded with zero rows by the tensor map)
+                        // the current rows (bf16, padded with zero rows by the tensor map; K of
+                        // all heads, then V)
                         if (lane == 0) {
                             tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
 #pragma unroll
                             for (int c = 0; c < 2; ++c)
-                                tc::tma_load_3d(dst + c * (BN * 128), is_v ? (const void *)&tmo : (const void *)&tmq,
-                                                full(stage), d0 + c * 64, 0, un.head_idx);
+                                tc::tma_load_3d(dst + c * (BN * 128), &tmo, full(stage), d0 + c * 64, 0,
+                                                (is_v ? a.lanes * a.n_kv_heads : 0) + un.head_idx);
                         }
                     } else if (lane == 0) {
                         tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
@@ -1288,9 +1293,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     put_q(cb, w);
                 }
+            } else if constexpr (!C::QTM) {
+                // f32 Q without TMA, Q in shared memory: each warp converts its 32 rows'
+                // half (the columns its threads own), a row per load instruction -- eight
+                // lanes per 32-column segment, so a warp reads whole 128-byte lines (a
+                // thread-per-row load would touch 32 rows per instruction) -- with every
+                // load of the warp in flight at once
+                constexpr int SEG = D / 64;           // 32-column segments of a row half
+                constexpr int PER = SEG * 32 / 128;   // float4 loads per lane per row
+                const int rbase = (warp & 3) * 32;
+                // rows that carry no query load row 0 of the tensor (any valid address) and
+                // are zeroed at conversion, so that no load result is consumed before all
+                // loads are issued
+                float4 x[32][PER];
+                uint32_t rows_ok = 0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    int hd = 0, rw = 0;
+                    const bool ok_row = row_of(a, un.t, rbase + j, hd, rw) && rw < un.ntok;
+                    rows_ok |= (ok_row ? 1u : 0u) << j;
+                    const float *src = static_cast<const float *>(a.q) +
+                                       (ok_row ? un.t.lane * a.q_lane + (int64_t)hd * a.q_head +
+                                                     (int64_t)(un.t0 + rw) * a.q_row
+                                               : 0) +
+                                       h * 32 + (lane & 7) * 4;
+#pragma unroll
+                    for (int k = 0; k < PER; ++k) x[j][k] = ld_nc_f4(src + (lane / 8 + 4 * k) * 64);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+#pragma unroll
+                    for (int k = 0; k < PER; ++k) {
+                        const int cb = lane / 8 + 4 * k, rr = rbase + j;
+                        const bool ok_row = (rows_ok >> j) & 1u;
+                        *reinterpret_cast<uint2 *>(smem + L::kQ + cb * (BM * 128) + sw128(rr, h * 4 + (lane & 7) / 2) +
+                                                   (lane & 1) * 8) =
+                            ok_row ? make_uint2(pack2(KV{}, x[j][k].x, x[j][k].y), pack2(KV{}, x[j][k].z, x[j][k].w))
+                                   : make_uint2(0u, 0u);
+                    }
             } else {
-                // f32 Q without TMA: each thread reads its half of its own row, every load
-                // in flight at once, then converts and stores the blocks
+                // f32 Q without TMA, Q in tensor memory: each thread reads its half of its
+                // own row (its TMEM lane), every load in flight at once, then converts and
+                // stores the blocks
                 float4 x[D / 64][8];
 #pragma unroll
                 for (int cb = 0; cb < D / 64; ++cb)
@@ -2264,15 +2308,28 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
             a.sched_perm = nullptr;
             a.sched_counter = nullptr;
         }
-        // key tile 0: the current rows in bf16, [lanes * kv heads][rows][head_dim], read in
-        // boxes of 128 rows (the rows past `rows` are out of bounds: zeros)
+        // key tile 0: the current rows in bf16, [K|V][lanes * kv heads][rows][head_dim], read
+        // in boxes of 128 rows (the rows past `rows` are out of bounds: zeros)
         const int kvh = p.lanes * p.n_kv_heads;
         const size_t half = (size_t)kvh * p.rows * p.head_dim;
-        if (!make_map(&maps[2], a.cur16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.head_dim, p.rows, kvh,
-                      p.head_dim, (int64_t)p.rows * p.head_dim, 64, BM) ||
-            !make_map(&maps[3], a.cur16 + half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.head_dim, p.rows,
-                      kvh, p.head_dim, (int64_t)p.rows * p.head_dim, 64, BM))
+        if (!make_map(&maps[3], a.cur16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.head_dim, p.rows, 2 * kvh,
+                      p.head_dim, (int64_t)p.rows * p.head_dim, 64, BM))
             return cudaErrorInvalidValue;
+        // f32 Q [lanes][rows][heads][d] by TMA: a box of 128 / rows heads x rows x 32
+        // columns lands as the tile's (head, row) rows in order (rows dividing 128)
+        if (BM % p.rows == 0 && pl.heads_per_tile * p.rows <= BM) {
+            auto fn = encode_fn();
+            cuuint64_t dims[4] = {(cuuint64_t)p.head_dim, (cuuint64_t)p.rows, (cuuint64_t)p.n_heads,
+                                  (cuuint64_t)p.lanes};
+            cuuint64_t strides[3] = {(cuuint64_t)p.q_row_stride * 4, (cuuint64_t)p.q_head_stride * 4,
+                                     (cuuint64_t)p.q_lane_stride * 4};
+            cuuint32_t box[4] = {32, (cuuint32_t)p.rows, (cuuint32_t)(BM / p.rows), 1};
+            cuuint32_t es[4] = {1, 1, 1, 1};
+            if (fn && fn(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(p.q), dims, strides,
+                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+                a.q_tma = 1;
+        }
         const int64_t chunks = (int64_t)2 * half / 8;
         const int conv = (int)std::min<int64_t>(64, (chunks + 1023) / 1024);
         order_units_kernel<<<1 + conv, 1024, (a.sched_perm ? groups : 1) * sizeof(int), stream>>>(a, units);

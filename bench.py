@@ -146,6 +146,7 @@ class Timer:
         self.torch = torch
         self.dist = dist
         self.flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        self.graphs_used = False
 
     def flush(self):
         self.flush_buf.zero_()
@@ -155,13 +156,44 @@ class Timer:
             self.dist.barrier()
         self.torch.cuda.synchronize()
 
-    def steps(self, fn, steps: int, warmup: int) -> list[float]:
-        """Per-step device ms of fn (L2 flushed before each step)."""
+    def graph(self, fn):
+        """fn captured into a CUDA graph (after the caller's eager warm-up): replaying it
+        submits the step's launches at once, so host-side launch overhead (ctypes
+        marshalling, argument checks) stays off the device timeline.  Falls back to
+        fn itself if the step cannot be captured."""
+        torch = self.torch
+        try:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                fn()
+            torch.cuda.current_stream().wait_stream(s)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            torch.cuda.synchronize()
+            self.graphs_used = True
+            return g.replay
+        except Exception as e:  # noqa: BLE001 -- report and time eagerly
+            print(f"graph capture failed ({e}); timing eagerly", file=sys.stderr)
+            torch.cuda.synchronize()
+            self.graphs_used = False
+            return fn
+
+    def steps(self, fn, steps: int, warmup: int, graph: bool = True) -> list[float]:
+        """Per-step device ms of fn (L2 flushed before each step), replayed as a CUDA
+        graph unless graph=False."""
         torch = self.torch
         for _ in range(warmup):
             self.flush()
             fn()
         self.barrier()
+        if graph:
+            fn = self.graph(fn)
+            for _ in range(2):
+                self.flush()
+                fn()
+            self.barrier()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(steps)]
         for e0, e1 in evs:
@@ -173,10 +205,12 @@ class Timer:
         return [e0.elapsed_time(e1) for e0, e1 in evs]
 
     def kernel_ms(self, g, fn, reps: int) -> float:
-        """Mean device ms of the dominant kernel of fn's last library call."""
+        """Mean device ms of the dominant kernel of fn's last library call: the
+        library records CUDA events around that launch (event nodes of the graph)."""
         g.gqa_timing_enable(True)
         out = []
         try:
+            fn = self.graph(fn)
             for _ in range(reps):
                 self.flush()
                 fn()
@@ -481,7 +515,8 @@ def main() -> None:
     value = world * info["flops"] / (ms_step * 1e-3) / 1e12
     kern = tm.kernel_ms(g, step, max(10, args.steps))
     achieved = info["flops"] / (kern * 1e-3) / 1e12
-    e2e_ms = tm.max_over_ranks(sum(tm.steps(e2e_step, args.steps, args.warmup)) / args.steps)
+    # end to end through the public call, eagerly (host copies, marshalling and launches included)
+    e2e_ms = tm.max_over_ranks(sum(tm.steps(e2e_step, args.steps, args.warmup, graph=False)) / args.steps)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -492,6 +527,8 @@ def main() -> None:
                    "head_dim": head.head_dim, "scale": head.scale,
                    "flops_per_step": info["flops"],
                    "l2": "flushed before every timed step (512 MiB device write)",
+                   "launch": "each step replayed as a CUDA graph of its library calls" if tm.graphs_used
+                             else "eager library calls",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "kernel": "attn_kernel<256,f16>", "achieved": achieved,
                      "peak": tensor_peak, "unit": "TFLOP/s", "frac": achieved / tensor_peak,
