@@ -787,6 +787,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             bool ok = true;
             const int qlen = a.queue_len ? *a.queue_len : units;
+            // ring-direct verify: every lane's history length, write position and split
+            // count read once, lane l holding lane l's (at most 32 lanes this way)
+            uint32_t my_rl = 0, my_rp = 0;
+            int my_ls = a.splits;
+            if (RING && a.lanes <= 32 && lane < a.lanes) {
+                my_rl = a.ring_len[lane];
+                my_rp = a.ring_wp[lane];
+                if (a.lane_splits) my_ls = a.lane_splits[lane];
+            }
             for (int k = 0; ok; ++k) {
                 int uid;
                 if (a.sched_perm) {
@@ -816,8 +825,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (PAGED) set_span(a, un, lane == 0);
                 // ring-direct verify: the lane's history length and write position
                 int ring_l = 0, ring_p = 0;
+                int lane_splits_here = a.splits;
                 if constexpr (RING) {
-                    const uint32_t rl = a.ring_len[un.t.lane], rp = a.ring_wp[un.t.lane];
+                    uint32_t rl, rp;
+                    if (a.lanes <= 32) {
+                        rl = __shfl_sync(0xffffffffu, my_rl, un.t.lane);
+                        rp = __shfl_sync(0xffffffffu, my_rp, un.t.lane);
+                        lane_splits_here = __shfl_sync(0xffffffffu, my_ls, un.t.lane);
+                    } else {
+                        rl = a.ring_len[un.t.lane];
+                        rp = a.ring_wp[un.t.lane];
+                        if (a.lane_splits) lane_splits_here = a.lane_splits[un.t.lane];
+                    }
                     // out-of-range counters are clamped, as by the pack and mask kernels
                     if (lane == 0 && (rl > (uint32_t)a.ring_w || rp >= (uint32_t)a.ring_w))
                         raise_flag(a.status, GQA_FLAG_RING_CLAMPED);
@@ -837,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int all = 0;
                     for (int base = un.jb; base < un.je; base += 32)
                         all += __popc(__ballot_sync(0xffffffffu, code_of(base + lane) != 0));
-                    const int S = a.lane_splits ? a.lane_splits[un.t.lane] : a.splits;
+                    const int S = (RING && a.lane_splits) ? lane_splits_here : a.splits;
                     lo = (int)((int64_t)un.split * all / S);
                     hi = (int)((int64_t)(un.split + 1) * all / S);
                 }

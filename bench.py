@@ -439,6 +439,7 @@ CAPTURE_CASES = {
     "prefill_d512": lambda w: w.prefill_d512_prefix(seed=0),
     "decode_16seq": lambda w: w.paged_decode(num_seqs=16, num_pages=16384, seed=0),
     "verify": lambda w: w.verify_full(seed=0),
+    "verify_fused": lambda w: w.verify_full(seed=0),
     "paged_chunk": lambda w: w.paged_chunk_full(seed=0),
 }
 
@@ -456,6 +457,12 @@ def run_capture(name: str, reps: int) -> None:
         step = setup_decode(torch, g, c)[0]
     elif name == "paged_chunk":
         step = setup_chunk(torch, g, c)[0]
+    elif name == "verify_fused":
+        fused = setup_verify(torch, g, c)[2]["fused"]
+
+        def step():
+            for f in fused.values():
+                f()
     else:
         step = setup_verify(torch, g, c)[0]
     for _ in range(max(1, reps)):
