@@ -615,6 +615,7 @@ def main() -> None:
             fkernels[name] = {"bytes": fby[name], "kernel_ms": k,
                               "achieved_gbs": fby[name] / (k * 1e-3) / 1e9,
                               "frac": fby[name] / (k * 1e-3) / 1e9 / hbm_peak}
+        fkernels["attn"]["traffic"] = traffic_for("attn_kernel<256,bf16,ring>", vc.name)
         paths["verify_fused"] = {"workload": vc.name, "value": world * ftotal / (t * 1e-3) / 1e9,
                                  "unit": "GB/s", "ms_per_step": t, "bytes_per_step": ftotal,
                                  "peak": hbm_peak, "frac": ftotal / (t * 1e-3) / 1e9 / hbm_peak,
@@ -634,8 +635,9 @@ def main() -> None:
             "roofline": {"bound": "tensor", "kernel": "attn_kernel<256,f16,paged>",
                          "achieved": ic["flops"] / (kt * 1e-3) / 1e12, "peak": tensor_peak,
                          "unit": "TFLOP/s", "frac": ic["flops"] / (kt * 1e-3) / 1e12 / tensor_peak,
-                         "kernel_ms": kt},
+                         "kernel_ms": kt, "traffic": traffic_for("attn_kernel<256,f16,paged>", cc.name)},
             "append": {"kernel": "page_append_kernel<f16>", "bytes": ic["append_bytes"],
+                       "traffic": traffic_for("page_append_kernel<f16>", cc.name),
                        "kernel_ms": ka, "achieved_gbs": ic["append_bytes"] / (ka * 1e-3) / 1e9,
                        "frac": ic["append_bytes"] / (ka * 1e-3) / 1e9 / hbm_peak}}
         del sc, cops, cc
