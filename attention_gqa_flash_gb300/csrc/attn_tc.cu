@@ -293,6 +293,7 @@ __device__ __forceinline__ float mask_to_f32(uint16_t v, int bf16) {
 // classification pre-pass: one CTA per (code group, 64 keys), thread = tile row
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(BM) classify_kernel(const AttnArgs a, uint8_t *codes) {
+    tc::griddep_launch_dependents();  // the attention kernel may start its set-up now
     const int cg = blockIdx.x, cb = blockIdx.y;
     Tile t;
     if (a.shared_mask) {
@@ -500,6 +501,7 @@ __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int
     __shared__ int wsum[32];
     extern __shared__ int gval[];  // group cost, then the group's place in the queue
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    tc::griddep_launch_dependents();  // the attention kernel may start its set-up now
     if (blockIdx.x > 0) {
         // ring-direct verify: the current K and V rows rounded to bf16 (8 per thread step)
         const int cpr = a.head_dim / 8;
@@ -786,6 +788,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             bool ok = true;
+            // the pre-pass (tile classes, or the unit queue and the current rows) is
+            // complete and visible from here on
+            tc::griddep_wait();
             const int qlen = a.queue_len ? *a.queue_len : units;
             // ring-direct verify: every lane's history length, write position and split
             // count read once, lane l holding lane l's (at most 32 lanes this way)
@@ -2031,23 +2036,25 @@ cudaError_t run_attn(const AttnArgs &a, const CUtensorMap *maps, int units, int 
         configured = true;
     }
     timing_mark(true, stream);
-    if constexpr (PAIR) {
+    {
+        // programmatic dependent launch: the kernel's set-up (barriers, TMEM, tensor-map
+        // prefetch) overlaps the pre-pass, whose results the producer waits for
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
         cfg.gridDim = dim3(units);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = Layout<D>::kBytes;
         cfg.stream = stream;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = PAIR ? 2 : 1;
         cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, maps[0], maps[1], maps[2], maps[3]);
         if (e != cudaSuccess) return e;
-    } else {
-        kern<<<units, kThreads, Layout<D>::kBytes, stream>>>(a, maps[0], maps[1], maps[2], maps[3]);
     }
     timing_mark(false, stream);
     cudaError_t e = cudaGetLastError();

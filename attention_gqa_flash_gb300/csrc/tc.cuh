@@ -59,6 +59,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: a pre-pass lets the dependent kernel launch early;
+// the dependent waits for the pre-pass's completion (and its memory) where it first
+// reads what the pre-pass wrote.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // TMA (tiled tensor loads into shared memory, completion on an mbarrier)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, uint32_t bar, int c0,
