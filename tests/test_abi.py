@@ -112,3 +112,55 @@ def test_cta_pair_mode_is_validated_and_keeps_workspace_size(g):
         sizes.append(g.gqa_attn_prefill_workspace_size(128, 2, 1, 256, 4032))
     lib.gqa_attn_set_cta_pairs(1)
     assert len(set(sizes)) == 1 and sizes[0] > 0
+
+
+def test_paged_append_rejects_bad_arguments_before_launch(g):
+    lib = g.library()
+    fake = ctypes.c_void_p(256)
+    tail = [2, 8, 2, 64, 16, 8, None, None]   # num_seqs, tokens, hk, d, page, pages, status, stream
+
+    # a well-formed call shape, with one field broken at a time
+    # k_new, v_new, new_bytes, offsets (+bytes), position starts (+bytes), page table
+    # (+bytes), max pages, pools, pool bytes, dtype, page / token / head strides
+    base = [fake, fake, 8 * 2 * 64 * 4, fake, 3 * 4, fake, 2 * 4, fake, 2 * 4 * 4, 4,
+            fake, fake, 1 << 20, 1, 2048, 128, 64]
+    rc = lib.gqa_paged_append(*base[:14], 2048, 128, 60, *tail)  # head stride not a multiple of 8
+    assert rc == 1 and "multiples of 8" in lib.gqa_last_error().decode()
+    rc = lib.gqa_paged_append(*base, 2, 8, 2, 60, 16, 8, None, None)  # head_dim not a multiple of 8
+    assert rc == 1 and "head_dim" in lib.gqa_last_error().decode()
+    rc = lib.gqa_paged_append(*base[:12], 100, *base[13:], *tail)  # pool too small for the geometry
+    assert rc == 1 and "k_pages" in lib.gqa_last_error().decode()
+    rc = lib.gqa_paged_append(*base[:4], 2 * 4, *base[5:], *tail)  # token_offsets needs num_seqs + 1
+    assert rc == 1 and "token_offsets" in lib.gqa_last_error().decode()
+    rc = lib.gqa_paged_append(*base[:13], 7, *base[14:], *tail)  # unknown dtype
+    assert rc == 1 and "kv_dtype" in lib.gqa_last_error().decode()
+    rc = lib.gqa_paged_append(*base[:2], 100, *base[3:], *tail)  # new rows too small
+    assert rc == 1 and "k_new" in lib.gqa_last_error().decode()
+
+
+def test_paged_prefill_rejects_bad_arguments_before_launch(g):
+    lib = g.library()
+    fake = ctypes.c_void_p(256)
+    # q, q_bytes, pools, pool_bytes, dtype, strides, table, table_bytes, max_pages, offsets,
+    # offs_bytes, pos, pos_bytes, o, o_bytes
+    base = [fake, 1 << 20, fake, fake, 1 << 22, 1, 4096, 256, 128, fake, 2 * 4 * 4, 4,
+            fake, 3 * 4, fake, 2 * 4, fake, 1 << 20]
+    ok_tail = [2, 8, 8, 4, 2, 128, 16, 8, 1.0, None, 0, None, None]
+    # num_seqs, total, max_tokens, h, hk, d, page, pages, scale, ws, ws_bytes, status, stream
+    rc = lib.gqa_attn_paged_prefill(*base, 2, 8, 8, 5, 2, 128, 16, 8, 1.0, None, 0, None, None)
+    assert rc == 1 and "n_kv_heads" in lib.gqa_last_error().decode()
+    rc = lib.gqa_attn_paged_prefill(*base, 2, 8, 8, 4, 2, 64, 16, 8, 1.0, None, 0, None, None)
+    assert rc == 1 and "head_dim" in lib.gqa_last_error().decode()
+    rc = lib.gqa_attn_paged_prefill(*base, 2, 8, 8, 4, 2, 128, 12, 8, 1.0, None, 0, None, None)
+    assert rc == 1 and "page_size" in lib.gqa_last_error().decode()
+    rc = lib.gqa_attn_paged_prefill(*base, 2, 8, 0, 4, 2, 128, 16, 8, 1.0, None, 0, None, None)
+    assert rc == 1 and "max_tokens" in lib.gqa_last_error().decode()
+    rc = lib.gqa_attn_paged_prefill(*base[:1], 100, *base[2:], *ok_tail)   # q too small
+    assert rc == 1 and "q holds" in lib.gqa_last_error().decode()
+    rc = lib.gqa_attn_paged_prefill(*base, *ok_tail[:8], float("nan"), None, 0, None, None)
+    assert rc == 1 and "scale" in lib.gqa_last_error().decode()
+    # with the shapes right, the missing workspace is what is reported
+    rc = lib.gqa_attn_paged_prefill(*base, *ok_tail)
+    ws = lib.gqa_attn_paged_prefill_workspace_size(2, 8, 4, 2, 128, 4, 16)
+    assert (rc == 1 and "workspace" in lib.gqa_last_error().decode()) or ws == 0
+    assert lib.gqa_attn_paged_prefill_workspace_size(2, 8, 4, 2, 96, 4, 16) == 0
