@@ -1329,32 +1329,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // rows that carry no query load row 0 of the tensor (any valid address) and
                 // are zeroed at conversion, so that no load result is consumed before all
                 // loads are issued
-                float4 x[32][PER];
-                uint32_t rows_ok = 0;
+                constexpr int RB = 32 / PER;          // rows per batch: 32 loads in flight
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    int hd = 0, rw = 0;
-                    const bool ok_row = row_of(a, un.t, rbase + j, hd, rw) && rw < un.ntok;
-                    rows_ok |= (ok_row ? 1u : 0u) << j;
-                    const float *src = static_cast<const float *>(a.q) +
-                                       (ok_row ? un.t.lane * a.q_lane + (int64_t)hd * a.q_head +
-                                                     (int64_t)(un.t0 + rw) * a.q_row
-                                               : 0) +
-                                       h * 32 + (lane & 7) * 4;
+                for (int j0 = 0; j0 < 32; j0 += RB) {
+                    float4 x[RB][PER];
+                    uint32_t rows_ok = 0;
 #pragma unroll
-                    for (int k = 0; k < PER; ++k) x[j][k] = ld_nc_f4(src + (lane / 8 + 4 * k) * 64);
-                }
+                    for (int j = 0; j < RB; ++j) {
+                        int hd = 0, rw = 0;
+                        const bool ok_row = row_of(a, un.t, rbase + j0 + j, hd, rw) && rw < un.ntok;
+                        rows_ok |= (ok_row ? 1u : 0u) << j;
+                        const float *src = static_cast<const float *>(a.q) +
+                                           (ok_row ? un.t.lane * a.q_lane + (int64_t)hd * a.q_head +
+                                                         (int64_t)(un.t0 + rw) * a.q_row
+                                                   : 0) +
+                                           h * 32 + (lane & 7) * 4;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-#pragma unroll
-                    for (int k = 0; k < PER; ++k) {
-                        const int cb = lane / 8 + 4 * k, rr = rbase + j;
-                        const bool ok_row = (rows_ok >> j) & 1u;
-                        *reinterpret_cast<uint2 *>(smem + L::kQ + cb * (BM * 128) + sw128(rr, h * 4 + (lane & 7) / 2) +
-                                                   (lane & 1) * 8) =
-                            ok_row ? make_uint2(pack2(KV{}, x[j][k].x, x[j][k].y), pack2(KV{}, x[j][k].z, x[j][k].w))
-                                   : make_uint2(0u, 0u);
+                        for (int k = 0; k < PER; ++k) x[j][k] = ld_nc_f4(src + (lane / 8 + 4 * k) * 64);
                     }
+#pragma unroll
+                    for (int j = 0; j < RB; ++j)
+#pragma unroll
+                        for (int k = 0; k < PER; ++k) {
+                            const int cb = lane / 8 + 4 * k, rr = rbase + j0 + j;
+                            const bool ok_row = (rows_ok >> j) & 1u;
+                            *reinterpret_cast<uint2 *>(smem + L::kQ + cb * (BM * 128) +
+                                                       sw128(rr, h * 4 + (lane & 7) / 2) + (lane & 1) * 8) =
+                                ok_row ? make_uint2(pack2(KV{}, x[j][k].x, x[j][k].y),
+                                                    pack2(KV{}, x[j][k].z, x[j][k].w))
+                                       : make_uint2(0u, 0u);
+                        }
+                }
             } else {
                 // f32 Q without TMA, Q in tensor memory: each thread reads its half of its
                 // own row (its TMEM lane), every load in flight at once, then converts and
