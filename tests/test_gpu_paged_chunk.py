@@ -163,3 +163,80 @@ def test_chunked_prefill_full_size_sampled(lib):
     ref = oracle.paged_decode(c.q[sel], rk, rv, kv_dtype="f16", page_table=c.page_table[seq],
                               context_lens=(pos + 1).astype(np.int32), scale=c.scale)
     assert_attention_close(got[sel], ref, "chunked prefill full size (sampled)")
+
+
+def test_chunked_prefill_edge_cases(lib):
+    """Sequences with no new token, a single token at position 0, 8-slot pages and
+    128-slot pages (the value rows past the context come from the pool row by row)."""
+    import torch
+    from gpu_helpers import assert_attention_close, dev, new_status
+    for ps_, tok, pre, seed in ((8, (2, 40), (0, 30), 31), (128, (2, 200), (0, 300), 32)):
+        c = workloads.paged_chunk(num_seqs=4, tokens_lo=tok[0], tokens_hi=tok[1], prefix_lo=pre[0],
+                                  prefix_hi=pre[1], num_pages=4 * (-(-(tok[1] + pre[1]) // ps_)) + 3,
+                                  page_size=ps_, n_heads=4, n_kv_heads=2, head_dim=128, seed=seed)
+        # force one empty sequence and one single token at position 0
+        toks = np.diff(c.token_offsets).astype(np.int64)
+        toks[1], toks[2] = 0, 1
+        offs = np.concatenate([[0], np.cumsum(toks)]).astype(np.int32)
+        ps = c.position_start.copy()
+        ps[2] = 0
+        T = int(offs[-1])
+        q, kn, vn = c.q[:T], c.k_new[:T], c.v_new[:T]
+        kp, vp = _pool_dev(c.k_pool, "f16"), _pool_dev(c.v_pool, "f16")
+        st = new_status()
+        lib.gqa_paged_append(dev(kn), dev(vn), dev(offs), dev(ps), dev(c.page_table), kp, vp, status=st)
+        out = lib.gqa_attn_paged_prefill(dev(q), kp, vp, dev(c.page_table), dev(offs), dev(ps),
+                                         max(1, int(toks.max())), c.scale, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        rk, rv, skipped = oracle.paged_append(kn, vn, offs, ps, c.page_table, c.k_pool, c.v_pool,
+                                              kv_dtype="f16", **_strides(c))
+        assert skipped == 0
+        np.testing.assert_array_equal(_bits(kp), rk.view(np.uint16))
+        ref = oracle.paged_prefill(q, rk, rv, c.page_table, offs, ps, kv_dtype="f16",
+                                   n_kv_heads=c.n_kv_heads, scale=c.scale, **_strides(c))
+        assert_attention_close(out.cpu().numpy(), ref, f"chunked prefill edges, page {ps_}")
+
+
+def test_chunked_prefill_clamps_and_flags_long_sequences(lib):
+    """A sequence with more tokens than max_tokens: its rows past max_tokens are not
+    computed (their output keeps what was there) and GQA_FLAG_CONTEXT_CLAMPED is raised;
+    the rows that are computed still match the oracle."""
+    import torch
+    from gpu_helpers import assert_attention_close, dev, new_status
+    c = workloads.paged_chunk(num_seqs=2, tokens_lo=40, tokens_hi=60, prefix_hi=50, head_dim=128,
+                              seed=33)
+    kp, vp, _ = _append_gpu(lib, c)
+    limit = 32
+    out = torch.full(c.q.shape, 7.0, dtype=torch.float32, device="cuda")
+    st = new_status()
+    lib.gqa_attn_paged_prefill(dev(c.q), kp, vp, dev(c.page_table), dev(c.token_offsets),
+                               dev(c.position_start), limit, c.scale, out=out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & 2   # GQA_FLAG_CONTEXT_CLAMPED
+    got = out.cpu().numpy()
+    rk, rv, _ = oracle.paged_append(c.k_new, c.v_new, c.token_offsets, c.position_start,
+                                    c.page_table, c.k_pool, c.v_pool, kv_dtype="f16", **_strides(c))
+    ref = oracle.paged_prefill(c.q, rk, rv, c.page_table, c.token_offsets, c.position_start,
+                               kv_dtype="f16", n_kv_heads=c.n_kv_heads, scale=c.scale, **_strides(c))
+    for s in range(c.num_seqs):
+        o0, o1 = int(c.token_offsets[s]), int(c.token_offsets[s + 1])
+        assert_attention_close(got[o0:o0 + limit], ref[o0:o0 + limit], f"seq {s} computed rows")
+        assert np.all(got[o0 + limit:o1] == 7.0)
+
+
+def test_page_append_and_prefill_with_no_tokens(lib):
+    """total_tokens = 0: both calls are accepted and do nothing."""
+    import torch
+    from gpu_helpers import dev, new_status
+    c = workloads.paged_chunk(num_seqs=2, tokens_hi=10, prefix_hi=20, head_dim=64, seed=34)
+    kp, vp = _pool_dev(c.k_pool, "f16"), _pool_dev(c.v_pool, "f16")
+    before = _bits(kp).copy()
+    z = np.zeros(3, np.int32)
+    st = new_status()
+    empty_kv = torch.empty((0, c.n_kv_heads, 64), dtype=torch.float32, device="cuda")
+    lib.gqa_paged_append(empty_kv, empty_kv, dev(z), dev(c.position_start), dev(c.page_table), kp, vp,
+                         status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(_bits(kp), before)
