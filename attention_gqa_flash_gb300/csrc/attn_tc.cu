@@ -1,12 +1,15 @@
 // attn_tc.cu -- masked GQA flash attention on the 5th-generation tensor
-// cores (tcgen05), used for prefill and for the speculative-verify attention.
+// cores (tcgen05): prefill, the speculative-verify attention (over the packed
+// copy, or read straight from the ring) and chunked prefill over pages.
 //
 // What it computes (mlx-native 0.18.0 src/ops/flash_attn_prefill_tensor.rs,
 // module doc): O = softmax(scale * Q K^T + mask) V with one KV head per
 // n_heads / n_kv_heads query heads and an additive f16 (or bf16) mask; a
 // query row whose mask hides every key yields zeros.
 //
-// Kernel structure (one CTA = one 128-row query tile, 320 threads):
+// Kernel structure: a persistent grid of at most one CTA (or CTA pair) per SM,
+// 384 threads each, running units of work (one 128-row query tile, one output
+// half, one key split) back to back:
 //   warps 0-7  softmax: two threads per query row (warp w and w+4 share the
 //              TMEM lanes of rows 32(w%4)..+31, each takes half of the 128
 //              columns of a key tile).  They stage Q (f32/bf16 -> f16/bf16),
@@ -14,13 +17,14 @@
 //              in the exp2 domain with lazy rescaling of O (only when the row
 //              maximum grows by more than 2^8; the two halves agree on the
 //              maximum through shared memory), write P over S in TMEM, and
-//              finally normalise O into global memory.
-//   warp 8     TMA producer: streams Q (f32 prefill), K and V tiles (128-byte
-//              swizzle) through a ring of 32 KiB stages guarded by full/empty
-//              mbarriers.
+//              finally normalise O and store it (staged, by TMA, where it can).
+//   warp 8     TMA producer: builds each unit's list of visible key tiles and
+//              streams Q (f32), K and V tiles (128-byte swizzle) through a ring
+//              of 32 KiB stages guarded by full/empty mbarriers.
 //   warp 9     MMA issuer: owns the TMEM allocation; S = Q K^T into one of two
 //              TMEM buffers (the next tile's Q K^T overlaps this tile's
 //              softmax), then O += P V with P read from TMEM.
+//   warps 10-11 only complete the third warpgroup (register split).
 // Key tiles are 128 wide so every MMA has N = 128 (narrower tcgen05 shapes
 // run far below the tensor-core rate).  Tiles whose mask is entirely -inf are
 // skipped (a classification pre-pass reads the mask once, 64 keys at a time);
@@ -28,8 +32,8 @@
 // head_dim 512 keeps a 128x512 f32 accumulator out of reach of the 512 TMEM
 // columns, so each query tile is processed as two units, one per 256-wide
 // half of the output, both recomputing S.
-// Few tiles (verify) are split along the keys; partial results carry a
-// log2-sum-exp and are merged by a combine kernel.
+// Few tiles (verify, short chunks) are split along the keys; partial results
+// carry a log2-sum-exp and are merged by a combine kernel.
 // Three ways of finding the visible keys, one kernel instance each: an
 // additive mask tensor (prefill, verify), a ring read directly (fused
 // verify), and pages (chunked prefill: ferrum-kernels 0.8.3
