@@ -179,10 +179,11 @@ struct AttnArgs {
     int vis_split;
     // ring-direct verify with splits over the visible tiles: the pre-pass gives lane l
     // lane_splits[l] of the `splits` split slots, in proportion to its visible tiles
-    // (split_budget of them per KV head in all, about one unit per SM), queues only
-    // those units (queue_len of them) and numbers their partial results in queue
-    // order: part_slot[(tile * d_parts + dpart) * splits + split]
-    int *lane_splits, *queue_len, *part_slot;
+    // (split_budget of them per query tile in all, about one unit per SM), and queues
+    // the lanes' units in blocks, the lane with the most tiles per split first: lane l's
+    // block starts at lane_start[l] and holds, for each of its query tiles in order,
+    // its splits in order.  A unit's partial result goes to slot = its queue position.
+    int *lane_splits, *lane_start, *queue_len;
     int split_budget;
 };
 
@@ -528,79 +529,46 @@ __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int
         }
         return;
     }
-    if (!a.sched_perm) return;
-    if (a.lane_splits) {
-        // ring-direct verify: split slots per lane in proportion to its visible tiles, then
-        // a counting sort of the units in use by decreasing cost
-        __shared__ int s_vis[64];
-        __shared__ int s_real;
-        if (t < a.lanes) {
-            const int L = (int)min(a.ring_len[t], (uint32_t)a.ring_w);
-            const int wp = (int)(a.ring_wp[t] % (uint32_t)a.ring_w);
-            int vis = 0;
+    if (a.lane_start) {
+        // ring-direct verify (at most 32 lanes): one warp works out each lane's split
+        // count and where its block of units starts in the queue
+        if (warp != 0) return;
+        int vis = 0;
+        if (lane < a.lanes) {
+            const int L = (int)min(a.ring_len[lane], (uint32_t)a.ring_w);
+            const int wp = (int)(a.ring_wp[lane] % (uint32_t)a.ring_w);
             for (int j = 0; j < a.n_blk; ++j) vis += ring_tile_code(a, j, L, wp) != 0;
-            s_vis[t] = vis;
         }
-        bins[t] = 0;
-        if (t == 0) s_real = 0;
-        __syncthreads();
-        if (t == 0) {
-            int total = 0;
-            for (int l = 0; l < a.lanes; ++l) total += s_vis[l];
-            for (int l = 0; l < a.lanes; ++l) {
-                int S = (int)((int64_t)s_vis[l] * a.split_budget / max(total, 1));
-                S = min(max(S, 1), min(a.splits, max(s_vis[l], 1)));
-                a.lane_splits[l] = S;
-            }
-        }
-        __syncthreads();
-        for (int u = t; u < units; u += 1024) {
-            const int c = unit_cost(a, u);
-            if (c > 0) {
-                atomicAdd(&bins[c], 1);
-                atomicAdd(&s_real, 1);
-            }
-        }
-        __syncthreads();
-        const int c = kCostBins - 1 - t;
-        const int v = c > 0 ? bins[c] : 0;
-        int x = v;
+        int total = vis;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+        int S = 0, cost = -1;
+        if (lane < a.lanes) {
+            S = (int)((int64_t)vis * a.split_budget / max(total, 1));
+            S = min(max(S, 1), min(a.splits, max(vis, 1)));
+            cost = (vis + S - 1) / S;
         }
-        if (lane == 31) wsum[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            int w = wsum[lane];
+        const int cnt = lane < a.lanes ? S * a.n_kv_heads * a.head_tiles : 0;
+        // this lane's block follows the blocks of the lanes with dearer units
+        int start = 0;
+        for (int l = 0; l < 32; ++l) {
+            const int cl = __shfl_sync(0xffffffffu, cost, l), nl = __shfl_sync(0xffffffffu, cnt, l);
+            if (cl > cost || (cl == cost && l < lane)) start += nl;
+        }
+        int sum = cnt;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, w, o);
-                if (lane >= o) w += y;
-            }
-            wsum[lane] = w;
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane < a.lanes) {
+            a.lane_splits[lane] = S;
+            a.lane_start[lane] = start;
         }
-        __syncthreads();
-        const int start = x - v + (warp > 0 ? wsum[warp - 1] : 0);
-        __syncthreads();
-        bins[c] = start;
-        __syncthreads();
-        int *perm = const_cast<int *>(a.sched_perm);
-        for (int u = t; u < units; u += 1024) {
-            const int cu = unit_cost(a, u);
-            if (cu == 0) continue;
-            const int pos = atomicAdd(&bins[cu], 1);
-            perm[pos] = u;
-            const Unit un = unit_of(a, u, false, 0, 0);
-            a.part_slot[((int64_t)un.tile_id * a.d_parts + un.dpart) * a.splits + un.split] = pos;
-        }
-        if (t == 0) {
-            *a.queue_len = s_real;
+        if (lane == 0) {
+            *a.queue_len = sum;
             *a.sched_counter = 0;
         }
         return;
     }
+    if (!a.sched_perm) return;
     const int groups = a.lanes * a.n_kv_heads, per_group = units / groups;
     bins[t] = 0;
     for (int g = t; g < groups; g += 1024) gval[g] = 0;
@@ -796,22 +764,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             // complete and visible from here on
             tc::griddep_wait();
             const int qlen = a.queue_len ? *a.queue_len : units;
-            // ring-direct verify: every lane's history length, write position and split
-            // count read once, lane l holding lane l's (at most 32 lanes this way)
+            // ring-direct verify: every lane's history length, write position, split count
+            // and queue block read once, lane l holding lane l's (at most 32 lanes this way)
             uint32_t my_rl = 0, my_rp = 0;
-            int my_ls = a.splits;
+            int my_ls = a.splits, my_start = 0;
             if (RING && a.lanes <= 32 && lane < a.lanes) {
                 my_rl = a.ring_len[lane];
                 my_rp = a.ring_wp[lane];
-                if (a.lane_splits) my_ls = a.lane_splits[lane];
+                if (a.lane_splits) {
+                    my_ls = a.lane_splits[lane];
+                    my_start = a.lane_start[lane];
+                }
             }
             for (int k = 0; ok; ++k) {
                 int uid;
-                if (a.sched_perm) {
+                if (a.sched_counter) {
                     int idx = 0;
                     if (lane == 0) idx = atomicAdd(a.sched_counter, 1);
                     idx = __shfl_sync(0xffffffffu, idx, 0);
-                    uid = idx < qlen ? a.sched_perm[idx] : -1;
+                    if (RING && a.lane_start) {
+                        // the lane whose block holds queue position idx; then its query
+                        // tile and split
+                        const int per_lane = my_ls * a.n_kv_heads * a.head_tiles;
+                        const unsigned own = __ballot_sync(
+                            0xffffffffu, lane < a.lanes && idx >= my_start && idx < my_start + per_lane);
+                        uid = -1;
+                        if (own && idx < qlen) {
+                            const int o = __ffs(own) - 1;
+                            const int S = __shfl_sync(0xffffffffu, my_ls, o);
+                            const int rem = idx - __shfl_sync(0xffffffffu, my_start, o);
+                            const int tile_in_lane = rem / S;  // kv head major, head tile minor
+                            uid = (o * a.n_kv_heads * a.head_tiles + tile_in_lane) * a.splits + (rem - tile_in_lane * S);
+                        }
+                    } else {
+                        uid = idx < qlen ? a.sched_perm[idx] : -1;
+                    }
                 } else {
                     uid = slot_unit(k, slot, slots, units);
                     if (uid < 0) break;
@@ -1123,7 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int g = 0;        // global index of the unit's first tile
                 int with_o = 0;   // units so far that produced O (one o_free phase each)
                 for (int k = 0; ok; ++k) {
-                    if (!a.sched_perm && slot_unit(k, slot, slots, units) < 0) break;
+                    if (!a.sched_counter && slot_unit(k, slot, slots, units) < 0) break;
                     const int b = k & 1;
                     if (!(ok = wt.wait(list_full(b), (k >> 1) & 1))) break;
                     if (uid_smem[b] < 0) break;  // the unit queue has ended
@@ -1405,7 +1392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int uid = -1;
         Unit cur{};
         int cur_n = 0, cur_pos = 0;  // visible tiles and first ring position of unit k
-        if (a.sched_perm || slot_unit(0, slot, slots, units) >= 0) {
+        if (a.sched_counter || slot_unit(0, slot, slots, units) >= 0) {
             ok = __all_sync(0xffffffffu, wt.wait(list_full(0), 0));
             uid = ok ? uid_smem[0] : -1;
             if (uid >= 0) {
@@ -1630,7 +1617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool stage_o = a.o_tma && cur_n > 0 && (!PAGED || cur.q_row0 + BM <= cur.ntok);
             int o_slot0 = 0;       // first ring position of the staging area
             bool hold_q = false;   // staging in the next unit's Q slots
-            if (ok && (a.sched_perm || slot_unit(k + 1, slot, slots, units) >= 0)) {
+            if (ok && (a.sched_counter || slot_unit(k + 1, slot, slots, units) >= 0)) {
                 ok = __all_sync(0xffffffffu, wt.wait(list_full((k + 1) & 1), ((k + 1) >> 1) & 1));
                 nuid = ok ? uid_smem[(k + 1) & 1] : -1;
             }
@@ -1724,7 +1711,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // partials column-chunk major: the 32 rows of a warp store 512
                     // contiguous bytes per instruction
                     int64_t unit = ((int64_t)cur.tile_id * a.d_parts + cur.dpart) * a.splits + cur.split;
-                    if (a.part_slot) unit = a.part_slot[unit];
+                    if (a.lane_start)  // ring-direct verify: the unit's queue position
+                        unit = a.lane_start[cur.t.lane] +
+                               (int64_t)((cur.t.kh * a.head_tiles + cur.t.ht) * a.lane_splits[cur.t.lane] + cur.split);
                     dst = nullptr;
                     if (valid) {
                         if (h == 0) a.ws_lse[unit * BM + r] = l > 0.f ? m_ref + __log2f(l) : kNegInf;
@@ -1814,7 +1803,9 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a, int
     const int64_t u0 = ((int64_t)tile_id * a.d_parts + dpart) * a.splits;
     // the splits in use and where their partials are
     const int S = a.lane_splits ? a.lane_splits[t.lane] : a.splits;
-    auto slot = [&](int s) -> int64_t { return a.part_slot ? a.part_slot[u0 + s] : u0 + s; };
+    auto slot = [&](int s) -> int64_t {
+        return a.lane_start ? a.lane_start[t.lane] + (int64_t)((t.kh * a.head_tiles + t.ht) * S + s) : u0 + s;
+    };
     float M = kNegInf;
     for (int s = 0; s < S; ++s) M = fmaxf(M, a.ws_lse[slot(s) * BM + r]);
     float acc[DO / 32];
@@ -1904,13 +1895,14 @@ Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, i
     p.splits = 1;
     // (the unit queue of the ordering pass is required: its group table and the lane
     // split counts in the queue header bound the lanes and groups)
-    p.vis_split = vis_split && !p.pair && p.n_blk <= kMaxListTiles && lanes <= 60 &&
-                  lanes * n_kv_heads <= kMaxQueueGroups;
+    // (the lane blocks of the queue are worked out by one warp: at most 30 lanes, whose
+    // split counts and block starts fit in the queue header)
+    p.vis_split = vis_split && !p.pair && p.n_blk <= kMaxListTiles && lanes <= 30;
     if (p.vis_split) {
-        // splits share out each tile's visible key tiles: at most sms / n_kv_heads per
-        // lane (the pre-pass hands them out in proportion to the lanes' visible tiles,
-        // about one unit per SM in all)
-        int s = sms / n_kv_heads;
+        // splits share out each tile's visible key tiles: at most sms / (query tiles per
+        // lane) per lane (the pre-pass hands them out in proportion to the lanes' visible
+        // tiles, about one unit per SM in all)
+        int s = sms / (n_kv_heads * p.head_tiles);
         p.split_budget = s < 1 ? 1 : s;
         p.splits = p.split_budget > p.n_blk ? p.n_blk : p.split_budget;
         p.bps = p.n_blk;
@@ -1929,18 +1921,18 @@ Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, i
     p.codes_bytes = align256((size_t)p.code_groups * p.code_cols);
     if (p.splits > 1) {
         size_t nunits = (size_t)p.tiles * p.d_parts * p.splits;
-        // splits over the visible tiles: at most split_budget + 1 per (lane, KV head) group
-        // are in use, fewer than the split slots
+        // splits over the visible tiles: the lanes' split counts add up to at most
+        // split_budget + lanes, each used by every query tile of its lane
         if (p.vis_split) {
-            const size_t used = (size_t)lanes * n_kv_heads * (p.split_budget + 1) * p.d_parts;
+            const size_t used = (size_t)(p.split_budget + lanes) * n_kv_heads * p.head_tiles * p.d_parts;
             if (used < nunits) nunits = used;
         }
         p.part_slots = nunits;
         p.part_o_bytes = align256(nunits * BM * p.do_ * 4);
         p.part_lse_bytes = align256(nunits * BM * 4);
     }
-    if (p.vis_split)  // counter, queue length, lane split counts; order; partial slots
-        p.sched_bytes = 256 + 2 * align256((size_t)p.tiles * p.d_parts * p.splits * 4);
+    if (p.vis_split)  // counter, queue length, lane split counts and block starts
+        p.sched_bytes = 256;
     if (ring) p.cur_bytes = align256((size_t)2 * lanes * n_kv_heads * rows * head_dim * 2);
     return p;
 }
@@ -2278,13 +2270,13 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     if (pl.sched_bytes) {
         char *sched = ws + pl.codes_bytes + pl.part_o_bytes + pl.part_lse_bytes;
         a.sched_counter = reinterpret_cast<int *>(sched);
-        a.sched_perm = reinterpret_cast<const int *>(sched + 256);
         if (pl.vis_split) {
             a.queue_len = reinterpret_cast<int *>(sched + 4);
             a.lane_splits = reinterpret_cast<int *>(sched + 8);
-            a.part_slot = reinterpret_cast<int *>(sched + 256 +
-                                                  align256((size_t)pl.tiles * pl.d_parts * pl.splits * 4));
+            a.lane_start = reinterpret_cast<int *>(sched + 8 + 30 * 4);
             a.split_budget = pl.split_budget;
+        } else {
+            a.sched_perm = reinterpret_cast<const int *>(sched + 256);
         }
     }
     a.head_dim = p.head_dim;
@@ -2338,11 +2330,6 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     if (p.ring) {
         // ring-direct verify: bf16 rings, head_dim 128 or 256, unpaired
         if (!bf || pl.pair) return cudaErrorInvalidValue;
-        const int groups = p.lanes * p.n_kv_heads;
-        if (groups > kMaxQueueGroups) {
-            a.sched_perm = nullptr;
-            a.sched_counter = nullptr;
-        }
         // key tile 0: the current rows in bf16, [K|V][lanes * kv heads][rows][head_dim], read
         // in boxes of 128 rows (the rows past `rows` are out of bounds: zeros)
         const int kvh = p.lanes * p.n_kv_heads;
@@ -2367,7 +2354,7 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
         }
         const int64_t chunks = (int64_t)2 * half / 8;
         const int conv = (int)std::min<int64_t>(64, (chunks + 1023) / 1024);
-        order_units_kernel<<<1 + conv, 1024, (a.sched_perm ? groups : 1) * sizeof(int), stream>>>(a, units);
+        order_units_kernel<<<1 + conv, 1024, sizeof(int), stream>>>(a, units);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if (p.head_dim == 128) return run_attn<128, BF16, false, kRingMode>(a, maps, ctas, pl.tiles, stream);
