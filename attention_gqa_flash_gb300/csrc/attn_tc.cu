@@ -760,6 +760,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             bool ok = true;
+            // while the pre-pass runs: the first unit's f32 Q into L2 (its rows and heads do
+            // not depend on the pre-pass when the units are assigned statically)
+            if (!a.sched_counter && a.q_tma && lane == 0 && !RING) {
+                const int uid0 = slot_unit(0, slot, slots, units);
+                if (uid0 >= 0) {
+                    Unit u0 = unit_of(a, uid0, PAIR, rank, DO);
+                    if constexpr (PAGED) set_span(a, u0, false);
+                    for (int qs = 0; qs < kQStages; ++qs)
+#pragma unroll
+                        for (int bx = 0; bx < 2; ++bx)
+                            tc::tma_prefetch_3d(&tmq, qs * 64 + bx * 32,
+                                                a.q_rows_dim1 ? u0.t0 + u0.q_row0 : u0.q_head0,
+                                                a.q_rows_dim1 ? u0.q_head0 : u0.t0 + u0.q_row0);
+                }
+            }
             // the pre-pass (tile classes, or the unit queue and the current rows) is
             // complete and visible from here on
             tc::griddep_wait();

@@ -87,6 +87,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// global -> L2 prefetch of a tiled box (no shared memory, no completion)
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0),
+                 "r"(c1), "r"(c2)
+                 : "memory");
+}
 // shared -> global tiled store; completion tracked by the issuing thread's bulk group
 __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int c0, int c1, int c2) {
     asm volatile(
