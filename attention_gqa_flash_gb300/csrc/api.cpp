@@ -337,7 +337,7 @@ int gqa_attn_paged_decode_noalloc(const float *q, size_t q_bytes, const void *k_
         gqa::decode_workspace_bytes(num_seqs, n_heads, head_dim, max_pages_per_seq, page_size);
     if (need > (size_t)GQA_NOALLOC_SCRATCH_BYTES)
         return fail("paged decode (no-alloc): this problem needs %zu bytes of scratch "
-                    "(num_seqs x ceil(max_pages_per_seq*page_size/256) x n_heads x (head_dim+1) x 4), "
+                    "(num_seqs x ceil(max_pages_per_seq*page_size/1024) x n_heads x (head_dim+1) x 4), "
                     "more than the fixed %u-byte array; use gqa_attn_paged_decode with a workspace",
                     need, (unsigned)GQA_NOALLOC_SCRATCH_BYTES);
     void *scratch = nullptr;

@@ -7,7 +7,9 @@
 // (validate_signature), and the decode query attends to every context token.
 //
 // Design (HBM-bound: each context token's K and V rows are read exactly once):
-//   * work unit = (sequence, KV head, 16-query-head group, 256-token chunk);
+//   * work unit = (sequence, KV head, 16-query-head group, 1024-token chunk:
+//     larger chunks measured slower at 4096, smaller ones write and merge more
+//     partial results);
 //     a persistent grid walks the units chunk-major, skipping chunks past a
 //     sequence's end without a launch;
 //   * the CTA's 4 warps take interleaved 16-token sub-tiles; each warp gathers
@@ -29,7 +31,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kSub = 16;                // tokens per warp step
-constexpr int kChunk = 256;             // tokens per work unit
+constexpr int kChunk = 1024;            // tokens per work unit
 constexpr float kNegInf = -INFINITY;
 
 struct DecodeArgs {

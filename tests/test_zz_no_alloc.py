@@ -65,12 +65,12 @@ def test_oversized_problem_is_refused(lib):
     from gpu_helpers import dev
     c = workloads.paged_decode(num_seqs=32, ctx_lo=16, ctx_hi=64, num_pages=256, n_heads=32,
                                n_kv_heads=8, head_dim=128, seed=33)
-    # a page table wide enough for 16384-token contexts: 32 sequences x 64 chunks x 32 heads
-    # x (128 + 1) x 4 B of partials is about 32 MiB, over the fixed 16 MiB
-    table = np.full((32, 1024), -1, np.int32)
+    # a page table wide enough for 65536-token contexts: 32 sequences x 64 chunks of 1024
+    # tokens x 32 heads x (128 + 1) x 4 B of partials is about 34 MB, over the fixed 16 MiB
+    table = np.full((32, 4096), -1, np.int32)
     table[:, :c.page_table.shape[1]] = c.page_table
     args = (dev(c.q), dev(c.k_pool), dev(c.v_pool), dev(table), dev(c.context_lens))
-    need = lib.gqa_attn_paged_decode_workspace_size(32, 32, 128, 1024, 16)
+    need = lib.gqa_attn_paged_decode_workspace_size(32, 32, 128, 4096, 16)
     assert need > lib.GQA_NOALLOC_SCRATCH_BYTES
     out = torch.empty((32, 32, 128), dtype=torch.float32, device="cuda")
     with pytest.raises(lib.GQAError, match="fixed"):
