@@ -220,11 +220,18 @@ class Timer:
         return sum(out) / len(out)
 
     def max_over_ranks(self, x: float) -> float:
-        if self.dist is None:
-            return x
-        t = self.torch.tensor([x], dtype=self.torch.float64, device="cuda")
-        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(self.torch, self.dist, x)
+
+
+def max_over_ranks(torch, dist, x: float) -> float:
+    """The slowest rank's value (every rank gets it); x itself without a process group.
+    The reduction runs on the device the group's backend serves (CUDA for NCCL)."""
+    if dist is None:
+        return x
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 # ---------------------------------------------------------------------------
