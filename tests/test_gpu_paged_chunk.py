@@ -240,3 +240,28 @@ def test_page_append_and_prefill_with_no_tokens(lib):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     np.testing.assert_array_equal(_bits(kp), before)
+
+
+def test_chunked_prefill_page_relabelling_is_bit_identical(lib):
+    """Moving every page to another physical slot (and the page table with it) gives the
+    same bits: the page gather depends only on the table."""
+    import torch
+    from gpu_helpers import dev, new_status
+    c = workloads.paged_chunk(num_seqs=3, tokens_lo=60, tokens_hi=200, prefix_hi=300, head_dim=256,
+                              seed=41)
+    kp, vp, _ = _append_gpu(lib, c)
+    perm = np.random.default_rng(5).permutation(c.num_pages)
+    inv = np.argsort(perm)
+    kp2, vp2 = torch.empty_like(kp), torch.empty_like(vp)
+    kp2[torch.from_numpy(inv).cuda()] = kp
+    vp2[torch.from_numpy(inv).cuda()] = vp
+    table2 = np.where(c.page_table >= 0, inv[np.maximum(c.page_table, 0)], -1).astype(np.int32)
+    max_tokens = int(np.diff(c.token_offsets).max())
+    st = new_status()
+    o1 = lib.gqa_attn_paged_prefill(dev(c.q), kp, vp, dev(c.page_table), dev(c.token_offsets),
+                                    dev(c.position_start), max_tokens, c.scale, status=st)
+    o2 = lib.gqa_attn_paged_prefill(dev(c.q), kp2, vp2, dev(table2), dev(c.token_offsets),
+                                    dev(c.position_start), max_tokens, c.scale, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(o1, o2)
