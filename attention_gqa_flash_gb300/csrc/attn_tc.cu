@@ -453,28 +453,16 @@ __device__ __forceinline__ int paged_tile_code(const AttnArgs &a, const Unit &n,
     return k0 + BN - 1 <= p0 ? 1 : 2;
 }
 
-// Key tiles unit u visits (chunked prefill, or ring-direct verify with splits
-// over the visible tiles), plus one for the unit's own overhead when it has any
-// (the scheduling cost), capped at kCostBins - 1.
+// Chunked prefill: visible key tiles of unit u, plus one for the unit's own overhead
+// when it has any (the scheduling cost), capped at kCostBins - 1.
 constexpr int kCostBins = 1024;
 constexpr int kMaxQueueGroups = 10240;  // (sequence, KV head) groups the ordering pass handles (40 KiB)
-__device__ __forceinline__ int unit_cost(const AttnArgs &a, int u) {
+__device__ __forceinline__ int paged_unit_cost(const AttnArgs &a, int u) {
     Unit un = unit_of(a, u, false, 0, 0);
-    int n;
-    if (a.ring) {
-        const int L = (int)min(a.ring_len[un.t.lane], (uint32_t)a.ring_w);
-        const int wp = (int)(a.ring_wp[un.t.lane] % (uint32_t)a.ring_w);
-        int all = 0;
-        for (int j = 0; j < a.n_blk; ++j) all += ring_tile_code(a, j, L, wp) != 0;
-        const int S = a.lane_splits ? a.lane_splits[un.t.lane] : a.splits;
-        if (un.split >= S) return 0;
-        n = (int)((int64_t)(un.split + 1) * all / S) - (int)((int64_t)un.split * all / S);
-    } else {
-        set_span(a, un, false);
-        if (un.q_row0 >= un.ntok) return 0;
-        const int p1 = un.ps + min(un.q_row0 + a.rows_per_head, un.ntok) - 1;
-        n = max(0, min(un.je, p1 / BN + 1) - un.jb);
-    }
+    set_span(a, un, false);
+    if (un.q_row0 >= un.ntok) return 0;
+    const int p1 = un.ps + min(un.q_row0 + a.rows_per_head, un.ntok) - 1;
+    const int n = max(0, min(un.je, p1 / BN + 1) - un.jb);
     return min(n + (n > 0 ? 1 : 0), kCostBins - 1);
 }
 
@@ -495,12 +483,17 @@ __device__ __forceinline__ int unit_in_group(const AttnArgs &a, int g, int j) {
     return (ut * a.d_parts + dpart) * a.splits + split;
 }
 
-// One CTA of 1024 threads: the queue order for a chunked prefill.  The units of
-// one (sequence, KV head) group read the same keys and values, so they are queued
-// together (and run at the same time, sharing those bytes through L2); groups go
-// in decreasing order of their mean unit cost (counting sort), so that the
-// dynamic queue ends with the light ones.  Also resets the queue counter for the
-// attention launch that follows.  Dynamic shared memory: one int per group.
+// Pre-pass of the dynamic unit queue (CTAs of 1024 threads), then the queue counter
+// reset for the attention launch that follows.
+//   CTA 0, chunked prefill: the queue order.  The units of one (sequence, KV head)
+//     group read the same keys and values, so they are queued together (and run at
+//     the same time, sharing those bytes through L2); groups go in decreasing order
+//     of their mean unit cost (counting sort), so that the queue ends with the light
+//     ones.  Dynamic shared memory: one int per group.
+//   CTA 0, ring-direct verify: one warp works out each lane's split count and the
+//     start of its block of units in the queue.
+//   CTAs 1.., ring-direct verify: the current K and V rows rounded to bf16 for the
+//     tensor map of key tile 0.
 __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int units) {
     __shared__ int bins[kCostBins];
     __shared__ int wsum[32];
@@ -575,7 +568,7 @@ __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int
     __syncthreads();
     for (int u = t; u < units; u += 1024) {
         const Unit un = unit_of(a, u, false, 0, 0);
-        atomicAdd(&gval[un.t.lane * a.n_kv_heads + un.t.kh], unit_cost(a, u));
+        atomicAdd(&gval[un.t.lane * a.n_kv_heads + un.t.kh], paged_unit_cost(a, u));
     }
     __syncthreads();
     for (int g = t; g < groups; g += 1024) {
@@ -1861,7 +1854,6 @@ struct Plan {
     int n_blk, code_cols, code_groups, splits, bps;
     bool shared_mask, pair, vis_split;
     int split_budget;
-    size_t part_slots;  // split partial slots in the workspace
     size_t codes_bytes, part_o_bytes, part_lse_bytes;
     size_t sched_bytes;  // dynamic unit queue: counter (256 bytes) + order
     size_t cur_bytes;    // ring-direct verify: the current rows in bf16
@@ -1942,7 +1934,6 @@ Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, i
             const size_t used = (size_t)(p.split_budget + lanes) * n_kv_heads * p.head_tiles * p.d_parts;
             if (used < nunits) nunits = used;
         }
-        p.part_slots = nunits;
         p.part_o_bytes = align256(nunits * BM * p.do_ * 4);
         p.part_lse_bytes = align256(nunits * BM * 4);
     }
