@@ -33,13 +33,6 @@ struct AppendArgs {
 };
 
 template <class KV>
-__device__ __forceinline__ uint4 round8(const float *src) {
-    const float4 x = ld_nc_f4(src), y = ld_nc_f4(src + 4);
-    return make_uint4(pack2(KV{}, x.x, x.y), pack2(KV{}, x.z, x.w), pack2(KV{}, y.x, y.y),
-                      pack2(KV{}, y.z, y.w));
-}
-
-template <class KV>
 __global__ void __launch_bounds__(256) page_append_kernel(const AppendArgs a) {
     const int64_t row_chunks = (int64_t)a.n_kv_heads * a.chunks;
     const int64_t work = (int64_t)a.total_tokens * row_chunks;
@@ -52,6 +45,10 @@ __global__ void __launch_bounds__(256) page_append_kernel(const AppendArgs a) {
         const int i = (int)(t / row_chunks);
         const int rem = (int)(t - (int64_t)i * row_chunks);
         const int g = rem / a.chunks, ch = rem - g * a.chunks;
+        // the row's data first: its loads are in flight while the slot is looked up
+        const int64_t src = ((int64_t)i * a.n_kv_heads + g) * (a.chunks * 8) + ch * 8;
+        const float4 k0 = ld_nc_f4(a.k_new + src), k1 = ld_nc_f4(a.k_new + src + 4);
+        const float4 v0 = ld_nc_f4(a.v_new + src), v1 = ld_nc_f4(a.v_new + src + 4);
         int lo = 0, hi = a.num_seqs - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -72,9 +69,10 @@ __global__ void __launch_bounds__(256) page_append_kernel(const AppendArgs a) {
         }
         const int64_t dst = (int64_t)page * a.page_stride + (p - pi * a.page_size) * a.token_stride +
                             (int64_t)g * a.head_stride + ch * 8;
-        const int64_t src = ((int64_t)i * a.n_kv_heads + g) * (a.chunks * 8) + ch * 8;
-        st_v4(a.k_pool + dst, round8<KV>(a.k_new + src));
-        st_v4(a.v_pool + dst, round8<KV>(a.v_new + src));
+        st_v4(a.k_pool + dst, make_uint4(pack2(KV{}, k0.x, k0.y), pack2(KV{}, k0.z, k0.w),
+                                         pack2(KV{}, k1.x, k1.y), pack2(KV{}, k1.z, k1.w)));
+        st_v4(a.v_pool + dst, make_uint4(pack2(KV{}, v0.x, v0.y), pack2(KV{}, v0.z, v0.w),
+                                         pack2(KV{}, v1.x, v1.y), pack2(KV{}, v1.z, v1.w)));
     }
 }
 
