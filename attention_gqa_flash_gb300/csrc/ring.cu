@@ -92,11 +92,9 @@ __global__ void __launch_bounds__(256) pack_attention_kernel(
     }
 }
 
-// Mask: every row (b, h, r) is a threshold: columns c < R + min(len_b, W-1-r)
-// are visible (the draft rows, then the history entries inside the window),
-// the rest are hidden.  The flat [B][H][R][K] array is cut into 8-element
-// chunks (16-byte stores); K is arbitrary, so a chunk may straddle rows.
-// IDX is int when the element count fits in 31 bits (cheap index math).
+// Mask: every row (b, h, r) of the [B][H][R][K] array is a threshold: columns
+// c < R + min(len_b, W-1-r) are visible (the draft rows, then the history entries
+// inside the window), the rest are hidden.
 template <typename IDX>
 __device__ __forceinline__ int mask_threshold(const uint32_t *cache_lengths, const RingGeom &g,
                                               IDX row) {
@@ -108,41 +106,39 @@ __device__ __forceinline__ int mask_threshold(const uint32_t *cache_lengths, con
     return g.R + (hist > 0 ? hist : 0);
 }
 
-template <typename IDX>
+// One warp per mask row (b, h, r): the row is a threshold, so a lane writes 16-byte
+// chunks of eight 0 / -inf values with no per-element index arithmetic; the few
+// elements before the row's first 16-byte boundary and after its last one (a row of
+// K bf16 values starts wherever row * K puts it) are written one by one.
 __global__ void __launch_bounds__(256) fill_mask_kernel(const uint32_t *__restrict__ cache_lengths,
                                                         uint16_t *__restrict__ mask, RingGeom g,
                                                         int32_t *status) {
-    const IDX total = (IDX)g.B * g.H * g.R * g.K;
-    const IDX nchunks = (total + 7) / 8;
+    const int64_t rows = (int64_t)g.B * g.H * g.R;
     if (blockIdx.x == 0 && threadIdx.x < g.B) {
         if (cache_lengths[threadIdx.x] > (uint32_t)g.W) raise_flag(status, GQA_FLAG_RING_CLAMPED);
     }
-    const IDX stride = (IDX)gridDim.x * blockDim.x;
-    for (IDX t = (IDX)blockIdx.x * blockDim.x + threadIdx.x; t < nchunks; t += stride) {
-        const IDX e0 = t * 8;
-        IDX row = e0 / g.K;
-        int c = (int)(e0 - row * g.K);
-        const IDX rows = total / g.K;
-        int thr = mask_threshold<IDX>(cache_lengths, g, row);
-        uint32_t w[4];
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); row < rows;
+         row += warps) {
+        const int thr = mask_threshold<int64_t>(cache_lengths, g, row);
+        uint16_t *m = mask + row * g.K;
+        const int head = (int)((8 - ((row * g.K) & 7)) & 7);  // elements before a 16-byte boundary
+        const int n = g.K;
+        const int lead = head < n ? head : n;
+        if (lane < lead) m[lane] = lane < thr ? 0x0000u : 0xff80u;
+        const int body = (n - lead) / 8;
+        for (int c = lane; c < body; c += 32) {
+            const int col0 = lead + c * 8;
+            uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t val = c < thr ? 0x0000u : 0xff80u;
-            if (i & 1)
-                w[i / 2] |= val << 16;
-            else
-                w[i / 2] = val;
-            if (++c == g.K) {
-                c = 0;
-                if (++row < rows) thr = mask_threshold<IDX>(cache_lengths, g, row);
-            }
+            for (int i = 0; i < 4; ++i)
+                w[i] = (col0 + 2 * i < thr ? 0x0000u : 0xff80u) |
+                       ((col0 + 2 * i + 1 < thr ? 0x0000u : 0xff80u) << 16);
+            st_v4(m + col0, make_uint4(w[0], w[1], w[2], w[3]));
         }
-        if (e0 + 8 <= total) {
-            st_v4(mask + e0, make_uint4(w[0], w[1], w[2], w[3]));
-        } else {
-            for (int i = 0; e0 + i < total; ++i)
-                mask[e0 + i] = (uint16_t)((w[i / 2] >> ((i & 1) * 16)) & 0xffff);
-        }
+        const int col = lead + body * 8 + lane;
+        if (col < n) m[col] = col < thr ? 0x0000u : 0xff80u;
     }
 }
 
@@ -232,14 +228,13 @@ cudaError_t launch_pack_attention(const uint16_t *ring_k, const uint16_t *ring_v
 cudaError_t launch_fill_mask(const uint32_t *cache_lengths, uint16_t *mask,
                              const gqa_ring_params &p, int32_t *status, cudaStream_t stream) {
     RingGeom g = geom_of(p);
-    int64_t work = ((int64_t)g.B * g.H * g.R * g.K + 7) / 8;
+    // one warp per row, eight warps per block, at most 8 blocks per SM
+    const int64_t rows = (int64_t)g.B * g.H * g.R;
+    int64_t blocks = (rows + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
     timing_mark(true, stream);
-    if ((int64_t)g.B * g.H * g.R * g.K + 8 < INT32_MAX)
-        fill_mask_kernel<int><<<grid_for(work, sm_count()), 256, 0, stream>>>(cache_lengths, mask,
-                                                                               g, status);
-    else
-        fill_mask_kernel<int64_t><<<grid_for(work, sm_count()), 256, 0, stream>>>(cache_lengths,
-                                                                                   mask, g, status);
+    fill_mask_kernel<<<(int)(blocks < 1 ? 1 : blocks), 256, 0, stream>>>(cache_lengths, mask, g, status);
     timing_mark(false, stream);
     return cudaGetLastError();
 }
