@@ -157,6 +157,11 @@ __global__ void __launch_bounds__(256) commit_kv_kernel(
         const int64_t bi = rest / g.HK;
         const int i = (int)(bi % g.MC);
         const int b = (int)(bi / g.MC);
+        // the offered row's data first (every offered row is in bounds): its loads are in
+        // flight while the counters are read
+        const int64_t src = rest * g.D + ch * 8;
+        const float4 k0 = ld_nc_f4(new_k + src), k1 = ld_nc_f4(new_k + src + 4);
+        const float4 v0 = ld_nc_f4(new_v + src), v1 = ld_nc_f4(new_v + src + 4);
         const uint32_t cnt = commit_counts[b];
         const uint32_t pos = write_positions[b];
         if (i == 0 && kh == 0 && ch == 0 && (cnt > (uint32_t)g.MC || pos >= (uint32_t)g.W))
@@ -164,10 +169,11 @@ __global__ void __launch_bounds__(256) commit_kv_kernel(
         const int n = cnt > (uint32_t)g.MC ? g.MC : (int)cnt;
         if (i >= n) continue;
         const int slot = (int)((pos % (uint32_t)g.W + (uint32_t)i) % (uint32_t)g.W);
-        const int64_t src = rest * g.D + ch * 8;
         const int64_t dst = (((int64_t)b * g.HK + kh) * g.W + slot) * g.D + ch * 8;
-        st_v4(ring_k + dst, f32x8_to_bf16x8(new_k + src));
-        st_v4(ring_v + dst, f32x8_to_bf16x8(new_v + src));
+        st_v4(ring_k + dst, make_uint4(pack_bf16x2(k0.x, k0.y), pack_bf16x2(k0.z, k0.w),
+                                       pack_bf16x2(k1.x, k1.y), pack_bf16x2(k1.z, k1.w)));
+        st_v4(ring_v + dst, make_uint4(pack_bf16x2(v0.x, v0.y), pack_bf16x2(v0.z, v0.w),
+                                       pack_bf16x2(v1.x, v1.y), pack_bf16x2(v1.z, v1.w)));
     }
 }
 
