@@ -92,3 +92,16 @@ def test_fused_full_size(lib):
     assert_attention_close(got, ref, "fused verify full size")
     assert_attention_close(got, _chain(lib, c, c.cache_lengths, c.write_positions).astype(np.float64),
                            "fused vs chain full size")
+
+
+def test_fused_long_window_uses_fixed_key_ranges(lib):
+    """A window of 20000 slots (158 key tiles, more than a unit's tile list holds): the
+    splits fall back to fixed key ranges; results still match the oracle."""
+    from gpu_helpers import assert_attention_close
+    c = workloads.ring(lanes=2, rows=8, window=20000, q_heads=4, kv_heads=1, head_dim=128, seed=77)
+    lens = np.array([19990, 7000], np.uint32)
+    pos = np.array([123, 19999], np.uint32)
+    got = _fused(lib, c, lens, pos)
+    ref = oracle.verify_ring_attention(c.ring_k, c.ring_v, c.cur_q, c.cur_k, c.cur_v, lens, pos,
+                                       c.geom, c.scale)
+    assert_attention_close(got, ref, "fused verify, window 20000")
