@@ -246,6 +246,68 @@ def _dev(torch, a, kind=None):
     return torch.from_numpy(a).cuda()
 
 
+class E2EPipe:
+    """End-to-end prefill steps double-buffered over three streams: step i's inputs go
+    host -> device on one stream while step i-1's attention runs on a second and its
+    output goes device -> host on a third.  Every step still copies its own inputs in
+    from pinned host memory and its result out; buffer set i % 2 is reused only after
+    the attention and the read-back of step i-2 that used it are done."""
+
+    def __init__(self, torch, g, case, host_in, dev0):
+        self.torch, self.g, self.case = torch, g, case
+        self.host_in = host_in
+        self.sets = [dev0, tuple(torch.empty_like(t) for t in dev0)]
+        self.hout = [torch.empty(dev0[4].shape, dtype=torch.float32).pin_memory()
+                     for _ in range(2)]
+        self.s_in, self.s_cmp, self.s_out = (torch.cuda.Stream() for _ in range(3))
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.ev_in, self.ev_kern, self.ev_out = ev(), ev(), ev()
+        self.used = [False, False]
+
+    def step(self, i: int):
+        torch, b = self.torch, i % 2
+        q, k, v, m, out, ws = self.sets[b]
+        with torch.cuda.stream(self.s_in):
+            if self.used[b]:
+                self.s_in.wait_event(self.ev_kern[b])
+            for d, h in zip((q, k, v, m), self.host_in):
+                d.copy_(h, non_blocking=True)
+            self.ev_in[b].record()
+        with torch.cuda.stream(self.s_cmp):
+            self.s_cmp.wait_event(self.ev_in[b])
+            if self.used[b]:
+                self.s_cmp.wait_event(self.ev_out[b])
+            self.g.gqa_attn_prefill(q, k, v, m, self.case.scale, out=out, workspace=ws)
+            self.ev_kern[b].record()
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(self.ev_kern[b])
+            self.hout[b].copy_(out, non_blocking=True)
+            self.ev_out[b].record()
+        self.used[b] = True
+
+    def run(self, steps: int, warmup: int) -> float:
+        """Mean device ms per step over `steps` pipelined steps, after `warmup` of them;
+        CUDA events on the current stream bracket the run, joined to all three streams."""
+        torch = self.torch
+        cur = torch.cuda.current_stream()
+        for i in range(warmup):
+            self.step(i)
+        for s in (self.s_in, self.s_cmp, self.s_out):
+            cur.wait_stream(s)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for s in (self.s_in, self.s_cmp, self.s_out):
+            s.wait_stream(cur)
+        for i in range(warmup, warmup + steps):
+            self.step(i)
+        for s in (self.s_in, self.s_cmp, self.s_out):
+            cur.wait_stream(s)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+
 def setup_prefill(torch, g, case):
     kind = "bf16" if case.kv_dtype == "bf16" else None
     q, k, v, m = (_dev(torch, case.q), _dev(torch, case.k, kind), _dev(torch, case.v, kind),
@@ -271,6 +333,8 @@ def setup_prefill(torch, g, case):
         m.copy_(hm, non_blocking=True)
         g.gqa_attn_prefill(q, k, v, m, case.scale, out=out, workspace=ws)
         hout.copy_(out, non_blocking=True)
+
+    e2e_step.pipe = lambda: E2EPipe(torch, g, case, (hq, hk, hv, hm), (q, k, v, m, out, ws))
 
     nb = lambda t: t.numel() * t.element_size()
     # classification pre-pass + attention kernel (these workloads need no key split)
@@ -529,8 +593,13 @@ def main() -> None:
     value = world * info["flops"] / (ms_step * 1e-3) / 1e12
     kern = tm.kernel_ms(g, step, max(10, args.steps))
     achieved = info["flops"] / (kern * 1e-3) / 1e12
-    # end to end through the public call, eagerly (host copies, marshalling and launches included)
-    e2e_ms = tm.max_over_ranks(sum(tm.steps(e2e_step, args.steps, args.warmup, graph=False)) / args.steps)
+    # end to end through the public call, eagerly (host copies, marshalling and launches
+    # included): one step at a time, and double-buffered (the reported figure)
+    e2e_serial = tm.max_over_ranks(sum(tm.steps(e2e_step, args.steps, args.warmup, graph=False)) / args.steps)
+    pipe = e2e_step.pipe()
+    tm.barrier()
+    e2e_ms = tm.max_over_ranks(pipe.run(args.steps, args.warmup))
+    del pipe
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -551,7 +620,10 @@ def main() -> None:
                      "traffic": traffic_for("attn_kernel<256,f16>", head.name)},
         "e2e": {"value": world * info["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": info["h2d"],
-                "d2h_bytes_per_step": info["d2h"]},
+                "d2h_bytes_per_step": info["d2h"],
+                "pipeline": "double-buffered: each step's host-to-device copy overlaps the "
+                            "previous step's attention and device-to-host copy",
+                "serial_ms_per_step": e2e_serial},
         "gpu_launches": info["launches"] * args.steps,
         "clocks": clk.summary(),
     }
