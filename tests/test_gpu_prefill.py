@@ -61,6 +61,8 @@ def test_tiny_prefill_full(lib):
     (256, 384, 8, 2, 256, 128, "bf16"),    # two pairs per KV head, bf16, prefix
     (128, 4000, 2, 1, 256, 3872, "f16"),   # one pair, keys split across many clusters
     (300, 700, 4, 2, 512, 400, "f16"),     # d512 pairs, ragged rows and keys
+    (48, 300, 16, 2, 128, 252, "f16"),     # 8 query heads per KV head, several heads per tile
+    (33, 97, 8, 1, 256, 64, "bf16"),       # one KV head for 8 query heads, odd sizes
 ])
 def test_prefill_shapes(lib, pairs_mode, rows, kv_len, h, hk, d, pos0, dtype):
     from gpu_helpers import assert_attention_close
