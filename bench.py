@@ -472,6 +472,94 @@ def cpu_baseline(case, target_s: float = 12.0) -> dict:
                       f"({f / 1e9:.1f} GFLOP, {t:.1f} s), float64 C with OpenMP"}
 
 
+def _cpu_line(value: float, unit: str, sample: str) -> dict:
+    import oracle
+    return {"value": value, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": sample}
+
+
+def cpu_prefill(case, target_s: float = 3.0) -> dict:
+    """The oracle on sampled (query row, head) outputs of a prefill workload."""
+    t, _ = oracle_prefill_sample(case, 16)
+    n = int(min(case.rows * case.n_heads, max(16, target_s / max(t / 16, 1e-6))))
+    t, f = oracle_prefill_sample(case, n, seed=2)
+    return _cpu_line(f / t / 1e12, "TFLOP/s",
+                     f"{n} random (query row, head) outputs ({f / 1e9:.1f} GFLOP, {t:.1f} s)")
+
+
+def cpu_decode(c, target_s: float = 3.0) -> dict:
+    """The oracle's paged decode of a random subset of the sequences; GB/s of their K/V."""
+    import oracle
+    order = np.random.default_rng(3).permutation(c.num_seqs).astype(np.int32)
+    per_tok = c.n_kv_heads * c.head_dim * 2 * 2
+
+    def run(seqs):
+        t0 = time.perf_counter()
+        oracle.paged_decode(c.q, c.k_pool, c.v_pool, kv_dtype=c.kv_dtype, page_table=c.page_table,
+                            context_lens=c.context_lens, scale=c.scale, seqs=seqs)
+        return time.perf_counter() - t0, int(c.context_lens[seqs].astype(np.int64).sum()) * per_tok
+
+    t, b = run(order[:1])
+    budget = b / max(t, 1e-6) * target_s  # bytes the oracle gets through in target_s
+    lens = c.context_lens[order].astype(np.int64) * per_tok
+    n = int(min(c.num_seqs, max(1, np.searchsorted(np.cumsum(lens), budget) + 1)))
+    t, b = run(order[:n])
+    return _cpu_line(b / t / 1e9, "GB/s",
+                     f"{n} of {c.num_seqs} sequences ({b / 1e9:.2f} GB of K/V, {t:.1f} s)")
+
+
+def cpu_verify(c, chain_bytes: int, fused_bytes: int) -> tuple[dict, dict]:
+    """The oracle's verify step on the whole workload: pack, mask, attention over the
+    packed copy and commit; and the attention read straight from the ring."""
+    import oracle
+    t0 = time.perf_counter()
+    pq, pk, pv = oracle.pack_attention(c.ring_k, c.ring_v, c.cur_q, c.cur_k, c.cur_v,
+                                       c.cache_lengths, c.write_positions, c.geom)
+    m = oracle.fill_mask(c.cache_lengths, c.geom)
+    oracle.verify_attention(pq, pk, pv, m, c.geom, c.scale)
+    oracle.commit_kv(c.new_k, c.new_v, c.commit_counts, c.write_positions, c.ring_k, c.ring_v, c.geom)
+    t_chain = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.verify_ring_attention(c.ring_k, c.ring_v, c.cur_q, c.cur_k, c.cur_v, c.cache_lengths,
+                                 c.write_positions, c.geom, c.scale)
+    oracle.commit_kv(c.new_k, c.new_v, c.commit_counts, c.write_positions, c.ring_k, c.ring_v, c.geom)
+    t_fused = time.perf_counter() - t0
+    return (_cpu_line(chain_bytes / t_chain / 1e9, "GB/s", f"the whole step ({t_chain:.2f} s)"),
+            _cpu_line(fused_bytes / t_fused / 1e9, "GB/s", f"the whole step ({t_fused:.2f} s)"))
+
+
+def cpu_chunk(c, target_s: float = 3.0) -> dict:
+    """The oracle's page append and chunked prefill for the first tokens of one sequence
+    (the one with the longest cached prefix)."""
+    import oracle
+    s = int(np.argmax(c.position_start))
+    o0, ps = int(c.token_offsets[s]), int(c.position_start[s])
+    ntok = int(c.token_offsets[s + 1]) - o0
+    strides = dict(page_stride=c.k_pool.strides[0] // 2, token_stride=c.k_pool.strides[1] // 2,
+                   head_stride=c.k_pool.strides[2] // 2)
+
+    def run(n):
+        offs = np.array([0, n], np.int32)
+        pos = np.array([ps], np.int32)
+        pt = c.page_table[s:s + 1]
+        t0 = time.perf_counter()
+        kp, vp, _ = oracle.paged_append(c.k_new[o0:o0 + n], c.v_new[o0:o0 + n], offs, pos, pt,
+                                        c.k_pool, c.v_pool, kv_dtype=c.kv_dtype,
+                                        page_size=c.page_size, **strides)
+        oracle.paged_prefill(c.q[o0:o0 + n], kp, vp, pt, offs, pos, kv_dtype=c.kv_dtype,
+                             n_kv_heads=c.n_kv_heads, page_size=c.page_size, scale=c.scale,
+                             **strides)
+        f = 4.0 * c.n_heads * c.head_dim * (n * ps + n * (n + 1) // 2)
+        return time.perf_counter() - t0, f
+
+    t, _ = run(4)
+    n = int(min(ntok, max(4, 4 * target_s / max(t, 1e-6))))
+    t, f = run(n)
+    return _cpu_line(f / t / 1e12, "TFLOP/s",
+                     f"append and attention of the first {n} of {ntok} new tokens of one sequence "
+                     f"after {ps} cached ({f / 1e9:.1f} GFLOP, {t:.1f} s)")
+
+
 def run_reference(args, case) -> None:
     """--impl reference: the oracle, as it stands, on bounded samples of the workload."""
     import oracle
@@ -630,6 +718,8 @@ def main() -> None:
     del step, e2e_step
     torch.cuda.empty_cache()
 
+    # the oracle beside each path, on rank 0 of a single-GPU run (after that path's GPU timing)
+    cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     if args.paths == "all":
         paths = {}
         # prefill d512 with a 7168-token prefix
@@ -646,6 +736,8 @@ def main() -> None:
                          "unit": "TFLOP/s", "frac": i512["flops"] / (k * 1e-3) / 1e12 / tensor_peak,
                          "kernel_ms": k, "traffic": traffic_for("attn_kernel<512,f16>", c512.name),
                          "note": "two output halves recompute Q.K^T: executed FLOPs are 1.5x"}}
+        if cpu:
+            paths["prefill_d512_prefix"]["cpu_baseline"] = cpu_prefill(c512)
         del s512
         torch.cuda.empty_cache()
         # paged decode
@@ -661,6 +753,8 @@ def main() -> None:
                          "achieved": idc["kernel_bytes"] / (k * 1e-3) / 1e9, "peak": hbm_peak,
                          "unit": "GB/s", "frac": idc["kernel_bytes"] / (k * 1e-3) / 1e9 / hbm_peak,
                          "kernel_ms": k, "traffic": traffic_for("paged_decode_kernel<f16,128>", dc.name)}}
+        if cpu:
+            paths["paged_decode"]["cpu_baseline"] = cpu_decode(dc)
         del sd, dc
         torch.cuda.empty_cache()
         # speculative verify chain
@@ -699,6 +793,9 @@ def main() -> None:
                                  "unit": "GB/s", "ms_per_step": t, "bytes_per_step": ftotal,
                                  "peak": hbm_peak, "frac": ftotal / (t * 1e-3) / 1e9 / hbm_peak,
                                  "kernels": fkernels}
+        if cpu:
+            paths["verify_chain"]["cpu_baseline"], paths["verify_fused"]["cpu_baseline"] = \
+                cpu_verify(vc, total, ftotal)
         del sv, ops, fops, fstep, vc
         torch.cuda.empty_cache()
         # chunked prefill over pages: page append + attention
@@ -719,6 +816,8 @@ def main() -> None:
                        "traffic": traffic_for("page_append_kernel<f16>", cc.name),
                        "kernel_ms": ka, "achieved_gbs": ic["append_bytes"] / (ka * 1e-3) / 1e9,
                        "frac": ic["append_bytes"] / (ka * 1e-3) / 1e9 / hbm_peak}}
+        if cpu:
+            paths["paged_chunk_prefill"]["cpu_baseline"] = cpu_chunk(cc)
         del sc, cops, cc
         torch.cuda.empty_cache()
         line["paths"] = paths
