@@ -164,3 +164,18 @@ def test_paged_prefill_rejects_bad_arguments_before_launch(g):
     ws = lib.gqa_attn_paged_prefill_workspace_size(2, 8, 4, 2, 128, 4, 16)
     assert (rc == 1 and "workspace" in lib.gqa_last_error().decode()) or ws == 0
     assert lib.gqa_attn_paged_prefill_workspace_size(2, 8, 4, 2, 96, 4, 16) == 0
+
+
+def test_no_cpu_fallback(g, monkeypatch):
+    """The product path fails loudly: host tensors are refused, and a missing library
+    raises instead of falling back to anything else."""
+    import torch
+    q = torch.zeros((64, 4, 128), dtype=torch.float32)
+    kv = torch.zeros((64, 2, 128), dtype=torch.float16)
+    mask = torch.zeros((64, 64), dtype=torch.float16)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        g.gqa_attn_prefill(q, kv, kv, mask, 1.0)
+    monkeypatch.setattr(g, "_lib", None)
+    monkeypatch.setattr(g, "LIB_PATH", ROOT / "attention_gqa_flash_gb300" / "lib" / "absent.so")
+    with pytest.raises(RuntimeError, match="missing"):
+        g.library()
