@@ -179,3 +179,27 @@ def test_no_cpu_fallback(g, monkeypatch):
     monkeypatch.setattr(g, "LIB_PATH", ROOT / "attention_gqa_flash_gb300" / "lib" / "absent.so")
     with pytest.raises(RuntimeError, match="missing"):
         g.library()
+
+
+def _declared_arity() -> dict[str, int]:
+    """Parameter count of every function declared in the header."""
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(gqa_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header(g):
+    """Every function the Python binding types has the header's parameter count."""
+    lib = g.library()
+    arity = _declared_arity()
+    typed = 0
+    for name, n in arity.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            continue
+        typed += 1
+        assert len(fn.argtypes) == n, f"{name}: binding has {len(fn.argtypes)} arguments, header {n}"
+    assert typed == len(arity), "every declared function is typed by the binding"
