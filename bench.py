@@ -552,8 +552,9 @@ def cpu_chunk(c, target_s: float = 3.0) -> dict:
         f = 4.0 * c.n_heads * c.head_dim * (n * ps + n * (n + 1) // 2)
         return time.perf_counter() - t0, f
 
-    t, _ = run(4)
-    n = int(min(ntok, max(4, 4 * target_s / max(t, 1e-6))))
+    n0 = min(4, ntok)
+    t, _ = run(n0)
+    n = int(min(ntok, max(n0, n0 * target_s / max(t, 1e-6))))
     t, f = run(n)
     return _cpu_line(f / t / 1e12, "TFLOP/s",
                      f"append and attention of the first {n} of {ntok} new tokens of one sequence "
