@@ -532,7 +532,8 @@ def cpu_chunk(c, target_s: float = 3.0) -> dict:
     """The oracle's page append and chunked prefill for the first tokens of one sequence
     (the one with the longest cached prefix)."""
     import oracle
-    s = int(np.argmax(c.position_start))
+    counts = np.diff(c.token_offsets)
+    s = int(np.argmax(np.where(counts > 0, c.position_start, -1)))
     o0, ps = int(c.token_offsets[s]), int(c.position_start[s])
     ntok = int(c.token_offsets[s + 1]) - o0
     strides = dict(page_stride=c.k_pool.strides[0] // 2, token_stride=c.k_pool.strides[1] // 2,
