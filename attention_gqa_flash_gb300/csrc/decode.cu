@@ -402,28 +402,64 @@ cudaError_t launch_paged_decode(const DecodeProblem &p, void *workspace, cudaStr
 // Fixed scratch for gqa_attn_paged_decode_noalloc: callers that cannot give the
 // library a device buffer get the split-KV partials kept here instead.  The
 // array is part of the library's device image; its device address is looked
-// up once per device (with that device current) and cached.
+// up with the device current and cached per device, together with the
+// identity of the context it was looked up in: a device reset destroys that
+// context (and the module holding the array), so an address cached before the
+// reset is never handed out after it -- the next call looks it up again.
 // ---------------------------------------------------------------------------
+#include <cuda.h>
+
 #include <mutex>
 
 namespace gqa {
 namespace {
 static __device__ __align__(256) unsigned char g_decode_fixed_scratch[GQA_NOALLOC_SCRATCH_BYTES];
 std::mutex g_fixed_scratch_mu;
-void *g_fixed_scratch_addr[64] = {nullptr};
+constexpr int kMaxDevices = 64;
+void *g_fixed_scratch_addr[kMaxDevices] = {nullptr};
+unsigned long long g_fixed_scratch_ctx[kMaxDevices] = {0};
+
+// Unique id (over the process lifetime) of the current context, or 0 when it
+// cannot be had; 0 never matches a cached entry, so the address is looked up again.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 }  // namespace
 
 cudaError_t decode_fixed_scratch(void **ptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_fixed_scratch_mu);
-    if (!g_fixed_scratch_addr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_fixed_scratch_addr[dev] || ctx == 0 || ctx != g_fixed_scratch_ctx[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_decode_fixed_scratch);
         if (e != cudaSuccess) return e;
         g_fixed_scratch_addr[dev] = p;
+        // the lookup makes the device's primary context current if it was not yet
+        g_fixed_scratch_ctx[dev] = current_context_id();
     }
     *ptr = g_fixed_scratch_addr[dev];
     return cudaSuccess;

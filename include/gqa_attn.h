@@ -189,7 +189,9 @@ int gqa_attn_paged_decode(const float *q, size_t q_bytes, const void *k_pages,
  *     exceeds GQA_NOALLOC_SCRATCH_BYTES are rejected with GQA_INVALID_ARGUMENT.
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture.  The address is cached with the identity of the context
+ *     it belongs to: after a cudaDeviceReset the next call on that device
+ *     looks it up again (make that call, too, outside any capture).
  *   - All calls share the one array and nothing in it needs clearing between
  *     calls, but calls whose work overlaps on the GPU (two streams, or two
  *     threads) race on it: serialise them.

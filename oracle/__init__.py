@@ -9,8 +9,9 @@ independent output rows).  This module only compiles it with gcc, loads it
 with ctypes and marshals NumPy arrays.  Strides are taken from the arrays
 themselves, so strided views are evaluated exactly as laid out.
 
-Pinned by ``tests/test_oracle_pins.py`` against the pages' worked example,
-closed forms, invariants and library routines (see that file's header).
+Pinned by ``tests/test_oracle_attention.py``, ``test_oracle_conversions.py``,
+``test_oracle_paged.py`` and ``test_oracle_ring.py`` against the pages' worked
+examples, closed forms, invariants and library routines (see each file's header).
 """
 from __future__ import annotations
 

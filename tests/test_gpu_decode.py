@@ -86,14 +86,13 @@ def test_bad_page_ids_are_clamped_and_flagged(lib):
     assert st & GQA_FLAG_CONTEXT_CLAMPED
 
 
-def test_full_size_decode_sampled(lib):
-    """64 sequences, contexts U{512..16384}, 65536-page pool, h32/hk8, d128."""
+def test_full_size_decode(lib):
+    """64 sequences, contexts U{512..16384}, 65536-page pool, h32/hk8, d128: every
+    (sequence, head) output."""
     from gpu_helpers import assert_attention_close
     c = workloads.paged_decode(seed=0)
     got, st = _run(lib, c)
     assert st == 0
-    assert np.all(np.isfinite(got))
-    seqs = np.array([0, int(np.argmax(c.context_lens)), int(np.argmin(c.context_lens)), 17, 42, 63])
     ref = oracle.paged_decode(c.q, c.k_pool, c.v_pool, kv_dtype="f16", page_table=c.page_table,
-                              context_lens=c.context_lens, scale=c.scale, seqs=seqs)
-    assert_attention_close(got[seqs], ref, "full-size decode")
+                              context_lens=c.context_lens, scale=c.scale)
+    assert_attention_close(got, ref, "full-size decode")

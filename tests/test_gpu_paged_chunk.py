@@ -135,11 +135,12 @@ def test_chunked_prefill_leaves_rows_of_no_sequence_alone(lib):
     assert torch.all(out[T:] == 7.0)
 
 
-def test_chunked_prefill_full_size_sampled(lib):
+def test_chunked_prefill_full_size(lib):
     """8 sequences x 512 new tokens over cached prefixes of up to 7680 tokens, 16/4
-    heads, head_dim 256, 16-slot f16 pages: every output must be finite, and sampled
-    query tokens match the oracle (a single query at position p over the pages is
-    the decode definition with context p + 1)."""
+    heads, head_dim 256, 16-slot f16 pages: the appended pages bit for bit, every
+    output finite, and every token of three whole sequences -- the one with the
+    longest cached prefix, the one with the shortest, and one more -- against the
+    oracle's chunked prefill over the oracle's own appended pages."""
     import torch
     from gpu_helpers import assert_attention_close, dev, new_status
     c = workloads.paged_chunk_full(seed=0)
@@ -152,17 +153,19 @@ def test_chunked_prefill_full_size_sampled(lib):
     assert int(status.item()) == 0
     got = out.cpu().numpy()
     assert np.all(np.isfinite(got))
-    rng = np.random.default_rng(5)
-    sel = np.sort(rng.choice(c.tokens, 48, replace=False))
-    seq = np.searchsorted(c.token_offsets, sel, side="right") - 1
-    pos = c.position_start[seq] + (sel - c.token_offsets[seq])
     rk, rv, _ = oracle.paged_append(c.k_new, c.v_new, c.token_offsets, c.position_start,
                                     c.page_table, c.k_pool, c.v_pool, kv_dtype="f16", **_strides(c))
     np.testing.assert_array_equal(_bits(kp), rk.view(np.uint16))
     np.testing.assert_array_equal(_bits(vp), rv.view(np.uint16))
-    ref = oracle.paged_decode(c.q[sel], rk, rv, kv_dtype="f16", page_table=c.page_table[seq],
-                              context_lens=(pos + 1).astype(np.int32), scale=c.scale)
-    assert_attention_close(got[sel], ref, "chunked prefill full size (sampled)")
+    seqs = sorted({int(np.argmax(c.position_start)), int(np.argmin(c.position_start)), 3})
+    for s in seqs:
+        o0, o1 = int(c.token_offsets[s]), int(c.token_offsets[s + 1])
+        ref = oracle.paged_prefill(c.q[o0:o1], rk, rv, c.page_table[s:s + 1],
+                                   np.array([0, o1 - o0], np.int32), c.position_start[s:s + 1],
+                                   kv_dtype="f16", n_kv_heads=c.n_kv_heads, scale=c.scale,
+                                   **_strides(c))
+        assert_attention_close(got[o0:o1], ref, f"chunked prefill full size, sequence {s} "
+                                                f"({o1 - o0} tokens after {int(c.position_start[s])})")
 
 
 def test_chunked_prefill_edge_cases(lib):

@@ -40,43 +40,50 @@ def _verify(g, c, lengths=None):
     return out.cpu().numpy(), host_bits(pq), host_bits(pk), host_bits(pv), host_bits(mask)
 
 
-@pytest.mark.parametrize("lanes,rows,window,h,hk,d", [
-    (1, 2, 5, 2, 1, 128), (2, 16, 200, 8, 2, 128), (3, 8, 150, 8, 8, 256), (4, 16, 700, 32, 8, 256)])
-def test_verify_attention_small(lib, lanes, rows, window, h, hk, d):
-    from gpu_helpers import assert_attention_close
-    c = workloads.ring(lanes=lanes, rows=rows, window=window, q_heads=h, kv_heads=hk,
-                       head_dim=d, seed=window)
-    got, pq, pk, pv, mask = _verify(lib, c)
-    ref = oracle.verify_attention(pq, pk, pv, mask, c.geom, c.scale)
-    assert_attention_close(got, ref, f"verify lanes{lanes} r{rows} w{window} d{d}")
-
-
-def test_verify_empty_history(lib):
-    from gpu_helpers import assert_attention_close
-    c = workloads.ring(lanes=2, rows=4, window=70, q_heads=4, kv_heads=2, head_dim=128, seed=9)
-    lengths = np.array([0, 69], np.uint32)
-    got, pq, pk, pv, mask = _verify(lib, c, lengths)
-    ref = oracle.verify_attention(pq, pk, pv, mask, c.geom, c.scale)
-    assert_attention_close(got, ref, "verify empty history")
-
-
-def test_full_size_verify_sampled(lib):
-    """lanes 4, rows 16, window 4096, h32/hk8, d256: every pack/mask bit, sampled outputs."""
-    from gpu_helpers import assert_attention_close
-    c = workloads.verify_full(seed=0)
-    got, pq, pk, pv, mask = _verify(lib, c)
+def _oracle_chain(c, lengths=None):
+    """The oracle's own pack and mask from the host inputs, and its attention over them
+    (nothing here comes from the GPU)."""
+    lengths = c.cache_lengths if lengths is None else lengths
     opq, opk, opv = oracle.pack_attention(c.ring_k, c.ring_v, c.cur_q, c.cur_k, c.cur_v,
-                                          c.cache_lengths, c.write_positions, c.geom)
+                                          lengths, c.write_positions, c.geom)
+    omask = oracle.fill_mask(lengths, c.geom)
+    return opq, opk, opv, omask
+
+
+def _check_chain(got, pq, pk, pv, mask, ref_ops, what, scale, geom):
+    """The GPU's pack and mask bit for bit, then its attention against the oracle's
+    attention over the oracle's own packed operands."""
+    from gpu_helpers import assert_attention_close
+    opq, opk, opv, omask = ref_ops
     np.testing.assert_array_equal(pq, opq)
     np.testing.assert_array_equal(pk, opk)
     np.testing.assert_array_equal(pv, opv)
-    np.testing.assert_array_equal(mask, oracle.fill_mask(c.cache_lengths, c.geom))
-    rng = np.random.default_rng(0)
-    B, H, HK, D, R = c.geom[:5]
-    pairs = [np.stack([rng.integers(0, R, 24), rng.integers(0, H, 24)], 1).astype(np.int32)
-             for _ in range(B)]
-    for p in pairs:
-        p[:2] = [[0, 0], [R - 1, H - 1]]
-    refs = oracle.verify_attention(pq, pk, pv, mask, c.geom, c.scale, pairs_per_lane=pairs)
-    for b in range(B):
-        assert_attention_close(got[b, pairs[b][:, 0], pairs[b][:, 1]], refs[b], f"lane {b}")
+    np.testing.assert_array_equal(mask, omask)
+    ref = oracle.verify_attention(opq, opk, opv, omask, geom, scale)
+    assert_attention_close(got, ref, what)
+
+
+@pytest.mark.parametrize("lanes,rows,window,h,hk,d", [
+    (1, 2, 5, 2, 1, 128), (2, 16, 200, 8, 2, 128), (3, 8, 150, 8, 8, 256), (4, 16, 700, 32, 8, 256)])
+def test_verify_attention_small(lib, lanes, rows, window, h, hk, d):
+    c = workloads.ring(lanes=lanes, rows=rows, window=window, q_heads=h, kv_heads=hk,
+                       head_dim=d, seed=window)
+    got, pq, pk, pv, mask = _verify(lib, c)
+    _check_chain(got, pq, pk, pv, mask, _oracle_chain(c), f"verify lanes{lanes} r{rows} w{window} d{d}",
+                 c.scale, c.geom)
+
+
+def test_verify_empty_history(lib):
+    c = workloads.ring(lanes=2, rows=4, window=70, q_heads=4, kv_heads=2, head_dim=128, seed=9)
+    lengths = np.array([0, 69], np.uint32)
+    got, pq, pk, pv, mask = _verify(lib, c, lengths)
+    _check_chain(got, pq, pk, pv, mask, _oracle_chain(c, lengths), "verify empty history",
+                 c.scale, c.geom)
+
+
+def test_full_size_verify(lib):
+    """lanes 4, rows 16, window 4096, h32/hk8, d256: every pack and mask bit, and every
+    (lane, row, head) output against the oracle's attention over its own packed operands."""
+    c = workloads.verify_full(seed=0)
+    got, pq, pk, pv, mask = _verify(lib, c)
+    _check_chain(got, pq, pk, pv, mask, _oracle_chain(c), "full-size verify", c.scale, c.geom)

@@ -10,12 +10,14 @@ image.
 
 Checked here, through the C ABI: two calls in a row (on different inputs, so
 stale contents of the shared array would show) agree with the regular entry
-point within the attention tolerance, and a problem too large for the fixed
-array is refused with a clear message.  This file is collected last.
+point and with the float64 oracle within the attention tolerance, and a problem
+too large for the fixed array is refused with a clear message.  This file is
+collected last.
 """
 import numpy as np
 import pytest
 
+import oracle
 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -56,8 +58,13 @@ def test_two_calls_match_the_workspace_entry_point(lib):
         lib.gqa_attn_paged_decode_noalloc(*args, c.scale, out=out, status=st)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
-        assert_attention_close(out.cpu().numpy(), ref.cpu().numpy().astype(np.float64),
+        got = out.cpu().numpy()
+        assert_attention_close(got, ref.cpu().numpy().astype(np.float64),
                                "no-alloc decode vs workspace decode")
+        expect = oracle.paged_decode(c.q, c.k_pool, c.v_pool, kv_dtype="f16",
+                                     page_table=c.page_table, context_lens=c.context_lens,
+                                     scale=c.scale)
+        assert_attention_close(got, expect, "no-alloc decode vs the oracle")
 
 
 def test_oversized_problem_is_refused(lib):
