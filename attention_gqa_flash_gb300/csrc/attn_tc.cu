@@ -1289,7 +1289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         put_q(qs, w);
                     }
-                    tc::named_bar(1, kSoftmaxThreads);  // every softmax thread is done with this stage
+                    ok = tc::named_bar_and(1, kSoftmaxThreads, ok);  // every softmax thread is done with this stage
                     if (threadIdx.x == 0 && !hold) release_slot(stage);
                 }
             } else if (!a.q_f32) {
@@ -1402,6 +1402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int cur_n = 0, cur_pos = 0;  // visible tiles and first ring position of unit k
         if (a.sched_counter || slot_unit(0, slot, slots, units) >= 0) {
             ok = __all_sync(0xffffffffu, wt.wait(list_full(0), 0));
+            ok = tc::named_bar_and(1, kSoftmaxThreads, ok);
             uid = ok ? uid_smem[0] : -1;
             if (uid >= 0) {
                 cur = unit_of(a, uid, PAIR, rank, DO);
@@ -1625,8 +1626,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool stage_o = a.o_tma && cur_n > 0 && (!PAGED || cur.q_row0 + BM <= cur.ntok);
             int o_slot0 = 0;       // first ring position of the staging area
             bool hold_q = false;   // staging in the next unit's Q slots
+            // every softmax warp takes the same path from here (a failed wait in one of
+            // them ends the loop for all)
+            ok = tc::named_bar_and(1, kSoftmaxThreads, ok);
             if (ok && (a.sched_counter || slot_unit(k + 1, slot, slots, units) >= 0)) {
                 ok = __all_sync(0xffffffffu, wt.wait(list_full((k + 1) & 1), ((k + 1) >> 1) & 1));
+                ok = tc::named_bar_and(1, kSoftmaxThreads, ok);
                 nuid = ok ? uid_smem[(k + 1) & 1] : -1;
             }
             if (nuid >= 0) {
@@ -1649,6 +1654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = __all_sync(0xffffffffu, wt.wait(o_done((ga - 1) & 1), ((ga - 1) >> 1) & 1));
                 tc::tc_fence_after();
             }
+            ok = tc::named_bar_and(1, kSoftmaxThreads, ok);
             // row sum = both halves' partial sums (the second barrier keeps the next
             // unit's first row-max exchange, which reuses this buffer, behind the reads)
             {
@@ -2027,8 +2033,10 @@ template <int D, class KV, bool PAIR, int MODE = kMaskMode>
 cudaError_t run_attn(const AttnArgs &a, const CUtensorMap *maps, int units, int tiles,
                      cudaStream_t stream) {
     auto kern = attn_kernel<D, KV, PAIR, MODE>;
-    static bool configured = false;
-    if (!configured) {
+    // function attributes belong to each device's context: set once per device (and
+    // again after a reset)
+    static DeviceSetup setup;
+    cudaError_t se = setup.run([&]() -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Layout<D>::kBytes);
         if (e != cudaSuccess) return e;
@@ -2040,8 +2048,9 @@ cudaError_t run_attn(const AttnArgs &a, const CUtensorMap *maps, int units, int 
         if (2 * 128 * kSoftmaxRegs + 128 * kControlRegs > kThreads * fa.numRegs ||
             kSoftmaxRegs < fa.numRegs || kControlRegs > fa.numRegs)
             return cudaErrorInvalidConfiguration;
-        configured = true;
-    }
+        return cudaSuccess;
+    });
+    if (se != cudaSuccess) return se;
     timing_mark(true, stream);
     {
         // programmatic dependent launch: the kernel's set-up (barriers, TMEM, tensor-map

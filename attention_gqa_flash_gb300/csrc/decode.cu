@@ -323,15 +323,26 @@ template <class KV, int D>
 cudaError_t run(const DecodeArgs &a, cudaStream_t stream) {
     const size_t smem = Smem<D>::kBytes;
     auto kern = paged_decode_kernel<KV, D>;
-    static int occ = 0;  // resident CTAs per SM for this instantiation
-    if (occ == 0) {
+    // resident CTAs per SM for this instantiation, per device (function attributes
+    // belong to each device's context)
+    static DeviceSetup setup;
+    static int occ_of[DeviceSetup::kMaxDevices] = {0};
+    int dev = 0;
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return de;
+    if (dev < 0 || dev >= DeviceSetup::kMaxDevices) return cudaErrorInvalidDevice;
+    de = setup.run([&]() -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;
+        int occ = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kWarps * 32, smem);
         if (e != cudaSuccess) return e;
-        if (occ < 1) occ = 1;
-    }
+        occ_of[dev] = occ < 1 ? 1 : occ;
+        return cudaSuccess;
+    });
+    if (de != cudaSuccess) return de;
+    const int occ = occ_of[dev];
     const int64_t units = (int64_t)a.num_seqs * a.n_kv_heads * a.head_groups * a.max_chunks;
     int64_t grid = (int64_t)sm_count() * occ;
     if (grid > units) grid = units;
@@ -419,31 +430,6 @@ constexpr int kMaxDevices = 64;
 void *g_fixed_scratch_addr[kMaxDevices] = {nullptr};
 unsigned long long g_fixed_scratch_ctx[kMaxDevices] = {0};
 
-// Unique id (over the process lifetime) of the current context, or 0 when it
-// cannot be had; 0 never matches a cached entry, so the address is looked up again.
-unsigned long long current_context_id() {
-    using GetCurrent = CUresult (*)(CUcontext *);
-    using GetId = CUresult (*)(CUcontext, unsigned long long *);
-    static GetCurrent get_current = nullptr;
-    static GetId get_id = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            get_current = reinterpret_cast<GetCurrent>(f);
-        f = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            get_id = reinterpret_cast<GetId>(f);
-    });
-    if (!get_current || !get_id) return 0;
-    CUcontext ctx = nullptr;
-    unsigned long long id = 0;
-    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
-    return id;
-}
 }  // namespace
 
 cudaError_t decode_fixed_scratch(void **ptr) {

@@ -5,12 +5,43 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "gqa_attn.h"
 
 namespace gqa {
 
 // SM count of the current device (cached per device).
 int sm_count();
+
+// Unique id (over the process lifetime) of the calling thread's current context,
+// or 0 when there is none or it cannot be had.
+unsigned long long current_context_id();
+
+// Runs a set-up step (kernel function attributes, occupancy queries) once per
+// device and context, thread-safely: function attributes belong to a device's
+// context, so a second device, or the same device after a reset, runs it again.
+// While the context id is unavailable the step runs on every call.
+struct DeviceSetup {
+    static constexpr int kMaxDevices = 64;
+    std::mutex mu;
+    unsigned long long ctx[kMaxDevices] = {};
+    template <class F>
+    cudaError_t run(F &&step) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lock(mu);
+        const unsigned long long id = current_context_id();
+        if (id != 0 && ctx[dev] == id) return cudaSuccess;
+        e = step();
+        if (e != cudaSuccess) return e;
+        // the step made the device's primary context current if it was not yet
+        ctx[dev] = current_context_id();
+        return cudaSuccess;
+    }
+};
 
 // Timing hook: record the start (before=true) or stop event around a
 // dominant kernel launch when gqa_timing_enable(1) is in effect.
