@@ -11,12 +11,13 @@
 // part of this library: the rows arrive ready.
 //
 // Design (HBM-bound; each element is read once as f32 and written once as
-// 16 bits, for K and for V): one thread moves one 8-element chunk of one
-// (token, KV head) row of both K and V -- two 32-byte reads and two 16-byte
-// stores.  Consecutive threads take consecutive chunks of a row, then the
-// next KV head, then the next token, so the reads are fully coalesced and each
-// row's stores fill whole sectors.  A token's sequence is the last s with
-// token_offsets[s] <= i (binary search; the offsets stay in L1).
+// 16 bits, for K and for V): one warp per new token.  The lanes take
+// consecutive 8-element chunks of the token's row (all KV heads), up to four
+// each per round with every load issued before the token's slot is looked up,
+// so that the lookup's chain of dependent reads (the token's sequence by binary
+// search over token_offsets, its start position, its page) is paid once per
+// token while its data are in flight.  Reads are coalesced 32-byte pieces;
+// each chunk's K and V go out as one 16-byte store each.
 #include "common.cuh"
 #include "launch.h"
 
@@ -32,47 +33,78 @@ struct AppendArgs {
     int32_t *status;
 };
 
+constexpr int kChunksPerLane = 4;  // chunks a lane moves per round, loads all in flight
+
 template <class KV>
 __global__ void __launch_bounds__(256) page_append_kernel(const AppendArgs a) {
-    const int64_t row_chunks = (int64_t)a.n_kv_heads * a.chunks;
-    const int64_t work = (int64_t)a.total_tokens * row_chunks;
+    const int lane = threadIdx.x & 31;
+    const int warps_per_block = blockDim.x >> 5;
+    const int row_chunks = a.n_kv_heads * a.chunks;  // 8-element chunks of a token's row
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         const int o0 = a.tok_off[0], on = a.tok_off[a.num_seqs];
         if (o0 < 0 || on > a.total_tokens || o0 > on) raise_flag(a.status, GQA_FLAG_CONTEXT_CLAMPED);
     }
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < work; t += stride) {
-        const int i = (int)(t / row_chunks);
-        const int rem = (int)(t - (int64_t)i * row_chunks);
-        const int g = rem / a.chunks, ch = rem - g * a.chunks;
-        // the row's data first: its loads are in flight while the slot is looked up
-        const int64_t src = ((int64_t)i * a.n_kv_heads + g) * (a.chunks * 8) + ch * 8;
-        const float4 k0 = ld_nc_f4(a.k_new + src), k1 = ld_nc_f4(a.k_new + src + 4);
-        const float4 v0 = ld_nc_f4(a.v_new + src), v1 = ld_nc_f4(a.v_new + src + 4);
-        int lo = 0, hi = a.num_seqs - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (a.tok_off[mid] <= i)
-                lo = mid;
-            else
-                hi = mid - 1;
+    for (int i = blockIdx.x * warps_per_block + (threadIdx.x >> 5); i < a.total_tokens;
+         i += gridDim.x * warps_per_block) {
+        const float *ksrc = a.k_new + (int64_t)i * row_chunks * 8;
+        const float *vsrc = a.v_new + (int64_t)i * row_chunks * 8;
+        bool looked_up = false, skip = false;
+        int64_t slot_base = 0;  // the token's slot in its page, head 0, column 0
+        for (int c0 = 0; c0 < row_chunks; c0 += 32 * kChunksPerLane) {
+            float4 k0[kChunksPerLane], k1[kChunksPerLane], v0[kChunksPerLane], v1[kChunksPerLane];
+#pragma unroll
+            for (int u = 0; u < kChunksPerLane; ++u) {
+                const int c = c0 + lane + 32 * u;
+                if (c < row_chunks) {
+                    k0[u] = ld_nc_f4(ksrc + c * 8);
+                    k1[u] = ld_nc_f4(ksrc + c * 8 + 4);
+                    v0[u] = ld_nc_f4(vsrc + c * 8);
+                    v1[u] = ld_nc_f4(vsrc + c * 8 + 4);
+                }
+            }
+            if (!looked_up) {
+                looked_up = true;
+                // the last sequence s with token_offsets[s] <= i (every lane reads the same
+                // offsets)
+                int lo = 0, hi = a.num_seqs - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (a.tok_off[mid] <= i)
+                        lo = mid;
+                    else
+                        hi = mid - 1;
+                }
+                const int o0 = a.tok_off[lo];
+                if (i < o0 || i >= a.tok_off[lo + 1]) {
+                    skip = true;  // the token belongs to no sequence
+                } else {
+                    const int64_t p = (int64_t)a.pos_start[lo] + (i - o0);
+                    const int64_t pi = p >= 0 ? p / a.page_size : -1;
+                    const int page =
+                        (pi >= 0 && pi < a.max_pages) ? a.page_table[(int64_t)lo * a.max_pages + pi] : -1;
+                    if (page < 0 || page >= a.num_pages) {
+                        // outside the page table or the pool: not written
+                        if (lane == 0) raise_flag(a.status, GQA_FLAG_PAGE_CLAMPED);
+                        skip = true;
+                    } else {
+                        slot_base = (int64_t)page * a.page_stride + (p - pi * a.page_size) * a.token_stride;
+                    }
+                }
+            }
+            if (skip) break;
+#pragma unroll
+            for (int u = 0; u < kChunksPerLane; ++u) {
+                const int c = c0 + lane + 32 * u;
+                if (c < row_chunks) {
+                    const int g = c / a.chunks, ch = c - g * a.chunks;
+                    const int64_t dst = slot_base + (int64_t)g * a.head_stride + ch * 8;
+                    st_v4(a.k_pool + dst, make_uint4(pack2(KV{}, k0[u].x, k0[u].y), pack2(KV{}, k0[u].z, k0[u].w),
+                                                     pack2(KV{}, k1[u].x, k1[u].y), pack2(KV{}, k1[u].z, k1[u].w)));
+                    st_v4(a.v_pool + dst, make_uint4(pack2(KV{}, v0[u].x, v0[u].y), pack2(KV{}, v0[u].z, v0[u].w),
+                                                     pack2(KV{}, v1[u].x, v1[u].y), pack2(KV{}, v1[u].z, v1[u].w)));
+                }
+            }
         }
-        const int o0 = a.tok_off[lo];
-        if (i < o0 || i >= a.tok_off[lo + 1]) continue;  // the token belongs to no sequence
-        const int64_t p = (int64_t)a.pos_start[lo] + (i - o0);
-        const int64_t pi = p >= 0 ? p / a.page_size : -1;
-        const int page = (pi >= 0 && pi < a.max_pages) ? a.page_table[(int64_t)lo * a.max_pages + pi] : -1;
-        if (page < 0 || page >= a.num_pages) {
-            // outside the page table or the pool: not written
-            if (g == 0 && ch == 0) raise_flag(a.status, GQA_FLAG_PAGE_CLAMPED);
-            continue;
-        }
-        const int64_t dst = (int64_t)page * a.page_stride + (p - pi * a.page_size) * a.token_stride +
-                            (int64_t)g * a.head_stride + ch * 8;
-        st_v4(a.k_pool + dst, make_uint4(pack2(KV{}, k0.x, k0.y), pack2(KV{}, k0.z, k0.w),
-                                         pack2(KV{}, k1.x, k1.y), pack2(KV{}, k1.z, k1.w)));
-        st_v4(a.v_pool + dst, make_uint4(pack2(KV{}, v0.x, v0.y), pack2(KV{}, v0.z, v0.w),
-                                         pack2(KV{}, v1.x, v1.y), pack2(KV{}, v1.z, v1.w)));
     }
 }
 
@@ -99,9 +131,9 @@ cudaError_t launch_paged_append(const PagedAppendProblem &p, cudaStream_t stream
     a.num_pages = p.num_pages;
     a.max_pages = p.max_pages_per_seq;
     a.status = p.status;
-    const int64_t work = (int64_t)p.total_tokens * p.n_kv_heads * a.chunks;
-    int64_t blocks = (work + 255) / 256;
-    const int64_t cap = (int64_t)sm_count() * 8;  // 8 resident blocks of 256 per SM
+    // one warp per token, one wave: 8 resident blocks of 8 warps per SM
+    int64_t blocks = ((int64_t)p.total_tokens + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 8;
     if (blocks > cap) blocks = cap;
     timing_mark(true, stream);
     if (p.kv_dtype == GQA_DTYPE_BF16)

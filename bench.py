@@ -308,6 +308,24 @@ class E2EPipe:
         return e0.elapsed_time(e1) / steps
 
 
+def host_io(torch, step, inputs, outputs):
+    """The same step end to end: every call first copies `inputs` (device tensors) in
+    from pinned host copies made here, then runs `step`, then reads `outputs` back into
+    pinned host memory.  Returns (e2e step, h2d bytes, d2h bytes)."""
+    hin = [t.cpu().pin_memory() for t in inputs]
+    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outputs]
+
+    def e2e_step():
+        for d, h in zip(inputs, hin):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(hout, outputs):
+            h.copy_(d, non_blocking=True)
+
+    nb = lambda t: t.numel() * t.element_size()
+    return e2e_step, sum(nb(t) for t in inputs), sum(nb(t) for t in outputs)
+
+
 def setup_prefill(torch, g, case):
     kind = "bf16" if case.kv_dtype == "bf16" else None
     q, k, v, m = (_dev(torch, case.q), _dev(torch, case.k, kind), _dev(torch, case.v, kind),
@@ -360,6 +378,9 @@ def setup_decode(torch, g, c):
     info = {"bytes": kv + 2 * qo + pages_used * 4 + c.num_seqs * 4,
             "kernel_bytes": kv + qo + pages_used * 4 + c.num_seqs * 4, "kv_bytes": kv,
             "launches": 2}
+    # end to end: the step's queries, page table and context lengths in, O out (the KV
+    # pools are the resident cache, not a per-step input)
+    info["e2e"] = host_io(torch, step, [q, pt, cl], [out])
     return step, info
 
 
@@ -409,8 +430,18 @@ def setup_verify(torch, g, c):
     # fused: the visible history once, the current rows, O
     fby = {"attn": hist * HK * D * 2 * 2 + nb(cq) + nb(ck) + nb(cv) + nb(out),
            "commit": by["commit"]}
+    # end to end: the draft rows (current Q/K/V, the rows to commit) and the lanes'
+    # counters in, O out (the rings are the resident cache)
+    step_in = [cq, ck, cv, nk, nv, lens, pos, cnt]
+
+    def fstep():
+        for f in fused.values():
+            f()
+
     return step, ops, {"bytes": by, "launches": 1 + 1 + 2 + 1, "fused": fused,
-                       "fused_bytes": fby, "fused_launches": 1 + 1 + 1}
+                       "fused_bytes": fby, "fused_launches": 1 + 1 + 1,
+                       "e2e": host_io(torch, step, step_in, [out]),
+                       "fused_e2e": host_io(torch, fstep, step_in, [fused_out])}
 
 
 def setup_chunk(torch, g, c):
@@ -439,7 +470,10 @@ def setup_chunk(torch, g, c):
     # append: f32 rows in, 16-bit rows out, for K and V
     append_bytes = nb(kn) + nb(vn) + (nb(kn) + nb(vn)) // 2
     # append, unit ordering, attention
-    return step, ops, {"flops": c.flops(), "append_bytes": append_bytes, "launches": 3}
+    # end to end: the new tokens' Q, K and V, the offsets, start positions and page table
+    # in, O out (the page pools are the resident cache)
+    return step, ops, {"flops": c.flops(), "append_bytes": append_bytes, "launches": 3,
+                       "e2e": host_io(torch, step, [q, kn, vn, off, ps, pt], [out])}
 
 
 # ---------------------------------------------------------------------------
@@ -714,7 +748,9 @@ def main() -> None:
                 "pipeline": "double-buffered: each step's host-to-device copy overlaps the "
                             "previous step's attention and device-to-host copy",
                 "serial_ms_per_step": e2e_serial},
-        "gpu_launches": info["launches"] * args.steps,
+        # every launch of this library's kernels inside a timed region: the device-timed
+        # steps, the kernel timing replays and the end-to-end steps (serial and pipelined)
+        "gpu_launches": info["launches"] * (args.steps + max(10, args.steps) + 2 * args.steps),
         "clocks": clk.summary(),
     }
     del step, e2e_step
@@ -726,13 +762,18 @@ def main() -> None:
         paths = {}
         # prefill d512 with a 7168-token prefix
         c512 = workloads.prefill_d512_prefix(seed=0)
-        s512, _, i512 = setup_prefill(torch, g, c512)
+        s512, _e512, i512 = setup_prefill(torch, g, c512)
         ms = tm.steps(s512, max(5, args.steps // 2), args.warmup)
         t = tm.max_over_ranks(sum(ms) / len(ms))
         k = tm.kernel_ms(g, s512, 5)
+        e512 = tm.max_over_ranks(sum(tm.steps(_e512, max(5, args.steps // 2), args.warmup, graph=False))
+                                 / max(5, args.steps // 2))
         paths["prefill_d512_prefix"] = {
             "workload": c512.name, "value": world * i512["flops"] / (t * 1e-3) / 1e12,
             "unit": "TFLOP/s", "ms_per_step": t,
+            "e2e": {"value": world * i512["flops"] / (e512 * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "ms_per_step": e512, "h2d_bytes_per_step": i512["h2d"],
+                    "d2h_bytes_per_step": i512["d2h"], "pipeline": "serial: one step at a time"},
             "roofline": {"bound": "tensor", "kernel": "attn_kernel<512,f16>",
                          "achieved": i512["flops"] / (k * 1e-3) / 1e12, "peak": tensor_peak,
                          "unit": "TFLOP/s", "frac": i512["flops"] / (k * 1e-3) / 1e12 / tensor_peak,
@@ -740,7 +781,7 @@ def main() -> None:
                          "note": "two output halves recompute Q.K^T: executed FLOPs are 1.5x"}}
         if cpu:
             paths["prefill_d512_prefix"]["cpu_baseline"] = cpu_prefill(c512)
-        del s512
+        del s512, _e512
         torch.cuda.empty_cache()
         # paged decode
         dc = workloads.paged_decode(seed=0)
@@ -748,16 +789,22 @@ def main() -> None:
         ms = tm.steps(sd, max(5, args.steps // 2), args.warmup)
         t = tm.max_over_ranks(sum(ms) / len(ms))
         k = tm.kernel_ms(g, sd, 5)
+        e2e_fn, hi, ho = idc["e2e"]
+        ed = tm.max_over_ranks(sum(tm.steps(e2e_fn, max(5, args.steps // 2), args.warmup, graph=False))
+                               / max(5, args.steps // 2))
         paths["paged_decode"] = {
             "workload": dc.name, "value": world * idc["bytes"] / (t * 1e-3) / 1e9, "unit": "GB/s",
             "kv_bytes_per_step": idc["kv_bytes"], "ms_per_step": t,
+            "e2e": {"value": world * idc["bytes"] / (ed * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ed,
+                    "h2d_bytes_per_step": hi, "d2h_bytes_per_step": ho,
+                    "pipeline": "serial: one step at a time; the KV pools are the resident cache"},
             "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel<f16,128>",
                          "achieved": idc["kernel_bytes"] / (k * 1e-3) / 1e9, "peak": hbm_peak,
                          "unit": "GB/s", "frac": idc["kernel_bytes"] / (k * 1e-3) / 1e9 / hbm_peak,
                          "kernel_ms": k, "traffic": traffic_for("paged_decode_kernel<f16,128>", dc.name)}}
         if cpu:
             paths["paged_decode"]["cpu_baseline"] = cpu_decode(dc)
-        del sd, dc
+        del sd, dc, e2e_fn, idc
         torch.cuda.empty_cache()
         # speculative verify chain
         vc = workloads.verify_full(seed=0)
@@ -771,10 +818,18 @@ def main() -> None:
             kernels[name] = {"bytes": iv["bytes"][name], "kernel_ms": k,
                              "achieved_gbs": iv["bytes"][name] / (k * 1e-3) / 1e9,
                              "frac": iv["bytes"][name] / (k * 1e-3) / 1e9 / hbm_peak}
+        e2e_fn, hi, ho = iv["e2e"]
+        ev_ = tm.max_over_ranks(sum(tm.steps(e2e_fn, max(5, args.steps // 2), args.warmup, graph=False))
+                                / max(5, args.steps // 2))
         paths["verify_chain"] = {"workload": vc.name, "value": world * total / (t * 1e-3) / 1e9,
                                  "unit": "GB/s", "ms_per_step": t, "bytes_per_step": total,
                                  "peak": hbm_peak, "frac": total / (t * 1e-3) / 1e9 / hbm_peak,
-                                 "kernels": kernels}
+                                 "kernels": kernels,
+                                 "e2e": {"value": world * total / (ev_ * 1e-3) / 1e9, "unit": "GB/s",
+                                         "ms_per_step": ev_, "h2d_bytes_per_step": hi,
+                                         "d2h_bytes_per_step": ho,
+                                         "pipeline": "serial: one step at a time; the rings are the "
+                                                     "resident cache"}}
         # the same verify step with the fused ring-direct attention (no pack, no mask)
         fops, fby = iv["fused"], iv["fused_bytes"]
 
@@ -791,14 +846,23 @@ def main() -> None:
                               "achieved_gbs": fby[name] / (k * 1e-3) / 1e9,
                               "frac": fby[name] / (k * 1e-3) / 1e9 / hbm_peak}
         fkernels["attn"]["traffic"] = traffic_for("attn_kernel<256,bf16,ring>", vc.name)
+        e2e_fn, hi, ho = iv["fused_e2e"]
+        ef = tm.max_over_ranks(sum(tm.steps(e2e_fn, max(5, args.steps // 2), args.warmup, graph=False))
+                               / max(5, args.steps // 2))
         paths["verify_fused"] = {"workload": vc.name, "value": world * ftotal / (t * 1e-3) / 1e9,
                                  "unit": "GB/s", "ms_per_step": t, "bytes_per_step": ftotal,
                                  "peak": hbm_peak, "frac": ftotal / (t * 1e-3) / 1e9 / hbm_peak,
-                                 "kernels": fkernels}
+                                 "kernels": fkernels,
+                                 "e2e": {"value": world * ftotal / (ef * 1e-3) / 1e9, "unit": "GB/s",
+                                         "ms_per_step": ef, "h2d_bytes_per_step": hi,
+                                         "d2h_bytes_per_step": ho,
+                                         "pipeline": "serial: one step at a time; the rings are the "
+                                                     "resident cache"}}
         if cpu:
             paths["verify_chain"]["cpu_baseline"], paths["verify_fused"]["cpu_baseline"] = \
                 cpu_verify(vc, total, ftotal)
-        del sv, ops, fops, fstep, vc
+        verify_launches, fused_launches = iv["launches"], iv["fused_launches"]
+        del sv, ops, fops, fstep, vc, iv, e2e_fn
         torch.cuda.empty_cache()
         # chunked prefill over pages: page append + attention
         cc = workloads.paged_chunk_full(seed=0)
@@ -807,9 +871,16 @@ def main() -> None:
         t = tm.max_over_ranks(sum(ms) / len(ms))
         ka = tm.kernel_ms(g, cops["append"], 5)
         kt = tm.kernel_ms(g, cops["attn"], 5)
+        e2e_fn, hi, ho = ic["e2e"]
+        ec = tm.max_over_ranks(sum(tm.steps(e2e_fn, max(5, args.steps // 2), args.warmup, graph=False))
+                               / max(5, args.steps // 2))
         paths["paged_chunk_prefill"] = {
             "workload": cc.name, "value": world * ic["flops"] / (t * 1e-3) / 1e12,
             "unit": "TFLOP/s", "ms_per_step": t, "flops_per_step": ic["flops"],
+            "e2e": {"value": world * ic["flops"] / (ec * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ec,
+                    "h2d_bytes_per_step": hi, "d2h_bytes_per_step": ho,
+                    "pipeline": "serial: one step at a time (append and attention); the page pools "
+                                "are the resident cache"},
             "roofline": {"bound": "tensor", "kernel": "attn_kernel<256,f16,paged>",
                          "achieved": ic["flops"] / (kt * 1e-3) / 1e12, "peak": tensor_peak,
                          "unit": "TFLOP/s", "frac": ic["flops"] / (kt * 1e-3) / 1e12 / tensor_peak,
@@ -820,11 +891,15 @@ def main() -> None:
                        "frac": ic["append_bytes"] / (ka * 1e-3) / 1e9 / hbm_peak}}
         if cpu:
             paths["paged_chunk_prefill"]["cpu_baseline"] = cpu_chunk(cc)
-        del sc, cops, cc
+        chunk_launches = ic["launches"]
+        del sc, cops, cc, ic, e2e_fn
         torch.cuda.empty_cache()
         line["paths"] = paths
-        line["gpu_launches"] += ((2 + 2 + iv["launches"] + iv["fused_launches"] + ic["launches"])
-                                 * max(5, args.steps // 2))
+        # per path: device-timed steps and end-to-end steps (n each), and the kernel timing
+        # replays (5 per timed kernel)
+        n = max(5, args.steps // 2)
+        line["gpu_launches"] += (2 * (2 * n + 5) + 2 * (2 * n + 5) + verify_launches * 2 * n + 5 * 4
+                                 + fused_launches * 2 * n + 5 * 2 + chunk_launches * 2 * n + 5 * 2)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(head)
