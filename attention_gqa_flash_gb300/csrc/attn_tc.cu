@@ -114,7 +114,8 @@ struct Layout {
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kNumVis = kAbort + 4;     // visible tiles of the unit in each list buffer
     static constexpr int kUid = kNumVis + 8;       // the unit in each list buffer (-1: queue ended)
-    static constexpr int kXchg = kUid + 8;         // row-max exchange: [2 tiles][2 halves][128] f32
+    static constexpr int kQpos = kUid + 8;         // its queue position (ring-direct verify)
+    static constexpr int kXchg = kQpos + 8;        // row-max exchange: [2 tiles][2 halves][128] f32
     static constexpr int kList = kXchg + 2 * 2 * BM * 4;  // two lists of visible key tiles (uint16)
     static constexpr int kEnd = kList + 2 * 2 * kMaxListTiles;
     static constexpr int kBytes = kEnd;
@@ -232,13 +233,15 @@ __device__ __forceinline__ int circ_overlap(int a, int b, int start, int len, in
 // is visible to draft row r when j < L and r + j + 1 < w: the slots seen by row 0
 // are the L' = min(L, w - 1) newest, those seen by every row the min(L, w - rows)
 // newest, each a circular range ending at slot wp - 1.
+// (0 <= L <= w and 0 <= wp < w, so a range's first slot wp - len is above -w.)
 __device__ __forceinline__ int ring_tile_code(const AttnArgs &a, int t, int L, int wp) {
     if (t == 0) return 2;  // current rows, then padding
     const int w = a.ring_w, s0 = (t - 1) * BN, s1 = min(s0 + BN, w);
     const int l_any = min(L, w - 1), l_all = max(0, min(L, w - a.ring_r));
-    const int any = circ_overlap(s0, s1, ((wp - l_any) % w + w) % w, l_any, w);
+    auto first = [&](int len) { return wp - len + (wp < len ? w : 0); };
+    const int any = circ_overlap(s0, s1, first(l_any), l_any, w);
     if (any == 0) return 0;
-    const int all = circ_overlap(s0, s1, ((wp - l_all) % w + w) % w, l_all, w);
+    const int all = circ_overlap(s0, s1, first(l_all), l_all, w);
     return all == BN ? 1 : 2;
 }
 
@@ -490,8 +493,6 @@ __device__ __forceinline__ int unit_in_group(const AttnArgs &a, int g, int j) {
 //     the same time, sharing those bytes through L2); groups go in decreasing order
 //     of their mean unit cost (counting sort), so that the queue ends with the light
 //     ones.  Dynamic shared memory: one int per group.
-//   CTA 0, ring-direct verify: one warp works out each lane's split count and the
-//     start of its block of units in the queue.
 //   CTAs 1.., ring-direct verify: the current K and V rows rounded to bf16 for the
 //     tensor map of key tile 0.
 __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int units) {
@@ -522,45 +523,7 @@ __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int
         }
         return;
     }
-    if (a.lane_start) {
-        // ring-direct verify (at most 32 lanes): one warp works out each lane's split
-        // count and where its block of units starts in the queue
-        if (warp != 0) return;
-        int vis = 0;
-        if (lane < a.lanes) {
-            const int L = (int)min(a.ring_len[lane], (uint32_t)a.ring_w);
-            const int wp = (int)(a.ring_wp[lane] % (uint32_t)a.ring_w);
-            for (int j = 0; j < a.n_blk; ++j) vis += ring_tile_code(a, j, L, wp) != 0;
-        }
-        int total = vis;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-        int S = 0, cost = -1;
-        if (lane < a.lanes) {
-            S = (int)((int64_t)vis * a.split_budget / max(total, 1));
-            S = min(max(S, 1), min(a.splits, max(vis, 1)));
-            cost = (vis + S - 1) / S;
-        }
-        const int cnt = lane < a.lanes ? S * a.n_kv_heads * a.head_tiles : 0;
-        // this lane's block follows the blocks of the lanes with dearer units
-        int start = 0;
-        for (int l = 0; l < 32; ++l) {
-            const int cl = __shfl_sync(0xffffffffu, cost, l), nl = __shfl_sync(0xffffffffu, cnt, l);
-            if (cl > cost || (cl == cost && l < lane)) start += nl;
-        }
-        int sum = cnt;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane < a.lanes) {
-            a.lane_splits[lane] = S;
-            a.lane_start[lane] = start;
-        }
-        if (lane == 0) {
-            *a.queue_len = sum;
-            *a.sched_counter = 0;
-        }
-        return;
-    }
+    if (a.lane_start) return;  // ring-direct verify: the attention kernel works out its plan
     if (!a.sched_perm) return;
     const int groups = a.lanes * a.n_kv_heads, per_group = units / groups;
     bins[t] = 0;
@@ -667,6 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlot);
     volatile int *n_vis_smem = reinterpret_cast<volatile int *>(smem + L::kNumVis);
     volatile int *uid_smem = reinterpret_cast<volatile int *>(smem + L::kUid);
+    volatile int *qpos_smem = reinterpret_cast<volatile int *>(smem + L::kQpos);
     float *xchg = reinterpret_cast<float *>(smem + L::kXchg);
     uint16_t *lists = reinterpret_cast<uint16_t *>(smem + L::kList);
     const Waiter wt{abort_flag, a.status, kWaitLimitNs};
@@ -768,28 +732,117 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 a.q_rows_dim1 ? u0.q_head0 : u0.t0 + u0.q_row0);
                 }
             }
-            // the pre-pass (tile classes, or the unit queue and the current rows) is
-            // complete and visible from here on
-            tc::griddep_wait();
-            const int qlen = a.queue_len ? *a.queue_len : units;
+            // ring-direct verify with a split plan: only key tile 0 (the current rows, which
+            // the pre-pass rounds to bf16) depends on the pre-pass; the plan is worked out
+            // here and everything else is loaded without waiting for it
+            const bool ring_plan = RING && a.lane_start;
+            bool prepass_done = !ring_plan;
+            // the pre-pass (tile classes, or the unit queue) is complete and visible from
+            // here on
+            if (!ring_plan) tc::griddep_wait();
+            int qlen = a.queue_len ? *a.queue_len : units;
             // ring-direct verify: every lane's history length, write position, split count
-            // and queue block read once, lane l holding lane l's (at most 32 lanes this way)
+            // and queue block, lane l holding lane l's (at most 32 lanes this way)
             uint32_t my_rl = 0, my_rp = 0;
             int my_ls = a.splits, my_start = 0;
             if (RING && a.lanes <= 32 && lane < a.lanes) {
                 my_rl = a.ring_len[lane];
                 my_rp = a.ring_wp[lane];
-                if (a.lane_splits) {
-                    my_ls = a.lane_splits[lane];
-                    my_start = a.lane_start[lane];
+            }
+            if (ring_plan) {
+                // Lane l gets S_l = ceil(vis_l / C) of the split slots, C the least cost (key
+                // tiles per unit) for which they add up to at most split_budget (no lane
+                // takes more than `splits`); its block of units (kv head major, head tile,
+                // split) follows the blocks of the lanes with dearer units.
+                // visible tiles of lane l (on lane l): key tile 0, and the ring tiles that
+                // meet the circular range of its min(L, w - 1) newest slots (the range
+                // ring_tile_code tests), counted in closed form
+                int vis = 0;
+                if (lane < a.lanes) {
+                    const int w = a.ring_w;
+                    const int la = min((int)min(my_rl, (uint32_t)w), w - 1);
+                    const int wp = (int)(my_rp % (uint32_t)w);
+                    vis = 1;
+                    if (la > 0) {
+                        int st = wp - la;
+                        if (st >= 0) {
+                            vis += (wp - 1) / BN - st / BN + 1;
+                        } else {
+                            st += w;
+                            vis += (w + BN - 1) / BN - st / BN;  // slots [st, w)
+                            if (wp > 0) vis += (wp - 1) / BN + 1 - ((wp - 1) / BN == st / BN ? 1 : 0);
+                        }
+                    }
+                }
+                auto warp_max = [](int v) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+                    return v;
+                };
+                // split slots the lanes take at cost C: the sum of ceil(vis_l / C)
+                auto need = [&](int C) {
+                    int t = 0;
+                    for (int l = 0; l < a.lanes; ++l) {
+                        const int v = __shfl_sync(0xffffffffu, vis, l);
+                        t += (v + C - 1) / C;
+                    }
+                    return t;
+                };
+                // the least feasible C in [lo, hi] (need is non-increasing in C; hi when
+                // none is), 32 candidates per pass
+                int lo = max(warp_max((vis + a.splits - 1) / a.splits), 1), hi = max(warp_max(vis), lo);
+                while (lo < hi) {
+                    const int step = (hi - lo + 31) / 32;
+                    const unsigned fit = __ballot_sync(0xffffffffu, need(min(lo + lane * step, hi)) <= a.split_budget);
+                    if (!fit) {
+                        lo = min(lo + 31 * step + 1, hi);  // none of the candidates fits
+                        continue;
+                    }
+                    const int f = __ffs(fit) - 1;
+                    const int cf = min(lo + f * step, hi);
+                    if (step == 1 || f == 0) {
+                        lo = hi = cf;
+                        break;
+                    }
+                    lo = lo + (f - 1) * step + 1;  // C_{f-1} does not fit
+                    hi = cf;
+                }
+                int S = 0, cost = -1;
+                if (lane < a.lanes) {
+                    S = max((vis + lo - 1) / lo, 1);
+                    cost = (vis + S - 1) / S;
+                }
+                const int cnt = lane < a.lanes ? S * a.n_kv_heads * a.head_tiles : 0;
+                int start = 0;
+                for (int l = 0; l < a.lanes; ++l) {
+                    const int cl = __shfl_sync(0xffffffffu, cost, l), nl = __shfl_sync(0xffffffffu, cnt, l);
+                    if (cl > cost || (cl == cost && l < lane)) start += nl;
+                }
+                int sum = cnt;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                my_ls = S;
+                my_start = start;
+                qlen = sum;
+                // the split combine reads the plan after this launch
+                if (blockIdx.x == 0 && lane < a.lanes) {
+                    a.lane_splits[lane] = S;
+                    a.lane_start[lane] = start;
                 }
             }
             for (int k = 0; ok; ++k) {
                 int uid;
+                int qpos = -1;
                 if (a.sched_counter) {
                     int idx = 0;
-                    if (lane == 0) idx = atomicAdd(a.sched_counter, 1);
-                    idx = __shfl_sync(0xffffffffu, idx, 0);
+                    if (ring_plan) {
+                        // the plan gives every CTA its queue positions (about one unit each)
+                        idx = (int)blockIdx.x + k * (int)gridDim.x;
+                    } else {
+                        if (lane == 0) idx = atomicAdd(a.sched_counter, 1);
+                        idx = __shfl_sync(0xffffffffu, idx, 0);
+                    }
+                    qpos = idx;
                     if (RING && a.lane_start) {
                         // the lane whose block holds queue position idx; then its query
                         // tile and split
@@ -821,6 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) {
                         uid_smem[b] = -1;
                         n_vis_smem[b] = 0;
+                        qpos_smem[b] = -1;
                         tc::mbar_arrive(list_full(b));
                     }
                     break;
@@ -855,19 +909,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       : tile_code(a, un.cg, j);
                 };
                 // splits over the visible tiles: this unit keeps visible tiles [lo, hi)
+                // (a unit spans at most kMaxListTiles key tiles: each lane's codes are
+                // worked out once)
+                int codes[kMaxListTiles / 32];
+#pragma unroll
+                for (int q = 0; q < kMaxListTiles / 32; ++q)
+                    codes[q] = un.jb + 32 * q < un.je ? code_of(un.jb + 32 * q + lane) : 0;
                 int lo = 0, hi = 0x7fffffff;
                 if (a.vis_split) {
                     int all = 0;
-                    for (int base = un.jb; base < un.je; base += 32)
-                        all += __popc(__ballot_sync(0xffffffffu, code_of(base + lane) != 0));
+#pragma unroll
+                    for (int q = 0; q < kMaxListTiles / 32; ++q)
+                        all += __popc(__ballot_sync(0xffffffffu, codes[q] != 0));
                     const int S = (RING && a.lane_splits) ? lane_splits_here : a.splits;
                     lo = (int)((int64_t)un.split * all / S);
                     hi = (int)((int64_t)(un.split + 1) * all / S);
                 }
                 int n = 0, seen = 0;
-                for (int base = un.jb; base < un.je; base += 32) {
-                    const int j = base + lane;
-                    const int code = code_of(j);
+#pragma unroll
+                for (int q = 0; q < kMaxListTiles / 32; ++q) {
+                    const int j = un.jb + 32 * q + lane;
+                    const int code = codes[q];
                     const unsigned vis = __ballot_sync(0xffffffffu, code != 0);
                     const int idx = seen + __popc(vis & ((1u << lane) - 1u));
                     const bool keep = code != 0 && idx >= lo && idx < hi;
@@ -878,9 +940,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     n += __popc(kept);
                     seen += __popc(vis);
                 }
+                __syncwarp();
+                if (ring_plan && n > 1 && un.jb == 0 && list[0] == 0x8000) {
+                    // key tile 0 (the current rows) last: its load waits for the pre-pass
+                    __syncwarp();
+                    uint16_t e[kMaxListTiles / 32];
+#pragma unroll
+                    for (int q = 0; q < kMaxListTiles / 32; ++q) {
+                        const int i = lane + 32 * q;
+                        e[q] = i < n ? list[(i + 1) % n] : 0;
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int q = 0; q < kMaxListTiles / 32; ++q) {
+                        const int i = lane + 32 * q;
+                        if (i < n) list[i] = e[q];
+                    }
+                }
                 if (lane == 0) {
                     n_vis_smem[b] = n;
                     uid_smem[b] = uid;
+                    qpos_smem[b] = qpos;
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(list_full(b));
@@ -981,7 +1061,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         fill_paged(dst, is_v, j, d0, checked(page));
                     } else if (RING && j == 0) {
                         // the current rows (bf16, padded with zero rows by the tensor map; K of
-                        // all heads, then V)
+                        // all heads, then V), rounded by the pre-pass
+                        if (!prepass_done) {
+                            if (lane == 0) tc::griddep_wait();
+                            prepass_done = true;
+                        }
                         if (lane == 0) {
                             tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
 #pragma unroll
@@ -1400,10 +1484,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int uid = -1;
         Unit cur{};
         int cur_n = 0, cur_pos = 0;  // visible tiles and first ring position of unit k
+        int cur_qpos = -1;           // its queue position (ring-direct verify)
         if (a.sched_counter || slot_unit(0, slot, slots, units) >= 0) {
             ok = __all_sync(0xffffffffu, wt.wait(list_full(0), 0));
             ok = tc::named_bar_and(1, kSoftmaxThreads, ok);
             uid = ok ? uid_smem[0] : -1;
+            cur_qpos = qpos_smem[0];
             if (uid >= 0) {
                 cur = unit_of(a, uid, PAIR, rank, DO);
                 if constexpr (PAGED) set_span(a, cur, false);
@@ -1611,7 +1697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- the next unit's Q is converted before this unit's epilogue, so that its
             // first Q.K^T products overlap the epilogue (all of unit k's S are complete:
             // nothing reads the Q staging area any more)
-            int nuid = -1;
+            int nuid = -1, nxt_qpos = -1;
             Unit nxt{};
             int nxt_n = 0;
             const int nxt_pos = cur_pos + (cur_n > 0 ? unit_positions(cur_n) : 0);
@@ -1633,6 +1719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = __all_sync(0xffffffffu, wt.wait(list_full((k + 1) & 1), ((k + 1) >> 1) & 1));
                 ok = tc::named_bar_and(1, kSoftmaxThreads, ok);
                 nuid = ok ? uid_smem[(k + 1) & 1] : -1;
+                nxt_qpos = qpos_smem[(k + 1) & 1];
             }
             if (nuid >= 0) {
                 nxt = unit_of(a, nuid, PAIR, rank, DO);
@@ -1726,8 +1813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // contiguous bytes per instruction
                     int64_t unit = ((int64_t)cur.tile_id * a.d_parts + cur.dpart) * a.splits + cur.split;
                     if (a.lane_start)  // ring-direct verify: the unit's queue position
-                        unit = a.lane_start[cur.t.lane] +
-                               (int64_t)((cur.t.kh * a.head_tiles + cur.t.ht) * a.lane_splits[cur.t.lane] + cur.split);
+                        unit = cur_qpos;
                     dst = nullptr;
                     if (valid) {
                         if (h == 0) a.ws_lse[unit * BM + r] = l > 0.f ? m_ref + __log2f(l) : kNegInf;
@@ -1775,6 +1861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             cur = nxt;
             cur_n = nxt_n;
             cur_pos = nxt_pos;
+            cur_qpos = nxt_qpos;
             uid = nuid;
             ++k;
         }
@@ -1820,29 +1907,59 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a, int
     auto slot = [&](int s) -> int64_t {
         return a.lane_start ? a.lane_start[t.lane] + (int64_t)((t.kh * a.head_tiles + t.ht) * S + s) : u0 + s;
     };
-    float M = kNegInf;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, a.ws_lse[slot(s) * BM + r]);
-    float acc[DO / 32];
+    // the splits' log-sum-exps, lane s holding split s0 + s (32 splits per pass)
+    static_assert(DO % 128 == 0, "a lane merges DO / 128 float4 columns");
+    const float lse0 = lane < S ? a.ws_lse[slot(lane) * BM + r] : kNegInf;
+    float M = lse0;
+    for (int s = 32 + lane; s < S; s += 32) M = fmaxf(M, a.ws_lse[slot(s) * BM + r]);
 #pragma unroll
-    for (int k = 0; k < DO / 32; ++k) acc[k] = 0.f;
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    // column chunk q = lane + 32 k (four columns) of row r: the float4 at (unit * DO/4 + q) * BM + r
+    float4 acc[DO / 128];
+#pragma unroll
+    for (int k = 0; k < DO / 128; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = 0.f;
     if (M != kNegInf) {
-        for (int s = 0; s < S; ++s) {
-            const float w = ex2(a.ws_lse[slot(s) * BM + r] - M);
-            L += w;
-            // [unit][DO / 4][BM] float4: column c of row r at ((unit * DO/4 + c/4) * BM + r) * 4 + c % 4
-            const float *src = a.ws_o + (slot(s) * (DO / 4) * BM + r) * 4;
+        for (int s0 = 0; s0 < S; s0 += 32) {
+            const float lse = s0 == 0 ? lse0 : (s0 + lane < S ? a.ws_lse[slot(s0 + lane) * BM + r] : kNegInf);
+            const float wl = s0 + lane < S ? ex2(lse - M) : 0.f;
+            L += wl;
+            const int ns = min(32, S - s0);
+            // every split's loads are independent of the weights: four splits in flight
+#pragma unroll 4
+            for (int i = 0; i < ns; ++i) {
+                const float w = __shfl_sync(0xffffffffu, wl, i);
+                const float4 *src = reinterpret_cast<const float4 *>(a.ws_o) + slot(s0 + i) * (DO / 4) * BM + r;
 #pragma unroll
-            for (int k = 0; k < DO / 32; ++k) {
-                const int c = lane + 32 * k;
-                acc[k] += w * src[(int64_t)(c >> 2) * BM * 4 + (c & 3)];
+                for (int k = 0; k < DO / 128; ++k) {
+                    const float4 x = ld_nc_f4(reinterpret_cast<const float *>(src + (int64_t)(lane + 32 * k) * BM));
+                    acc[k].x += w * x.x;
+                    acc[k].y += w * x.y;
+                    acc[k].z += w * x.z;
+                    acc[k].w += w * x.w;
+                }
             }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     }
     float *out = a.o + t.lane * a.o_lane + (int64_t)head * a.o_head + (int64_t)row * a.o_row +
                  dpart * DO;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const bool vec = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
 #pragma unroll
-    for (int k = 0; k < DO / 32; ++k) out[lane + 32 * k] = L > 0.f ? acc[k] / L : 0.f;
+    for (int k = 0; k < DO / 128; ++k) {
+        const float4 v = make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
+        float *dst = out + 4 * (lane + 32 * k);
+        if (vec) {
+            *reinterpret_cast<float4 *>(dst) = v;
+        } else {
+            dst[0] = v.x;
+            dst[1] = v.y;
+            dst[2] = v.z;
+            dst[3] = v.w;
+        }
+    }
 }
 
 }  // namespace
