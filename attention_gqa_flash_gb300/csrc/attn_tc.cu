@@ -170,10 +170,12 @@ struct AttnArgs {
     int total_tokens, max_pages, page_size, num_pages, pg_box;
     int pg_dim[3];  // logical coordinate (0 kv head, 1 slot, 2 page) of map dimensions 1..3
     // dynamic unit queue (unpaired): units in decreasing cost order; each CTA takes
-    // the next one from the counter when it starts a unit.  Null: the static
-    // snake assignment.
+    // the next one from the counter when it starts a unit.  Null counter: the static
+    // snake assignment, over the order in sched_perm when there is one (chunked
+    // prefill in CTA pairs, whose two CTAs must agree on every unit)
     const int *sched_perm;
     int *sched_counter;
+    int pair;  // units are CTA-pair units (for the ordering pass)
     // key splits over the visible tiles (ring-direct verify): every split of a tile
     // scans all key tiles and takes the split-th of `splits` equal shares of the
     // visible ones, instead of a fixed range of tiles
@@ -461,7 +463,7 @@ __device__ __forceinline__ int paged_tile_code(const AttnArgs &a, const Unit &n,
 constexpr int kCostBins = 1024;
 constexpr int kMaxQueueGroups = 10240;  // (sequence, KV head) groups the ordering pass handles (40 KiB)
 __device__ __forceinline__ int paged_unit_cost(const AttnArgs &a, int u) {
-    Unit un = unit_of(a, u, false, 0, 0);
+    Unit un = unit_of(a, u, a.pair != 0, 0, 0);
     set_span(a, un, false);
     if (un.q_row0 >= un.ntok) return 0;
     const int p1 = un.ps + min(un.q_row0 + a.rows_per_head, un.ntok) - 1;
@@ -470,19 +472,18 @@ __device__ __forceinline__ int paged_unit_cost(const AttnArgs &a, int u) {
 }
 
 // Unit j of group g = (sequence, KV head) in the queue order: row tiles from the
-// last (the most keys), then head tiles, output halves and key splits.  This
-// inverts unit_of's (unpaired) numbering.
+// last (the most keys), then head tiles (pairs of them for CTA-pair units), output
+// halves and key splits.  This inverts unit_of's numbering.
 __device__ __forceinline__ int unit_in_group(const AttnArgs &a, int g, int j) {
     const int split = j % a.splits;
     j /= a.splits;
     const int dpart = j % a.d_parts;
     j /= a.d_parts;
-    const int ht = j % a.head_tiles;
-    const int rt = a.row_tiles - 1 - j / a.head_tiles;
-    const int lane = g / a.n_kv_heads, kh = g - lane * a.n_kv_heads;
-    const int per_rt = a.lanes * a.n_kv_heads * a.head_tiles;
-    const int tile_id = ((rt * a.lanes + lane) * a.n_kv_heads + kh) * a.head_tiles + ht;
-    const int ut = (a.row_tiles - 1 - rt) * per_rt + tile_id % per_rt;
+    const int hts = a.pair ? a.head_tiles / 2 : a.head_tiles;
+    const int ht = j % hts;
+    const int rt = a.row_tiles - 1 - j / hts;
+    const int per_rt = a.lanes * a.n_kv_heads * hts;
+    const int ut = (a.row_tiles - 1 - rt) * per_rt + g * hts + ht;
     return (ut * a.d_parts + dpart) * a.splits + split;
 }
 
@@ -530,7 +531,7 @@ __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int
     for (int g = t; g < groups; g += 1024) gval[g] = 0;
     __syncthreads();
     for (int u = t; u < units; u += 1024) {
-        const Unit un = unit_of(a, u, false, 0, 0);
+        const Unit un = unit_of(a, u, a.pair != 0, 0, 0);
         atomicAdd(&gval[un.t.lane * a.n_kv_heads + un.t.kh], paged_unit_cost(a, u));
     }
     __syncthreads();
@@ -571,7 +572,7 @@ __global__ void __launch_bounds__(1024) order_units_kernel(const AttnArgs a, int
         const int g = i / per_group, j = i - g * per_group;
         perm[gval[g] * per_group + j] = unit_in_group(a, g, j);
     }
-    if (t == 0) *a.sched_counter = 0;
+    if (t == 0 && a.sched_counter) *a.sched_counter = 0;
 }
 
 // The k-th unit of work slot `slot` of `slots` (a slot is a CTA, or a CTA pair):
@@ -599,7 +600,7 @@ template <int D, class KV, bool PAIR, int MODE = kMaskMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq,
-                const __grid_constant__ CUtensorMap tmo) {
+                const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmv1) {
     using C = Cfg<D>;
     using L = Layout<D>;
     constexpr int DO = C::DO, KSUB = C::KSUB, VSUB = C::VSUB, NS = C::STAGES;
@@ -607,7 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kQStages = D / 64;  // an f32 Q tile crosses the ring 64 columns per stage
     static_assert(!PAIR || D >= 256, "CTA pairs stage Q in shared memory (head_dim >= 256)");
     constexpr bool RING = MODE == kRingMode, PAGED = MODE == kPagedMode;
-    static_assert(!(PAIR && MODE != kMaskMode), "ring-direct verify and chunked prefill run unpaired");
+    static_assert(!(PAIR && MODE == kRingMode), "ring-direct verify runs unpaired");
+    static_assert(!(PAIR && MODE == kPagedMode && D != 256), "chunked prefill pairs at head_dim 256");
     // ring stages per K and per V tile (PAIR: one stage holds this CTA's 64 keys x
     // 256 columns of K, or its 128 keys x 128 output columns of V)
     constexpr int KST = PAIR ? D / 256 : KSUB;
@@ -719,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             // while the pre-pass runs: the first unit's f32 Q into L2 (its rows and heads do
             // not depend on the pre-pass when the units are assigned statically)
-            if (!a.sched_counter && a.q_tma && lane == 0 && !RING) {
+            if (!a.sched_counter && !a.sched_perm && a.q_tma && lane == 0 && !RING) {
                 const int uid0 = slot_unit(0, slot, slots, units);
                 if (uid0 >= 0) {
                     Unit u0 = unit_of(a, uid0, PAIR, rank, DO);
@@ -863,6 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     uid = slot_unit(k, slot, slots, units);
                     if (uid < 0) break;
+                    if (a.sched_perm) uid = a.sched_perm[uid];
                 }
                 const int b = k & 1;
                 uint16_t *list = lists + b * kMaxListTiles;
@@ -1091,8 +1094,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // full barrier (which expects both halves): K = keys [64 rank, +64) of the
                 // tile, columns [d0, d0 + 256); V = all 128 keys, output columns
                 // [d_off + 128 rank, +128)
-                auto load_half = [&](int j, bool is_v, int d0) -> bool {
+                auto load_half = [&](int j, bool is_v, int d0, int page = 0) -> bool {
                     if (!slot_free()) return false;
+                    if constexpr (PAGED) {
+                        // chunked prefill: lane b issues box b of the tile (pg_box keys of one
+                        // page) if it falls in this CTA's half.  Every stage carries its whole
+                        // bytes, as the even CTA's barrier expects: a box past the context end
+                        // ctx reads the zero fill of an out-of-range page, and the V box holding
+                        // ctx goes one row at a time, rows past ctx from an out-of-range slot,
+                        // so that V rows past ctx are zero (they meet zero probabilities); K
+                        // rows past ctx inside a box are left as they are (their scores are
+                        // replaced by -inf).
+                        const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
+                        if (lane == 0 && rank == 0) tc::mbar_arrive_expect_tx(full(stage), 2 * kStageBytes);
+                        const uint32_t fb = tc::mapa_shared(full(stage), 0);
+                        const int ctx = un.ps + un.ntok;
+                        const int k_lo = is_v ? 0 : (int)rank * (BN / 2), k_n = is_v ? BN : BN / 2;
+                        const int r0 = lane * a.pg_box - k_lo;  // the box's first row in this CTA's image
+                        if (r0 >= 0 && r0 < k_n) {
+                            const int key0 = j * BN + lane * a.pg_box;
+                            const int slot0 = key0 % a.page_size;
+                            const int pg = key0 < ctx ? checked(page) : a.num_pages;
+                            auto crd = [&](int w, int slot) { return w == 0 ? un.t.kh : (w == 1 ? slot : pg); };
+                            if (!is_v) {
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    tc::tma_load_4d_pair(dst + c * (BN / 2 * 128) + r0 * 128, &tmk, fb, d0 + c * 64,
+                                                         crd(a.pg_dim[0], slot0), crd(a.pg_dim[1], slot0),
+                                                         crd(a.pg_dim[2], slot0));
+                            } else if (key0 + a.pg_box <= ctx || key0 >= ctx) {
+#pragma unroll
+                                for (int c = 0; c < 2; ++c)
+                                    tc::tma_load_4d_pair(dst + c * (BN * 128) + r0 * 128, &tmv, fb,
+                                                         un.d_off + (int)rank * 128 + c * 64,
+                                                         crd(a.pg_dim[0], slot0), crd(a.pg_dim[1], slot0),
+                                                         crd(a.pg_dim[2], slot0));
+                            } else {
+                                for (int rr = 0; rr < a.pg_box; ++rr) {
+                                    const int slot = key0 + rr < ctx ? slot0 + rr : a.page_size;
+#pragma unroll
+                                    for (int c = 0; c < 2; ++c)
+                                        tc::tma_load_4d_pair(dst + c * (BN * 128) + (r0 + rr) * 128, &tmv1, fb,
+                                                             un.d_off + (int)rank * 128 + c * 64,
+                                                             crd(a.pg_dim[0], slot), crd(a.pg_dim[1], slot),
+                                                             crd(a.pg_dim[2], slot));
+                                }
+                            }
+                        }
+                        next();
+                        return true;
+                    }
                     if (lane == 0) {
                         const uint32_t dst = sbase + L::kStages + stage * kStageBytes;
                         if (rank == 0) tc::mbar_arrive_expect_tx(full(stage), 2 * kStageBytes);
@@ -1118,11 +1169,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 // the MMA issuer consumes K of tile v+1 before V of tile v: K0, K1, V0, K2, V1, ...
                 if constexpr (PAIR) {
-                    for (int ks = 0; ks < KST && ok && n > 0; ++ks) ok = load_half(tile_at(0), false, ks * 256);
+                    // (chunked prefill: the pages of tiles v and v + 1)
+                    int pg_v = PAGED && n > 0 ? box_page(tile_at(0)) : 0;
+                    int pg_n = PAGED && n > 1 ? box_page(tile_at(1)) : 0;
+                    for (int ks = 0; ks < KST && ok && n > 0; ++ks) ok = load_half(tile_at(0), false, ks * 256, pg_v);
                     for (int v = 0; ok && v < n; ++v) {
+                        const int pg_nn = PAGED && v + 2 < n ? box_page(tile_at(v + 2)) : 0;
                         for (int ks = 0; ks < KST && ok && v + 1 < n; ++ks)
-                            ok = load_half(tile_at(v + 1), false, ks * 256);
-                        if (ok) ok = load_half(tile_at(v), true, 0);
+                            ok = load_half(tile_at(v + 1), false, ks * 256, pg_n);
+                        if (ok) ok = load_half(tile_at(v), true, 0, pg_v);
+                        pg_v = pg_n;
+                        pg_n = pg_nn;
                     }
                 } else {
                     // pages of tiles v and v + 1 (chunked prefill)
@@ -1991,14 +2048,16 @@ int g_pair_mode = 1;
 // CTA pairs need two query tiles that see the same key tiles: one head each,
 // 128 rows each, the same rows, a mask shared by all heads, an even number of
 // head tiles per KV group, and Q staged in shared memory (head_dim >= 256).
-bool pairable(int rows, int n_heads, int n_kv_heads, int head_dim, bool shared_mask) {
+// (same_keys: the heads' rows see the same keys without a shared mask, as in a
+// chunked prefill, where visibility follows the token positions alone)
+bool pairable(int rows, int n_heads, int n_kv_heads, int head_dim, bool shared_mask, bool same_keys) {
     const int group = n_heads / n_kv_heads;
     if (g_pair_mode == 0 || (g_pair_mode == 1 && head_dim < 256)) return false;
-    return shared_mask && head_dim >= 256 && rows >= BM && group % 2 == 0;
+    return (shared_mask || same_keys) && head_dim >= 256 && rows >= BM && group % 2 == 0;
 }
 
 Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, int n_keys,
-               bool shared_mask, bool ring = false) {
+               bool shared_mask, bool ring = false, bool same_keys = false) {
     const bool vis_split = ring;
     Plan p{};
     p.bn = BN;
@@ -2016,7 +2075,7 @@ Plan make_plan(int lanes, int rows, int n_heads, int n_kv_heads, int head_dim, i
     p.shared_mask = shared_mask;
     p.code_groups = shared_mask ? lanes * p.row_tiles : p.tiles;
     p.pair = p.heads_per_tile == 1 && p.rows_per_head == BM &&
-             pairable(rows, n_heads, n_kv_heads, head_dim, shared_mask);
+             pairable(rows, n_heads, n_kv_heads, head_dim, shared_mask, same_keys);
     // a pair occupies two SMs
     const int units = p.tiles * p.d_parts / (p.pair ? 2 : 1);
     int sms = sm_count();
@@ -2186,7 +2245,7 @@ cudaError_t run_attn(const AttnArgs &a, const CUtensorMap *maps, int units, int 
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = PAIR ? 2 : 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, maps[0], maps[1], maps[2], maps[3]);
+        cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, maps[0], maps[1], maps[2], maps[3], maps[4]);
         if (e != cudaSuccess) return e;
     }
     timing_mark(false, stream);
@@ -2235,8 +2294,15 @@ size_t verify_ring_workspace_bytes(const gqa_ring_params &p) {
 // max_pages_per_seq * page_size; no mask classification, never paired.
 static Plan paged_plan(int num_seqs, int max_tokens, int n_heads, int n_kv_heads, int head_dim,
                        int max_pages_per_seq, int page_size) {
+    // CTA pairs (head_dim 256) halve the page boxes each SM copies per tile; they run
+    // without key splits
+    // (a CTA's half of a K tile, 64 keys, must hold whole page boxes: gcd(page, 128) <= 64)
     Plan pl = make_plan(num_seqs, max_tokens, n_heads, n_kv_heads, head_dim,
-                        max_pages_per_seq * page_size, false);
+                        max_pages_per_seq * page_size, false, false,
+                        head_dim == 256 && std::gcd(page_size, BN) <= BN / 2);
+    if (pl.pair && pl.splits > 1)
+        pl = make_plan(num_seqs, max_tokens, n_heads, n_kv_heads, head_dim, max_pages_per_seq * page_size,
+                       false);
     pl.codes_bytes = 0;
     // units differ in cost with each sequence's prefix: a cost-ordered dynamic queue
     pl.sched_bytes = 256 + align256((size_t)pl.tiles * pl.d_parts * pl.splits * 4);
@@ -2299,7 +2365,7 @@ cudaError_t launch_paged_prefill(const PagedPrefillProblem &p, void *workspace, 
     a.num_pages = p.num_pages;
     a.pg_box = std::gcd(p.page_size, BN);  // >= 8: the page size is a multiple of 8
 
-    CUtensorMap maps[4];
+    CUtensorMap maps[5];
     memset(maps, 0, sizeof maps);
     const CUtensorMapDataType kvt =
         a.kv_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -2310,6 +2376,11 @@ cudaError_t launch_paged_prefill(const PagedPrefillProblem &p, void *workspace, 
                         p.head_stride, p.token_stride, p.page_stride, a.pg_box, dim_v))
         return cudaErrorInvalidValue;
     for (int i = 0; i < 3; ++i) a.pg_dim[i] = dim_k[i];
+    // CTA pairs: V pages one row high, for the box that holds a sequence's context end
+    if (pl.pair && !make_paged_map(&maps[4], p.v_pool, kvt, p.head_dim, p.n_kv_heads, p.page_size,
+                                   p.num_pages, p.head_stride, p.token_stride, p.page_stride, 1, dim_v))
+        return cudaErrorInvalidValue;
+    a.pair = pl.pair ? 1 : 0;
     // f32 Q in by TMA and O out by TMA for one head's 128-token tiles
     if (pl.heads_per_tile == 1 && pl.rows_per_head == BM &&
         make_map(&maps[2], p.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.head_dim, p.total_tokens,
@@ -2323,15 +2394,19 @@ cudaError_t launch_paged_prefill(const PagedPrefillProblem &p, void *workspace, 
             a.o_rows_dim1 = a.q_rows_dim1;
         }
     }
-    const int units = pl.tiles * pl.d_parts * pl.splits;
+    // units: query tiles (CTA pairs: pairs of them) x output halves x key splits
+    const int units = pl.tiles * pl.d_parts * pl.splits / (pl.pair ? 2 : 1);
     int sms = sm_count();
     if (sms <= 0) sms = 148;
-    const int ctas = std::min(units, sms);
+    const int ctas = pl.pair ? 2 * std::min(units, sms / 2) : std::min(units, sms);
     const int groups = p.num_seqs * p.n_kv_heads;
     if (groups <= kMaxQueueGroups) {
         order_units_kernel<<<1, 1024, groups * sizeof(int), stream>>>(a, units);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+        // CTA pairs take the ordered units in the static snake order (both CTAs of a
+        // pair work out the same unit without talking)
+        if (pl.pair) a.sched_counter = nullptr;
     } else {
         a.sched_perm = nullptr;  // too many groups for one CTA's table: static snake order
         a.sched_counter = nullptr;
@@ -2342,6 +2417,9 @@ cudaError_t launch_paged_prefill(const PagedPrefillProblem &p, void *workspace, 
             return bf ? run_attn<128, BF16, false, kPagedMode>(a, maps, ctas, pl.tiles, stream)
                       : run_attn<128, F16, false, kPagedMode>(a, maps, ctas, pl.tiles, stream);
         case 256:
+            if (pl.pair)
+                return bf ? run_attn<256, BF16, true, kPagedMode>(a, maps, ctas, pl.tiles, stream)
+                          : run_attn<256, F16, true, kPagedMode>(a, maps, ctas, pl.tiles, stream);
             return bf ? run_attn<256, BF16, false, kPagedMode>(a, maps, ctas, pl.tiles, stream)
                       : run_attn<256, F16, false, kPagedMode>(a, maps, ctas, pl.tiles, stream);
         default:
@@ -2418,7 +2496,7 @@ cudaError_t launch_attention(const AttnProblem &p, void *workspace, cudaStream_t
     a.status = p.status;
 
     // K, V (and, for single-head 128-row prefill tiles, f32 Q and O) tensor maps
-    CUtensorMap maps[4];
+    CUtensorMap maps[5];
     memset(maps, 0, sizeof maps);
     const int heads = p.lanes * p.n_kv_heads;
     const CUtensorMapDataType kvt =

@@ -91,6 +91,10 @@ CASES = [
     (3, (50, 200), (0, 400), 4, 1, 128, 24, "f16", True),     # 24-slot pages, head-major pool
     (2, (129, 260), (0, 300), 2, 2, 256, 256, "bf16", False), # pages longer than a key tile
     (2, (128, 128), (0, 0), 4, 2, 128, 32, "f16", False),     # no prefix, one whole tile
+    # enough 128-token tiles at head_dim 256 for CTA pairs (no key splits): page boxes
+    # split between the two CTAs, value rows past each context end zeroed row by row
+    (4, (257, 384), (0, 1000), 16, 4, 256, 16, "f16", False),
+    (8, (257, 300), (0, 500), 8, 2, 256, 32, "bf16", True),
 ]
 
 
