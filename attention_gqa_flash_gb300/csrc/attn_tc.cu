@@ -109,13 +109,15 @@ struct Layout {
     static constexpr int kBars = kStages + C::STAGES * kStageBytes;
     // barriers: full[S], empty[S], q_full, s_full[2], p_full[2], o_done[2], mma_fin,
     // list_full[2], list_free[2], o_free
-    static constexpr int kNumBars = 2 * C::STAGES + 13;
+    // (+ peer_full[2], peer_free[2]: the unit hand-over of a CTA pair's dynamic queue)
+    static constexpr int kNumBars = 2 * C::STAGES + 17;
     static constexpr int kTmemSlot = kBars + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 4;
     static constexpr int kNumVis = kAbort + 4;     // visible tiles of the unit in each list buffer
     static constexpr int kUid = kNumVis + 8;       // the unit in each list buffer (-1: queue ended)
     static constexpr int kQpos = kUid + 8;         // its queue position (ring-direct verify)
-    static constexpr int kXchg = kQpos + 8;        // row-max exchange: [2 tiles][2 halves][128] f32
+    static constexpr int kPeerUid = kQpos + 8;     // CTA pair, odd CTA: the units the even CTA drew
+    static constexpr int kXchg = kPeerUid + 8;     // row-max exchange: [2 tiles][2 halves][128] f32
     static constexpr int kList = kXchg + 2 * 2 * BM * 4;  // two lists of visible key tiles (uint16)
     static constexpr int kEnd = kList + 2 * 2 * kMaxListTiles;
     static constexpr int kBytes = kEnd;
@@ -628,6 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto list_full = [&](int b) { return bar(2 * NS + 8 + b); };
     auto list_free = [&](int b) { return bar(2 * NS + 10 + b); };
     const uint32_t o_free = bar(2 * NS + 12);
+    // CTA pair with a dynamic queue: the even CTA draws each unit and hands it to the odd
+    // CTA (peer_full, in the odd CTA), which gives the slot back (peer_free, in the even)
+    auto peer_full = [&](int b) { return bar(2 * NS + 13 + b); };
+    auto peer_free = [&](int b) { return bar(2 * NS + 15 + b); };
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlot);
     volatile int *n_vis_smem = reinterpret_cast<volatile int *>(smem + L::kNumVis);
@@ -675,6 +681,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::mbar_init(mma_fin, 1);
         tc::mbar_init(o_free, kSoftmaxWarps + ((PAIR && rank == 0) ? 1 : 0));
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(peer_full(b), 1);
+            tc::mbar_init(peer_free(b), 1);
+        }
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -840,6 +850,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ring_plan) {
                         // the plan gives every CTA its queue positions (about one unit each)
                         idx = (int)blockIdx.x + k * (int)gridDim.x;
+                    } else if (PAIR) {
+                        // the even CTA draws the unit and hands it to the odd CTA; the hand-over
+                        // slot k & 1 is reused once the odd CTA has read unit k - 2 from it
+                        volatile int *peer_uid = reinterpret_cast<volatile int *>(smem + L::kPeerUid);
+                        const int pb = k & 1;
+                        bool hw = true;
+                        if (lane == 0) {
+                            if (rank == 0) {
+                                if (k >= 2) hw = wt.template wait<true>(peer_free(pb), ((k - 2) >> 1) & 1);
+                                idx = hw ? atomicAdd(a.sched_counter, 1) : 0x7fffffff;
+                                tc::st_shared_cluster_u32(tc::mapa_shared(smem_u32((const void *)(peer_uid + pb)), 1),
+                                                          (uint32_t)idx);
+                                tc::mbar_arrive_cluster(tc::mapa_shared(peer_full(pb), 1));
+                            } else {
+                                hw = wt.template wait<true>(peer_full(pb), (k >> 1) & 1);
+                                idx = hw ? peer_uid[pb] : 0x7fffffff;
+                                tc::mbar_arrive_cluster(tc::mapa_shared(peer_free(pb), 0));  // after the read
+                            }
+                        }
+                        idx = __shfl_sync(0xffffffffu, idx, 0);
                     } else {
                         if (lane == 0) idx = atomicAdd(a.sched_counter, 1);
                         idx = __shfl_sync(0xffffffffu, idx, 0);
@@ -1345,9 +1375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bool ok = true;
                     int g = 0, with_o = 0;
                     for (int k = 0; ok; ++k) {
-                        if (slot_unit(k, slot, slots, units) < 0) break;
+                        if (!a.sched_counter && slot_unit(k, slot, slots, units) < 0) break;
                         const int b = k & 1;
                         if (!(ok = wt.wait(list_full(b), (k >> 1) & 1))) break;
+                        if (uid_smem[b] < 0) break;  // the unit queue has ended
                         const int n = n_vis_smem[b];
                         tc::mbar_arrive(list_free(b));
                         for (int i = 0; ok && i < n; ++i) {
@@ -2404,9 +2435,6 @@ cudaError_t launch_paged_prefill(const PagedPrefillProblem &p, void *workspace, 
         order_units_kernel<<<1, 1024, groups * sizeof(int), stream>>>(a, units);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        // CTA pairs take the ordered units in the static snake order (both CTAs of a
-        // pair work out the same unit without talking)
-        if (pl.pair) a.sched_counter = nullptr;
     } else {
         a.sched_perm = nullptr;  // too many groups for one CTA's table: static snake order
         a.sched_counter = nullptr;

@@ -261,6 +261,10 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
+// 32-bit store to a shared-memory address of a CTA of the cluster
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
 // Arrive without release semantics.  For signals whose data is already
 // complete when the arrive is issued (e.g. tensor-memory stores finished by
 // tcgen05.wait::st before a local barrier the signalling thread waited on):
