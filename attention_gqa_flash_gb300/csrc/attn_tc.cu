@@ -1153,18 +1153,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                          crd(a.pg_dim[0], slot0), crd(a.pg_dim[1], slot0),
                                                          crd(a.pg_dim[2], slot0));
                             } else if (key0 + a.pg_box <= ctx || key0 >= ctx) {
-#pragma unroll
-                                for (int c = 0; c < 2; ++c)
-                                    tc::tma_load_4d_pair(dst + c * (BN * 128) + r0 * 128, &tmv, fb,
-                                                         un.d_off + (int)rank * 128 + c * 64,
-                                                         crd(a.pg_dim[0], slot0), crd(a.pg_dim[1], slot0),
-                                                         crd(a.pg_dim[2], slot0));
+                                // V stage page-major: both 64-column chunks of the page's rows
+                                // in one copy, {64 columns, slots, chunks, kv head, page}
+                                tc::tma_load_5d_pair(dst + r0 * 256, &tmv, fb, 0, slot0,
+                                                     (un.d_off + (int)rank * 128) / 64, un.t.kh, pg);
                             } else {
                                 for (int rr = 0; rr < a.pg_box; ++rr) {
                                     const int slot = key0 + rr < ctx ? slot0 + rr : a.page_size;
 #pragma unroll
                                     for (int c = 0; c < 2; ++c)
-                                        tc::tma_load_4d_pair(dst + c * (BN * 128) + (r0 + rr) * 128, &tmv1, fb,
+                                        tc::tma_load_4d_pair(dst + r0 * 256 + c * a.pg_box * 128 + rr * 128, &tmv1, fb,
                                                              un.d_off + (int)rank * 128 + c * 64,
                                                              crd(a.pg_dim[0], slot), crd(a.pg_dim[1], slot),
                                                              crd(a.pg_dim[2], slot));
@@ -1314,9 +1312,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!(ok = wt.template wait<true>(full(stage), round & 1))) break;
                             tc::tc_fence_after();
                             const uint32_t vb = sbase + L::kStages + stage * kStageBytes;
+                            // (chunked prefill: V stages are page-major, [page][2 column
+                            // chunks][pg_box rows][128 B], so that one copy brings a page's
+                            // rows of both chunks: a 16-key step starts in its page's block,
+                            // the chunks are pg_box rows apart, and the two 8-key row groups
+                            // 1 KiB apart within a page, or a page block apart for 8-slot pages)
+                            const int lg = PAGED ? __ffs(a.pg_box) - 1 : 7;  // log2 of the page box (a power of 2)
+                            const uint32_t v_lbo = 128u << lg;
+                            const uint32_t v_sbo = lg < 4 ? 256u << lg : 1024u;
 #pragma unroll
                             for (int kk = 0; kk < BN / 16; ++kk) {
-                                const uint64_t db = tc::smem_desc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
+                                const uint32_t va = PAGED ? vb + ((uint32_t)((kk * 16) >> lg) << (lg + 8)) +
+                                                                ((uint32_t)((kk * 16) & ((1 << lg) - 1)) << 7)
+                                                          : vb + kk * 16 * 128;
+                                const uint64_t db = tc::smem_desc_sw128(va, v_lbo, v_sbo);
                                 tc::mma_f16_ts_pair(tm_o, tm_s + (uint32_t)(gi & 1) * BN + kk * 8, db, idesc_pv,
                                                     (i | kk) != 0);
                             }
@@ -2236,6 +2245,23 @@ bool make_paged_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, in
     return r == CUDA_SUCCESS;
 }
 
+// A 5-D tiled map over a V page pool for page-major stages: {64 columns, page slots, the
+// head_dim / 64 column chunks, kv heads, pages} with element strides (ts, 64, hs, ps); a box is
+// box_rows slots x 2 chunks of one head and one page, 128-byte swizzle, so that its
+// shared-memory image is [2 chunks][box_rows][64 columns].
+bool make_paged_v_chunk_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int d, int hk,
+                            int page_size, int num_pages, int64_t hs, int64_t ts, int64_t ps, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[5] = {64, (cuuint64_t)page_size, (cuuint64_t)(d / 64), (cuuint64_t)hk, (cuuint64_t)num_pages};
+    cuuint64_t strides[4] = {(cuuint64_t)ts * 2, 128, (cuuint64_t)hs * 2, (cuuint64_t)ps * 2};
+    cuuint32_t box[5] = {64, (cuuint32_t)box_rows, 2, 1, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, dt, 5, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, class KV, bool PAIR, int MODE = kMaskMode>
 cudaError_t run_attn(const AttnArgs &a, const CUtensorMap *maps, int units, int tiles,
                      cudaStream_t stream) {
@@ -2407,9 +2433,13 @@ cudaError_t launch_paged_prefill(const PagedPrefillProblem &p, void *workspace, 
                         p.head_stride, p.token_stride, p.page_stride, a.pg_box, dim_v))
         return cudaErrorInvalidValue;
     for (int i = 0; i < 3; ++i) a.pg_dim[i] = dim_k[i];
-    // CTA pairs: V pages one row high, for the box that holds a sequence's context end
-    if (pl.pair && !make_paged_map(&maps[4], p.v_pool, kvt, p.head_dim, p.n_kv_heads, p.page_size,
-                                   p.num_pages, p.head_stride, p.token_stride, p.page_stride, 1, dim_v))
+    // CTA pairs: V in page-major stages (one box per page for both of a CTA's column
+    // chunks), and V pages one row high, for the box that holds a sequence's context end
+    if (pl.pair && (!make_paged_v_chunk_map(&maps[1], p.v_pool, kvt, p.head_dim, p.n_kv_heads, p.page_size,
+                                            p.num_pages, p.head_stride, p.token_stride, p.page_stride,
+                                            a.pg_box) ||
+                    !make_paged_map(&maps[4], p.v_pool, kvt, p.head_dim, p.n_kv_heads, p.page_size,
+                                    p.num_pages, p.head_stride, p.token_stride, p.page_stride, 1, dim_v)))
         return cudaErrorInvalidValue;
     a.pair = pl.pair ? 1 : 0;
     // f32 Q in by TMA and O out by TMA for one head's 128-token tiles
