@@ -11,9 +11,11 @@
 // part of this library: the rows arrive ready.
 //
 // Design (HBM-bound; each element is read once as f32 and written once as
-// 16 bits, for K and for V): one warp per new token.  The lanes take
-// consecutive 8-element chunks of the token's row (all KV heads), up to four
-// each per round with every load issued before the token's slot is looked up,
+// 16 bits, for K and for V): one warp per new token, a batch's tokens in one
+// wave where they fit (two 8-element chunks a lane per round keep a lane at 58
+// registers, so that four blocks of 8 warps fit an SM: 4864 tokens at once on
+// 152 SMs).  The lanes take consecutive chunks of the token's row (all KV
+// heads), every load of a round issued before the token's slot is looked up,
 // so that the lookup's chain of dependent reads (the token's sequence by binary
 // search over token_offsets, its start position, its page) is paid once per
 // token while its data are in flight.  Reads are coalesced 32-byte pieces;
@@ -33,10 +35,10 @@ struct AppendArgs {
     int32_t *status;
 };
 
-constexpr int kChunksPerLane = 4;  // chunks a lane moves per round, loads all in flight
+constexpr int kChunksPerLane = 2;  // chunks a lane moves per round, loads all in flight
 
 template <class KV>
-__global__ void __launch_bounds__(256) page_append_kernel(const AppendArgs a) {
+__global__ void __launch_bounds__(256, 4) page_append_kernel(const AppendArgs a) {
     const int lane = threadIdx.x & 31;
     const int warps_per_block = blockDim.x >> 5;
     const int row_chunks = a.n_kv_heads * a.chunks;  // 8-element chunks of a token's row
@@ -131,9 +133,9 @@ cudaError_t launch_paged_append(const PagedAppendProblem &p, cudaStream_t stream
     a.num_pages = p.num_pages;
     a.max_pages = p.max_pages_per_seq;
     a.status = p.status;
-    // one warp per token, one wave: 8 resident blocks of 8 warps per SM
+    // one warp per token, one wave: 4 resident blocks of 8 warps per SM
     int64_t blocks = ((int64_t)p.total_tokens + 7) / 8;
-    const int64_t cap = (int64_t)sm_count() * 8;
+    const int64_t cap = (int64_t)sm_count() * 4;
     if (blocks > cap) blocks = cap;
     timing_mark(true, stream);
     if (p.kv_dtype == GQA_DTYPE_BF16)

@@ -55,9 +55,12 @@ def _bits(t):
 
 @pytest.mark.parametrize("kv", ["f16", "bf16"])
 @pytest.mark.parametrize("head_major", [False, True])
-def test_append_is_bit_exact(lib, kv, head_major):
-    c = workloads.paged_chunk(num_seqs=6, tokens_hi=70, prefix_hi=200, head_dim=128, kv_dtype=kv,
-                              seed=11)
+@pytest.mark.parametrize("hk,d", [(2, 128), (8, 256), (1, 2048)])
+def test_append_is_bit_exact(lib, kv, head_major, hk, d):
+    """Rows of 256 elements (one round of loads per token) and of 2048 elements, over
+    eight heads or one (four rounds per token), bit for bit against the oracle."""
+    c = workloads.paged_chunk(num_seqs=6, tokens_hi=70, prefix_hi=200, n_heads=hk, n_kv_heads=hk,
+                              head_dim=d, kv_dtype=kv, seed=11)
     kp, vp, st = _append_gpu(lib, c, head_major)
     assert st == 0
     rk, rv, skipped = oracle.paged_append(c.k_new, c.v_new, c.token_offsets, c.position_start,
