@@ -98,6 +98,12 @@ CASES = [
     # split between the two CTAs, value rows past each context end zeroed row by row
     (4, (257, 384), (0, 1000), 16, 4, 256, 16, "f16", False),
     (8, (257, 300), (0, 500), 8, 2, 256, 32, "bf16", True),
+    # CTA pairs (192 query tiles: no key splits) with page boxes of 8, 16 (48-slot pages)
+    # and 64 slots: eight, four and one box per CTA half of a K tile; value stages of 8,
+    # 16 and 64 rows a page
+    (4, (257, 330), (0, 600), 16, 2, 256, 8, "f16", False),
+    (4, (257, 330), (0, 600), 16, 2, 256, 48, "bf16", False),
+    (4, (257, 330), (0, 700), 16, 2, 256, 64, "f16", True),
 ]
 
 
