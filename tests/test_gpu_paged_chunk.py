@@ -281,3 +281,35 @@ def test_chunked_prefill_page_relabelling_is_bit_identical(lib):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     assert torch.equal(o1, o2)
+
+
+def test_chunked_prefill_pair_edge_cases(lib):
+    """CTA pairs (head_dim 256, 16 query heads over 2 KV heads, up to 300 rows: 192 query
+    tiles): a sequence with no new token and one with a single token at position 0 beside
+    two long ones whose contexts end inside a page, against the oracle."""
+    import torch
+    from gpu_helpers import assert_attention_close, dev, new_status
+    c = workloads.paged_chunk(num_seqs=4, tokens_lo=260, tokens_hi=300, prefix_lo=0, prefix_hi=400,
+                              num_pages=4 * 27 + 5, page_size=16, n_heads=16, n_kv_heads=2,
+                              head_dim=256, seed=51)
+    toks = np.diff(c.token_offsets).astype(np.int64)
+    toks[1], toks[2] = 0, 1
+    offs = np.concatenate([[0], np.cumsum(toks)]).astype(np.int32)
+    ps = c.position_start.copy()
+    ps[2] = 0
+    assert (ps[0] + toks[0]) % 16 and (ps[3] + toks[3]) % 16  # contexts end inside a page
+    T = int(offs[-1])
+    q, kn, vn = c.q[:T], c.k_new[:T], c.v_new[:T]
+    kp, vp = _pool_dev(c.k_pool, "f16"), _pool_dev(c.v_pool, "f16")
+    st = new_status()
+    lib.gqa_paged_append(dev(kn), dev(vn), dev(offs), dev(ps), dev(c.page_table), kp, vp, status=st)
+    out = lib.gqa_attn_paged_prefill(dev(q), kp, vp, dev(c.page_table), dev(offs), dev(ps),
+                                     int(toks.max()), c.scale, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rk, rv, skipped = oracle.paged_append(kn, vn, offs, ps, c.page_table, c.k_pool, c.v_pool,
+                                          kv_dtype="f16", **_strides(c))
+    assert skipped == 0
+    ref = oracle.paged_prefill(q, rk, rv, c.page_table, offs, ps, kv_dtype="f16",
+                               n_kv_heads=c.n_kv_heads, scale=c.scale, **_strides(c))
+    assert_attention_close(out.cpu().numpy(), ref, "chunked prefill pair edges")
